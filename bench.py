@@ -1,0 +1,506 @@
+#!/usr/bin/env python
+"""Benchmark of the FP8 (e4m3) implicit-GEMM conv3d on one GB300, through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
+
+A step is one conv3d_fp8_run (operand packing, the tcgen05 implicit-GEMM kernel and, for
+split-K plans, the ordered reduction) over one batch of seeded synthetic e4m3 inputs already
+resident in HBM. The default workload is the largest single-GPU layer of the five (1x256x17x90x160
+-> 256 channels, 3x3x3, stride 1, pad 1: 866 GFLOP); ``--config`` picks another.
+
+Metric: TFLOP/s, FLOP = 2 * N*Do*Ho*Wo * K * C*T*R*S (padding taps counted). L2 is flushed
+between steps by a 2x-L2-sized write that lies outside the per-step CUDA events.
+
+Multi-GPU: the path needs no exchange, so N GPUs run N independent replicas of the same workload
+(weak scaling); ranks meet only at the barriers that bracket the timed region, and the slowest
+rank's time is the job's time.
+
+``--impl reference`` times the CPU oracle (fp64, OpenMP) on rank 0 on bounded samples of the
+same workload; the other ranks exit without work.
+
+Prints exactly one JSON line on stdout (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_CONFIG = 4
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+MAIN_KERNEL_SOURCES = ["conv_tc.cu", "ptx.cuh", "conv3d_fp8_internal.h"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------------------------- problem math
+def problem_figures(shape):
+    Do = (shape.D + 2 * shape.pad[0] - shape.T) // shape.stride[0] + 1
+    Ho = (shape.H + 2 * shape.pad[1] - shape.R) // shape.stride[1] + 1
+    Wo = (shape.W + 2 * shape.pad[2] - shape.S) // shape.stride[2] + 1
+    npq = shape.N * Do * Ho * Wo
+    kg = shape.C * shape.T * shape.R * shape.S
+    flop = 2.0 * npq * shape.K * kg
+    x_bytes = shape.N * shape.C * shape.D * shape.H * shape.W
+    w_bytes = shape.K * kg
+    y_bytes = 2 * npq * shape.K
+    return {"Do": Do, "Ho": Ho, "Wo": Wo, "npq": npq, "k_gemm": kg, "flop": flop,
+            "x_bytes": x_bytes, "w_bytes": w_bytes, "y_bytes": y_bytes,
+            "alg_bytes": x_bytes + w_bytes + y_bytes}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def main_kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in MAIN_KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "fp8_implicit_gemm_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """DRAM bytes per launch of the main kernel from a committed ncu summary, if that summary was
+    taken on the current kernel source for this workload (line: ``bench-traffic: {json}``)."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    want = main_kernel_source_hash()
+    for name in sorted(os.listdir(pdir)):
+        if not name.endswith((".md", ".txt")):
+            continue
+        with open(os.path.join(pdir, name)) as f:
+            for line in f:
+                if line.startswith("bench-traffic:"):
+                    try:
+                        d = json.loads(line.split(":", 1)[1])
+                    except ValueError:
+                        continue
+                    if d.get("workload") == workload and d.get("source_sha256") == want:
+                        return d.get("dram_bytes_per_launch")
+    return None
+
+
+# --------------------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id is not None:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self, min_samples: int = 2, wait_s: float = 1.0):
+        if self.proc is None:
+            return
+        t0 = time.time()
+        while len(self.lines) < min_samples and time.time() - t0 < wait_s:
+            time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.lines:
+            return None
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def gpu_query_id(torch, dev: int):
+    try:
+        props = torch.cuda.get_device_properties(dev)
+        bus = getattr(props, "pci_bus_id", None)
+        dom = getattr(props, "pci_domain_id", 0)
+        pdev = getattr(props, "pci_device_id", 0)
+        if bus is not None:
+            return f"{dom:08x}:{bus:02x}:{pdev:02x}.0"
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if dev < len(ids):
+            return ids[dev]
+    return str(dev)
+
+
+# --------------------------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class Dist:
+    def __init__(self, backend: str):
+        import torch.distributed as dist
+        self.dist = dist
+        self.world, self.rank, self.local = dist_env()
+        self.on = self.world > 1
+        if self.on and not dist.is_initialized():
+            dist.init_process_group(backend=backend)
+
+    def barrier(self):
+        if self.on:
+            self.dist.barrier()
+
+    def max(self, v: float, device=None) -> float:
+        if not self.on:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.on and self.dist.is_initialized():
+            self.dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------- CPU baseline
+def cpu_oracle_sample(inp, shape, target_s: float, seed: int, min_points: int = 256):
+    """Time the oracle on a random sample of outputs sized to about target_s seconds."""
+    import numpy as np
+    import oracle
+    fig = problem_figures(shape)
+    total = shape.K * fig["npq"]
+    x, w = inp["x"].numpy(), inp["w"].numpy()
+    rng = np.random.default_rng(seed)
+    n = min_points
+    t = 0.0
+    while True:
+        idx = rng.integers(0, total, n)
+        t0 = time.perf_counter()
+        oracle.conv3d_fp8_points(x, w, inp["sx"], inp["sw"], idx, shape.stride, shape.pad)
+        t = time.perf_counter() - t0
+        if t >= target_s * 0.5 or n >= total:
+            break
+        n = int(min(total, max(n * 2, n * target_s / max(t, 1e-3))))
+    flop = 2.0 * fig["k_gemm"] * n
+    return {"value": flop / t / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "seconds": round(t, 3),
+            "sample": f"{n} random outputs of {total} (fp64 direct sum, one by one)"}
+
+
+# ----------------------------------------------------------------------------------------- ours
+def run_ours(args):
+    import numpy as np
+    import torch
+    from fp8_implicit_gemm_gb300 import build, capi, synth
+
+    dist = Dist("nccl")
+    torch.cuda.set_device(dist.local)
+    dev = torch.cuda.current_device()
+    build.build()
+    shape = synth.CONFIGS[args.config]
+    fig = problem_figures(shape)
+    inp = synth.make_config_inputs(args.config)
+
+    plan = capi.conv3d_fp8_plan(shape.N, shape.C, shape.D, shape.H, shape.W, shape.K, shape.T,
+                                shape.R, shape.S, shape.stride, shape.pad, dev)
+    info = capi.conv3d_fp8_get_info(plan)
+    stream = torch.cuda.current_stream()
+    x = inp["x"].to(dev)
+    w = inp["w"].to(dev)
+    sx = torch.tensor([inp["sx"]], dtype=torch.float32, device=dev)
+    sw = torch.tensor([inp["sw"]], dtype=torch.float32, device=dev)
+    y = torch.full((shape.N, shape.K, fig["Do"], fig["Ho"], fig["Wo"]), float("nan"),
+                   dtype=torch.bfloat16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    launches_per_step = 2 + (1 if info["splits"] > 1 else 0)
+
+    def step():
+        capi.conv3d_fp8_run(plan, x, w, sx, sw, y, shape.stride, shape.pad, stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    if torch.isnan(y).any().item():
+        raise RuntimeError("outputs left unwritten after warm-up")
+    capi.conv3d_fp8_check(plan)
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    for e in ev:  # materialise the lazily created events before they are handed to the library
+        for x_ in e:
+            x_.record()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_query_id(torch, dev))
+    sampler.start()
+    time.sleep(0.3)
+    dist.barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_(i & 0xFF)
+        s0, s1, k0, k1 = ev[i]
+        capi.conv3d_fp8_set_timing_events(plan, k0, k1)
+        s0.record(stream)
+        step()
+        s1.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    sampler.stop()
+    capi.conv3d_fp8_set_timing_events(plan, None, None)
+    if capi.conv3d_fp8_check(plan) != capi.CONV3D_OK:
+        raise RuntimeError("a kernel reported a timed-out wait")
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    kern_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    total_ms = dist.max(sum(step_ms), dev)
+    mean_step_ms = total_ms / K
+    mean_kern_ms = statistics.mean(kern_ms)
+    value = fig["flop"] * K * dist.world / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end through the public C-ABI call with host buffers
+    x_h = inp["x"].pin_memory()
+    w_h = inp["w"].pin_memory()
+    s_h = torch.tensor([inp["sx"], inp["sw"]], dtype=torch.float32).pin_memory()
+    s_d = torch.empty(2, dtype=torch.float32, device=dev)
+    y_h = torch.empty(y.shape, dtype=torch.bfloat16).pin_memory()
+    e2e_steps = max(3, min(K, 200))
+    for _ in range(3):
+        x.copy_(x_h, non_blocking=True)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e_start = torch.cuda.Event(enable_timing=True)
+    e_stop = torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for i in range(e2e_steps):
+        x.copy_(x_h, non_blocking=True)
+        w.copy_(w_h, non_blocking=True)
+        s_d.copy_(s_h, non_blocking=True)
+        capi.conv3d_fp8_run(plan, x, w, s_d[0:1], s_d[1:2], y, shape.stride, shape.pad, stream)
+        y_h.copy_(y, non_blocking=True)
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = dist.max(e_start.elapsed_time(e_stop) / e2e_steps, dev)
+    dist.barrier()
+    if torch.isnan(y_h.float()).any().item():
+        raise RuntimeError("e2e result has unwritten outputs")
+    e2e = {"value": fig["flop"] * dist.world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+           "ms_per_step": round(e2e_ms, 4),
+           "h2d_bytes_per_step": int(x_h.numel() + w_h.numel() + 4 * s_h.numel()),
+           "d2h_bytes_per_step": int(2 * y_h.numel())}
+
+    # ---- roofline of the dominant kernel (the implicit-GEMM kernel)
+    peaks, peaks_kind = load_peaks()
+    fp8_peak = FP8_PER_BF16 * float(peaks["bf16_tflops"])
+    hbm_peak = float(peaks["hbm_gbs"])
+    t_flop = fig["flop"] / (fp8_peak * 1e12)
+    t_hbm = fig["alg_bytes"] / (hbm_peak * 1e9)
+    workload = shape.name
+    traffic = committed_traffic(workload)
+    if t_flop >= t_hbm:
+        achieved = fig["flop"] / (mean_kern_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak, 1),
+                "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
+                "peak_source": f"{peaks_kind} bf16 burst x {FP8_PER_BF16:g} (nominal fp8/bf16)"}
+    else:
+        achieved = fig["alg_bytes"] / (mean_kern_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": round(hbm_peak, 1),
+                "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                "peak_source": f"{peaks_kind} copy bandwidth"}
+    roof["traffic"] = traffic
+    roof["kernel"] = "conv3d_fp8_tc_kernel"
+    roof["kernel_ms"] = round(mean_kern_ms, 5)
+    roof["alg_flop"] = fig["flop"]
+    roof["alg_bytes"] = fig["alg_bytes"]
+    roof["step_roofline_frac"] = round(max(t_flop, t_hbm) / (mean_step_ms * 1e-3), 4)
+
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(inp, shape, args.cpu_seconds, seed=7)
+
+    clocks = sampler.summary()
+    capi.conv3d_fp8_destroy(plan)
+    out = {
+        "metric": "conv3d fp8 TFLOP/s and % of FP8/HBM roofline at 1 GB300",
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": dist.world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(mean_step_ms, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3",
+        "data": "synthetic (seeded N(0,1) inputs quantised to e4m3 per tensor)",
+        "config": {"workload": workload, "N": shape.N, "C": shape.C, "D": shape.D, "H": shape.H,
+                   "W": shape.W, "K": shape.K, "filter": [shape.T, shape.R, shape.S],
+                   "stride": list(shape.stride), "pad": list(shape.pad), "npq": fig["npq"],
+                   "gflop_per_step": round(fig["flop"] / 1e9, 3),
+                   "plan": {k: info[k] for k in ("block_n", "m_tiles", "n_tiles", "splits",
+                                                 "stages", "grid", "row_chk")},
+                   "l2": f"flushed between steps ({flush.numel() >> 20} MiB write outside the "
+                         "per-step events)",
+                   "parallelism": f"replicas x{dist.world}"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    if dist.rank == 0:
+        print(json.dumps(out), flush=True)
+    dist.close()
+
+
+# ------------------------------------------------------------------------------------ reference
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from fp8_implicit_gemm_gb300 import synth
+
+    oracle.build()
+    shape = synth.CONFIGS[args.config]
+    fig = problem_figures(shape)
+    inp = synth.make_config_inputs(args.config)
+    x, w = inp["x"].numpy(), inp["w"].numpy()
+    total = shape.K * fig["npq"]
+    rng = np.random.default_rng(11)
+    # size each step so that warm-up + timed steps take about args.ref_seconds in total
+    probe = rng.integers(0, total, 512)
+    t0 = time.perf_counter()
+    oracle.conv3d_fp8_points(x, w, inp["sx"], inp["sw"], probe, shape.stride, shape.pad)
+    rate = 512 / max(time.perf_counter() - t0, 1e-6)
+    per_step = max(32, int(rate * args.ref_seconds / max(1, args.steps + args.warmup)))
+    per_step = min(per_step, total)
+    for _ in range(args.warmup):
+        oracle.conv3d_fp8_points(x, w, inp["sx"], inp["sw"], rng.integers(0, total, per_step),
+                                 shape.stride, shape.pad)
+    times = []
+    for _ in range(args.steps):
+        idx = rng.integers(0, total, per_step)
+        t0 = time.perf_counter()
+        oracle.conv3d_fp8_points(x, w, inp["sx"], inp["sw"], idx, shape.stride, shape.pad)
+        times.append(time.perf_counter() - t0)
+    flop = 2.0 * fig["k_gemm"] * per_step
+    ms = 1e3 * statistics.mean(times)
+    value = flop * len(times) / sum(times) / 1e12
+    sample = f"{per_step} random outputs of {total} per step (fp64 direct sum, one by one)"
+    out = {
+        "impl": "reference",
+        "metric": "conv3d fp8 TFLOP/s and % of FP8/HBM roofline at 1 GB300",
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) inputs quantised to e4m3 per tensor)",
+        "config": {"workload": shape.name, "N": shape.N, "C": shape.C, "D": shape.D,
+                   "H": shape.H, "W": shape.W, "K": shape.K,
+                   "filter": [shape.T, shape.R, shape.S], "stride": list(shape.stride),
+                   "pad": list(shape.pad), "npq": fig["npq"],
+                   "parallelism": "rank 0 only (CPU oracle)"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, _, _ = dist_env()
+    if world != args.gpus:
+        log(f"note: --gpus {args.gpus} but WORLD_SIZE={world}; using WORLD_SIZE")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,404 @@
+// api.cu -- the C ABI declared in include/conv3d_fp8.h: planning, validation and launch.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "conv3d_fp8.h"
+#include "conv3d_fp8_internal.h"
+
+using namespace c3d;
+
+struct conv3d_fp8_plan_s {
+  int device = -1;
+  int stride[3] = {0, 0, 0};
+  int pad[3] = {0, 0, 0};
+  ConvParams p{};
+  CUtensorMap wmap{};
+  conv3d_fp8_plan_info info{};
+  void* workspace = nullptr;
+  cudaEvent_t ev_begin = nullptr;  // measurement hook, caller-owned
+  cudaEvent_t ev_end = nullptr;
+};
+
+namespace {
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000ull * 1000ull * 1000ull;
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+long long round_up(long long a, long long b) { return ceil_div(a, b) * b; }
+
+int out_dim(int in, int k, int stride, int pad) {
+  const long long span = (long long)in + 2LL * pad - k;
+  if (stride <= 0 || span < 0) return 0;
+  return (int)(span / stride + 1);
+}
+
+int next_pow2(int v) {
+  int r = 1;
+  while (r < v) r <<= 1;
+  return r;
+}
+
+struct Layout {
+  size_t xp_off, xp_bytes, wp_off, wp_bytes, part_off, part_bytes, status_off, total;
+};
+
+// Validation and every tiling decision, with no device access.
+conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int S,
+                     const int stride[3], const int pad[3], int sm_count,
+                     const conv3d_fp8_options* opts, conv3d_fp8_plan_info* info, ConvParams* pp,
+                     Layout* lay) {
+  if (!stride || !pad || !info) return CONV3D_EINVAL;
+  if (N <= 0 || C <= 0 || D <= 0 || H <= 0 || W <= 0 || K <= 0 || T <= 0 || R <= 0 || S <= 0)
+    return CONV3D_EINVAL;
+  for (int i = 0; i < 3; ++i)
+    if (stride[i] <= 0 || pad[i] < 0) return CONV3D_EINVAL;
+  if (sm_count <= 0) return CONV3D_EINVAL;
+  const int Do = out_dim(D, T, stride[0], pad[0]);
+  const int Ho = out_dim(H, R, stride[1], pad[1]);
+  const int Wo = out_dim(W, S, stride[2], pad[2]);
+  if (Do <= 0 || Ho <= 0 || Wo <= 0) return CONV3D_EINVAL;
+  if (C % 16 != 0) return CONV3D_EUNSUPPORTED;
+
+  const long long dhw = (long long)Do * Ho * Wo;
+  const long long npq = (long long)N * dhw;
+  const long long taps = (long long)T * R * S;
+  const long long kg = taps * C;
+  const long long Dp = D + 2LL * pad[0], Hp = H + 2LL * pad[1], Wp = W + 2LL * pad[2];
+  const long long y_elems = npq * K;
+  const long long x_elems = (long long)N * C * D * H * W;
+  const long long xp_elems = (long long)N * Dp * Hp * Wp * C;
+  // 32-bit limits of the index arithmetic inside the kernels.
+  if (npq + kBlockM >= (1LL << 31) || kg + kBlockK >= (1LL << 31) || y_elems >= (1LL << 40) ||
+      x_elems >= (1LL << 40) || xp_elems >= (1LL << 40) || Dp >= (1LL << 30) ||
+      Hp >= (1LL << 30) || Wp >= (1LL << 30) || K >= (1 << 30) || taps >= (1 << 20))
+    return CONV3D_EUNSUPPORTED;
+
+  conv3d_fp8_options o{};
+  if (opts) o = *opts;
+  int block_n = o.block_n;
+  if (block_n == 0) block_n = (int)std::min<long long>(256, round_up(K, 32));
+  if (block_n < 32 || block_n > 256 || block_n % 32 != 0) return CONV3D_EINVAL;
+
+  const long long m_tiles = ceil_div(npq, kBlockM);
+  const long long n_tiles = ceil_div(K, block_n);
+  const long long k_blocks = ceil_div(kg, kBlockK);
+  const long long tiles = m_tiles * n_tiles;
+  long long splits = o.splits;
+  if (splits < 0) return CONV3D_EINVAL;
+  if (splits == 0) {
+    splits = 1;
+    if (tiles * 2 <= sm_count && k_blocks >= 8)
+      splits = std::max<long long>(1, std::min<long long>(sm_count / tiles, k_blocks / 4));
+  }
+  splits = std::min(splits, k_blocks);
+  const long long kbps = ceil_div(k_blocks, splits);
+  splits = ceil_div(k_blocks, kbps);  // every split owns at least one K block
+  const long long units = tiles * splits;
+  if (units >= (1LL << 31)) return CONV3D_EUNSUPPORTED;
+
+  const long long stage_bytes = kATileBytes + (long long)block_n * kBlockK;
+  const int stages = (int)std::min<long long>(kMaxStages, kSmemBudget / stage_bytes);
+  if (stages < 3) return CONV3D_EUNSUPPORTED;
+  long long grid = std::min<long long>(units, sm_count);
+  if (o.max_ctas > 0) grid = std::min<long long>(grid, o.max_ctas);
+  if (o.max_ctas < 0 || o.wait_timeout_ms < 0) return CONV3D_EINVAL;
+
+  Layout L{};
+  L.xp_off = 0;
+  L.xp_bytes = (size_t)xp_elems;
+  L.wp_off = (size_t)round_up((long long)L.xp_off + L.xp_bytes, 256);
+  L.wp_bytes = (size_t)(K * kg);
+  L.part_off = (size_t)round_up((long long)L.wp_off + L.wp_bytes, 256);
+  L.part_bytes = splits > 1 ? (size_t)(tiles * splits * block_n * kBlockM * 4) : 0;
+  L.status_off = (size_t)round_up((long long)L.part_off + L.part_bytes, 256);
+  L.total = L.status_off + 256;
+
+  std::memset(info, 0, sizeof(*info));
+  info->Do = Do;
+  info->Ho = Ho;
+  info->Wo = Wo;
+  info->npq = npq;
+  info->k_gemm = (int)kg;
+  info->block_m = kBlockM;
+  info->block_n = block_n;
+  info->m_tiles = (int)m_tiles;
+  info->n_tiles = (int)n_tiles;
+  info->k_blocks = (int)k_blocks;
+  info->splits = (int)splits;
+  info->k_blocks_per_split = (int)kbps;
+  info->stages = stages;
+  info->row_chk = (npq % kBlockM) != 0;
+  info->grid = (int)grid;
+  info->sm_count = sm_count;
+  info->workspace_bytes = L.total;
+
+  if (pp) {
+    ConvParams& p = *pp;
+    std::memset(&p, 0, sizeof(p));
+    p.N = N; p.C = C; p.D = D; p.H = H; p.W = W; p.K = K; p.T = T; p.R = R; p.S = S;
+    p.sd = stride[0]; p.sh = stride[1]; p.sw = stride[2];
+    p.pd = pad[0]; p.ph = pad[1]; p.pw = pad[2];
+    p.Do = Do; p.Ho = Ho; p.Wo = Wo;
+    p.Dp = (int)Dp; p.Hp = (int)Hp; p.Wp = (int)Wp;
+    p.dhw = (int)dhw;
+    p.npq = (int)npq;
+    p.taps = (int)taps;
+    p.kg = (int)kg;
+    p.block_n = block_n;
+    p.m_tiles = (int)m_tiles;
+    p.n_tiles = (int)n_tiles;
+    p.k_blocks = (int)k_blocks;
+    p.splits = (int)splits;
+    p.kb_per_split = (int)kbps;
+    p.num_units = (int)units;
+    p.stages = stages;
+    p.acc_stride = std::max(32, next_pow2(block_n));
+    p.tmem_cols = 2 * p.acc_stride;
+    p.timeout_ns = o.wait_timeout_ms > 0 ? (unsigned long long)o.wait_timeout_ms * 1000000ull
+                                         : kDefaultTimeoutNs;
+    p.debug_flags = o.debug_flags;
+  }
+  if (lay) *lay = L;
+  return CONV3D_OK;
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// The packed weights as a 2D tensor [K rows][kg bytes]; a box is one 128-byte K block of
+// block_n rows, written to shared memory with the 128-byte swizzle the MMA descriptor expects.
+conv3d_status encode_weight_map(CUtensorMap* map, void* wp, int K, int kg, int block_n) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return CONV3D_ECUDA;
+  const cuuint64_t dims[2] = {(cuuint64_t)kg, (cuuint64_t)K};
+  const cuuint64_t strides[1] = {(cuuint64_t)kg};
+  const cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)block_n};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, wp, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV3D_OK : CONV3D_ECUDA;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  cudaError_t set(int dev) {
+    cudaError_t e = cudaGetDevice(&prev);
+    if (e != cudaSuccess) return e;
+    if (prev != dev) {
+      e = cudaSetDevice(dev);
+      changed = (e == cudaSuccess);
+    }
+    return e;
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+conv3d_status conv3d_fp8_describe(int N, int C, int D, int H, int W, int K, int T, int R, int S,
+                                  const int stride[3], const int pad[3], int sm_count,
+                                  const conv3d_fp8_options* opts, conv3d_fp8_plan_info* info) {
+  return decide(N, C, D, H, W, K, T, R, S, stride, pad, sm_count, opts, info, nullptr, nullptr);
+}
+
+conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t* out, int N, int C, int D, int H, int W, int K,
+                                 int T, int R, int S, const int stride[3], const int pad[3],
+                                 int device, const conv3d_fp8_options* opts) {
+  if (!out) return CONV3D_EINVAL;
+  *out = nullptr;
+  // Shape errors first, without touching any device.
+  conv3d_fp8_plan_info probe{};
+  conv3d_status st = decide(N, C, D, H, W, K, T, R, S, stride, pad, 1, opts, &probe, nullptr, nullptr);
+  if (st != CONV3D_OK) return st;
+
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || ndev <= 0) {
+    cudaGetLastError();
+    return CONV3D_ECUDA;
+  }
+  if (device < 0 || device >= ndev) return CONV3D_EINVAL;
+  DeviceGuard guard;
+  if (guard.set(device) != cudaSuccess) return CONV3D_ECUDA;
+  cudaDeviceProp prop{};
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return CONV3D_ECUDA;
+  if (prop.major != 10 || prop.minor != 3) return CONV3D_EUNSUPPORTED;
+
+  conv3d_fp8_plan_s* plan = new (std::nothrow) conv3d_fp8_plan_s();
+  if (!plan) return CONV3D_ENOMEM;
+  Layout L{};
+  st = decide(N, C, D, H, W, K, T, R, S, stride, pad, prop.multiProcessorCount, opts, &plan->info,
+              &plan->p, &L);
+  if (st != CONV3D_OK) {
+    delete plan;
+    return st;
+  }
+  plan->device = device;
+  for (int i = 0; i < 3; ++i) {
+    plan->stride[i] = stride[i];
+    plan->pad[i] = pad[i];
+  }
+  const size_t smem = conv_smem_bytes(plan->p.block_n, plan->p.stages);
+  if ((int)smem > prop.sharedMemPerBlockOptin) {
+    delete plan;
+    return CONV3D_EUNSUPPORTED;
+  }
+  if (conv_set_smem_attr(smem) != cudaSuccess) {
+    delete plan;
+    return CONV3D_ECUDA;
+  }
+  if (cudaMalloc(&plan->workspace, L.total) != cudaSuccess) {
+    cudaGetLastError();
+    delete plan;
+    return CONV3D_ENOMEM;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(plan->workspace);
+  plan->p.xp = ws + L.xp_off;
+  plan->p.wp = ws + L.wp_off;
+  plan->p.partials = L.part_bytes ? reinterpret_cast<float*>(ws + L.part_off) : nullptr;
+  plan->p.status = reinterpret_cast<int*>(ws + L.status_off);
+  if (cudaMemset(plan->p.status, 0, 256) != cudaSuccess) {
+    cudaFree(plan->workspace);
+    delete plan;
+    return CONV3D_ECUDA;
+  }
+  st = encode_weight_map(&plan->wmap, plan->p.wp, K, plan->p.kg, plan->p.block_n);
+  if (st != CONV3D_OK) {
+    cudaFree(plan->workspace);
+    delete plan;
+    return st;
+  }
+  *out = plan;
+  return CONV3D_OK;
+}
+
+conv3d_status conv3d_fp8_plan(conv3d_fp8_plan_t* out, int N, int C, int D, int H, int W, int K,
+                              int T, int R, int S, const int stride[3], const int pad[3],
+                              int device) {
+  return conv3d_fp8_plan_ex(out, N, C, D, H, W, K, T, R, S, stride, pad, device, nullptr);
+}
+
+conv3d_status conv3d_fp8_run(conv3d_fp8_plan_t plan, const void* x, const void* w,
+                             const float* scale_x, const float* scale_w, void* y,
+                             const int stride[3], const int pad[3], void* stream) {
+  if (!plan || !x || !w || !scale_x || !scale_w || !y || !stride || !pad) return CONV3D_EINVAL;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(scale_x, 4) ||
+      !aligned(scale_w, 4))
+    return CONV3D_EINVAL;
+  for (int i = 0; i < 3; ++i)
+    if (stride[i] != plan->stride[i] || pad[i] != plan->pad[i]) return CONV3D_EINVAL;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return CONV3D_ECUDA;
+  if (cur != plan->device) return CONV3D_EINVAL;
+
+  ConvParams p = plan->p;
+  p.x = static_cast<const uint8_t*>(x);
+  p.w = static_cast<const uint8_t*>(w);
+  p.y = static_cast<uint16_t*>(y);
+  p.scale_x = scale_x;
+  p.scale_w = scale_w;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_pack(p, s) != cudaSuccess) return CONV3D_ECUDA;
+  if (plan->ev_begin && cudaEventRecord(plan->ev_begin, s) != cudaSuccess) return CONV3D_ECUDA;
+  if (launch_conv(p, plan->wmap, plan->info.row_chk != 0, plan->info.grid, s) != cudaSuccess)
+    return CONV3D_ECUDA;
+  if (plan->ev_end && cudaEventRecord(plan->ev_end, s) != cudaSuccess) return CONV3D_ECUDA;
+  if (p.splits > 1 && launch_splitk_reduce(p, plan->info.row_chk != 0, s) != cudaSuccess)
+    return CONV3D_ECUDA;
+  return CONV3D_OK;
+}
+
+conv3d_status conv3d_fp8_set_timing_events(conv3d_fp8_plan_t plan, void* ev_begin, void* ev_end) {
+  if (!plan) return CONV3D_EINVAL;
+  plan->ev_begin = static_cast<cudaEvent_t>(ev_begin);
+  plan->ev_end = static_cast<cudaEvent_t>(ev_end);
+  return CONV3D_OK;
+}
+
+conv3d_status conv3d_fp8_check(conv3d_fp8_plan_t plan) {
+  if (!plan) return CONV3D_EINVAL;
+  DeviceGuard guard;
+  if (guard.set(plan->device) != cudaSuccess) return CONV3D_ECUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return CONV3D_ECUDA;
+  int status = 0;
+  if (cudaMemcpy(&status, plan->p.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return CONV3D_ECUDA;
+  if (status != 0) {
+    cudaMemset(plan->p.status, 0, sizeof(int));
+    cudaDeviceSynchronize();
+    return CONV3D_EDEVICE;
+  }
+  return CONV3D_OK;
+}
+
+conv3d_status conv3d_fp8_get_info(conv3d_fp8_plan_t plan, conv3d_fp8_plan_info* info) {
+  if (!plan || !info) return CONV3D_EINVAL;
+  *info = plan->info;
+  return CONV3D_OK;
+}
+
+size_t conv3d_fp8_workspace_size(conv3d_fp8_plan_t plan) {
+  return plan ? plan->info.workspace_bytes : 0;
+}
+
+conv3d_status conv3d_fp8_out_dims(conv3d_fp8_plan_t plan, int* Do, int* Ho, int* Wo) {
+  if (!plan || !Do || !Ho || !Wo) return CONV3D_EINVAL;
+  *Do = plan->info.Do;
+  *Ho = plan->info.Ho;
+  *Wo = plan->info.Wo;
+  return CONV3D_OK;
+}
+
+void conv3d_fp8_destroy(conv3d_fp8_plan_t plan) {
+  if (!plan) return;
+  {
+    DeviceGuard guard;
+    if (guard.set(plan->device) == cudaSuccess) {
+      cudaDeviceSynchronize();
+      cudaFree(plan->workspace);
+    }
+  }
+  delete plan;
+}
+
+const char* conv3d_fp8_strerror(conv3d_status s) {
+  switch (s) {
+    case CONV3D_OK: return "success";
+    case CONV3D_EINVAL: return "invalid argument";
+    case CONV3D_EUNSUPPORTED: return "unsupported problem or device";
+    case CONV3D_ENOMEM: return "device workspace allocation failed";
+    case CONV3D_ECUDA: return "CUDA call failed";
+    case CONV3D_EDEVICE: return "kernel stopped early: a bounded wait ran out of time";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,65 @@
+// conv3d_fp8_internal.h -- what the host launcher and the kernels of the library share.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace c3d {
+
+constexpr int kBlockM = 128;        // rows (output positions) per tile = TMEM lanes
+constexpr int kBlockK = 128;        // K_gemm bytes per pipeline stage (= one 128-byte swizzle row)
+constexpr int kMmaK = 32;           // K of one tcgen05.mma kind::f8f6f4
+constexpr int kATileBytes = kBlockM * kBlockK;  // 16 KB
+constexpr int kNumThreads = 320;    // 4 epilogue warps, 4 A-loader warps, 1 TMA warp, 1 MMA warp
+constexpr int kSmemBudget = 200 * 1024;
+constexpr int kMaxStages = 8;
+
+// Status-word bits recorded by kernels whose bounded waits ran out.
+enum : int {
+  kStatusWaitFull = 1 << 0,       // MMA warp waiting for operands
+  kStatusWaitEmpty = 1 << 1,      // a loader waiting for a free stage
+  kStatusWaitAccFull = 1 << 2,    // epilogue waiting for an accumulator
+  kStatusWaitAccEmpty = 1 << 3,   // MMA warp waiting for the epilogue to drain TMEM
+  kStatusWaitDrain = 1 << 4,      // final drain of outstanding MMAs
+};
+
+struct ConvParams {
+  // problem
+  int N, C, D, H, W, K, T, R, S;
+  int sd, sh, sw, pd, ph, pw;
+  int Do, Ho, Wo;
+  int Dp, Hp, Wp;        // extents of the zero-padded channels-last copy of x
+  int dhw;               // Do*Ho*Wo
+  int npq;               // N*dhw, the M of the GEMM view
+  int taps;              // T*R*S
+  int kg;                // taps*C, the K of the GEMM view
+  // tiling
+  int block_n;           // N tile (multiple of 32, <= 256)
+  int m_tiles, n_tiles, k_blocks, splits, kb_per_split, num_units;
+  int stages;
+  int tmem_cols;         // allocated TMEM columns (power of two)
+  int acc_stride;        // TMEM column offset between the two accumulator buffers
+  // tensors
+  const uint8_t* x;      // e4m3 NCDHW (caller's)
+  const uint8_t* w;      // e4m3 KCTRS (caller's)
+  uint8_t* xp;           // e4m3 [N][Dp][Hp][Wp][C], zero halo (workspace)
+  uint8_t* wp;           // e4m3 [K][taps][C] (workspace)
+  uint16_t* y;           // bf16 NCDHW (caller's)
+  const float* scale_x;
+  const float* scale_w;
+  float* partials;       // fp32 [tile][split][block_n][128] when splits > 1 (workspace)
+  int* status;           // status word (workspace)
+  unsigned long long timeout_ns;
+  int debug_flags;
+};
+
+// Launchers (defined in the .cu files). Each returns the CUDA error of its launch.
+cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream);
+cudaError_t launch_conv(const ConvParams& p, const CUtensorMap& wmap, bool row_chk, int grid,
+                        cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const ConvParams& p, bool row_chk, cudaStream_t stream);
+size_t conv_smem_bytes(int block_n, int stages);
+cudaError_t conv_set_smem_attr(size_t smem_bytes);
+
+}  // namespace c3d

@@ -1,0 +1,327 @@
+// conv_tc.cu -- the implicit-GEMM main kernel: tcgen05 FP8 MMAs with TMEM accumulators.
+//
+// GEMM view (the subject page, "Root cause"): row = output position (npq = N*Do*Ho*Wo rows),
+// col = output channel (K columns), reduction over K_gemm = (tap, channel) of T*R*S*C.
+//
+// One persistent CTA per SM walks a static list of work units (m-tile, n-tile, K-split). Warp roles:
+//   warps 0-3  epilogue: TMEM -> registers, scale, bf16, stores masked on row < npq and col < K
+//              (warp w owns TMEM lanes 32w..32w+31, i.e. rows 32w..32w+31 of the tile)
+//   warps 4-7  A loader: cp.async 16-byte gathers from the zero-padded channels-last input into the
+//              128-byte-swizzled K-major A stage; rows at or past npq are zero-filled
+//   warp 8     B loader: one TMA 2D tile of the packed weights per stage (out-of-range zero fill);
+//              also owns the TMEM allocation
+//   warp 9     MMA issuer: 4 x tcgen05.mma (M=128, N=block_n, K=32) per 128-byte K block
+// Stages are handed over with mbarriers: A-full (128 loader arrivals), B-full (TMA bytes),
+// stage-empty (tcgen05.commit). Two TMEM accumulators let the epilogue of one tile overlap the
+// main loop of the next. Every wait is bounded; a wait that runs out records a status bit and
+// the whole CTA winds down without faulting.
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "conv3d_fp8_internal.h"
+#include "ptx.cuh"
+
+namespace c3d {
+
+constexpr int kLoaderLag = 2;  // cp.async groups kept in flight before a stage is signalled full
+
+struct Unit {
+  int tile, m_tile, n_tile, split, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit decode_unit(const ConvParams& p, int u) {
+  Unit r;
+  r.split = u % p.splits;
+  r.tile = u / p.splits;
+  r.n_tile = r.tile % p.n_tiles;
+  r.m_tile = r.tile / p.n_tiles;
+  r.kb0 = r.split * p.kb_per_split;
+  r.kb1 = min(r.kb0 + p.kb_per_split, p.k_blocks);
+  return r;
+}
+
+// Wait used only while winding down: ignores the abort flag, still bounded.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                           int* status, int code) {
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if ((++spins & 63u) == 0 && globaltimer_ns() - t0 > timeout_ns) {
+      atomicOr(status, code);
+      return;
+    }
+  }
+}
+
+template <bool kRowChk>
+__global__ void __launch_bounds__(kNumThreads, 1)
+    conv3d_fp8_tc_kernel(const __grid_constant__ CUtensorMap wmap, const ConvParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);  // 1024-aligned stages
+
+  const int S = p.stages;
+  const uint32_t b_bytes = (uint32_t)p.block_n * kBlockK;
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + (size_t)S * kATileBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)S * b_bytes);
+  // bars: fullA[S], fullB[S], empty[S], accFull[2], accEmpty[2], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const uint32_t sA_u32 = smem_u32(sA), sB_u32 = smem_u32(sB);
+  const uint32_t bars_u32 = smem_u32(bars);
+  auto fullA = [&](int s) { return bars_u32 + 8u * s; };
+  auto fullB = [&](int s) { return bars_u32 + 8u * (S + s); };
+  auto empty = [&](int s) { return bars_u32 + 8u * (2 * S + s); };
+  auto accFull = [&](int b) { return bars_u32 + 8u * (3 * S + b); };
+  auto accEmpty = [&](int b) { return bars_u32 + 8u * (3 * S + 2 + b); };
+  const uint32_t drain_bar = bars_u32 + 8u * (3 * S + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(fullA(s), 128);
+      mbar_init(fullB(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accFull(b), 1);
+      mbar_init(accEmpty(b), 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
+    tmem_relinquish();
+    if (lane == 0) prefetch_tensormap(&wmap);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const AbortState ab{abort_flag, p.status, p.timeout_ns};
+
+  if (warp < 4) {
+    // ------------------------------------------------------------------------------ epilogue
+    const int e = threadIdx.x;  // tile row == TMEM lane
+    const float scale = __ldg(p.scale_x) * __ldg(p.scale_w);
+    uint32_t tc = 0;
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tc) {
+      const Unit un = decode_unit(p, u);
+      const int buf = tc & 1;
+      if (!wait_bounded(accFull(buf), (tc >> 1) & 1, ab, kStatusWaitAccFull)) break;
+      tc_fence_after();
+      const uint32_t trow = tmem_base + (uint32_t)buf * p.acc_stride + ((uint32_t)(warp * 32) << 16);
+      const int n0 = un.n_tile * p.block_n;
+      if (p.splits == 1) {
+        const int m = un.m_tile * kBlockM + e;
+        const bool row_ok = !kRowChk || m < p.npq;
+        const int n = m / p.dhw;
+        const int pix = m - n * p.dhw;
+        uint16_t* ybase = p.y + (long long)n * p.K * p.dhw + pix;
+        for (int cc = 0; cc < p.block_n; cc += 32) {
+          if (n0 + cc >= p.K) break;  // warp-uniform
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(trow + cc, r);
+          tmem_ld_wait();
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int col = n0 + cc + j;
+              if (col < p.K) {
+                const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(r[j]) * scale);
+                ybase[(long long)col * p.dhw] = *reinterpret_cast<const uint16_t*>(&b);
+              }
+            }
+          }
+        }
+      } else {
+        float* dst = p.partials + ((long long)(un.tile * p.splits + un.split) * p.block_n) * kBlockM + e;
+        for (int cc = 0; cc < p.block_n; cc += 32) {
+          uint32_t r[32];
+          tmem_ld_32x32b_x32(trow + cc, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) __stcg(dst + (long long)(cc + j) * kBlockM, __uint_as_float(r[j]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(accEmpty(buf));
+    }
+  } else if (warp < 8) {
+    // ------------------------------------------------------------------------------ A loader
+    const int pt = threadIdx.x - 128;
+    const int q = pt & 7;    // 16-byte chunk of the 128-byte K block
+    const int rb = pt >> 3;  // rows rb, rb+16, ..., rb+112
+    const uint32_t row_dst = sA_u32 + (uint32_t)rb * 128u + (uint32_t)((q ^ (rb & 7)) << 4);
+    const int RS = p.R * p.S;
+    uint32_t it = 0, signaled = 0;
+    int inflight = 0;
+    bool aborted = false;
+    for (int u = blockIdx.x; u < p.num_units && !aborted; u += gridDim.x) {
+      const Unit un = decode_unit(p, u);
+      long long rowoff[8];
+      bool rowok[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int m = un.m_tile * kBlockM + rb + 16 * i;
+        rowok[i] = !kRowChk || m < p.npq;
+        const int mm = rowok[i] ? m : 0;
+        const int n = mm / p.dhw;
+        const int pix = mm - n * p.dhw;
+        const int wo = pix % p.Wo;
+        const int t2 = pix / p.Wo;
+        const int ho = t2 % p.Ho;
+        const int od = t2 / p.Ho;
+        rowoff[i] = ((((long long)n * p.Dp + od * p.sd) * p.Hp + ho * p.sh) * p.Wp + wo * p.sw) * p.C;
+      }
+      for (int kb = un.kb0; kb < un.kb1; ++kb) {
+        const int stage = it % S;
+        if (!wait_bounded(empty(stage), ((it / S) & 1) ^ 1, ab, kStatusWaitEmpty)) {
+          aborted = true;
+          break;
+        }
+        const int kk = kb * kBlockK + q * 16;
+        const bool kok = kk < p.kg;
+        long long tapoff = 0;
+        if (kok) {
+          const int tap = kk / p.C;
+          const int c = kk - tap * p.C;
+          const int t = tap / RS;
+          const int rs = tap - t * RS;
+          const int r = rs / p.S;
+          const int s = rs - r * p.S;
+          tapoff = (((long long)t * p.Hp + r) * p.Wp + s) * p.C + c;
+        }
+        const uint32_t dst = row_dst + (uint32_t)stage * kATileBytes;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const bool ok = kok && rowok[i];
+          const uint8_t* src = ok ? p.xp + rowoff[i] + tapoff : p.xp;
+          cp_async_16_zfill(dst + (uint32_t)i * 2048u, src, ok ? 16u : 0u);
+        }
+        cp_async_commit();
+        ++it;
+        if (++inflight > kLoaderLag) {
+          cp_async_wait_group<kLoaderLag>();
+          fence_proxy_async_smem();
+          mbar_arrive(fullA(signaled % S));
+          ++signaled;
+          --inflight;
+        }
+      }
+    }
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    if (!aborted) {
+      for (; inflight > 0; --inflight, ++signaled) mbar_arrive(fullA(signaled % S));
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------------------------ B loader
+    if (lane == 0) {
+      uint32_t it = 0;
+      const bool skip_first = (p.debug_flags & 1) != 0;
+      for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        const Unit un = decode_unit(p, u);
+        bool aborted = false;
+        for (int kb = un.kb0; kb < un.kb1; ++kb) {
+          const int stage = it % S;
+          if (!wait_bounded(empty(stage), ((it / S) & 1) ^ 1, ab, kStatusWaitEmpty)) {
+            aborted = true;
+            break;
+          }
+          if (!(skip_first && it == 0)) {
+            mbar_arrive_expect_tx(fullB(stage), b_bytes);
+            tma_load_2d(sB_u32 + (uint32_t)stage * b_bytes, &wmap, fullB(stage), kb * kBlockK,
+                        un.n_tile * p.block_n);
+          }
+          ++it;
+        }
+        if (aborted) break;
+      }
+      // Before the CTA may exit, every weight tile this thread requested must have landed.
+      const uint32_t first = it > (uint32_t)S ? it - (uint32_t)S : 0u;
+      for (uint32_t j = first; j < it; ++j) {
+        if (skip_first && j == 0) continue;
+        wait_drain(fullB(j % S), (j / S) & 1, p.timeout_ns, p.status, kStatusWaitDrain);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = make_idesc_e4m3_f32(kBlockM, (uint32_t)p.block_n);
+      uint32_t it = 0, tc = 0;
+      bool aborted = false;
+      for (int u = blockIdx.x; u < p.num_units && !aborted; u += gridDim.x, ++tc) {
+        const Unit un = decode_unit(p, u);
+        const int buf = tc & 1;
+        if (!wait_bounded(accEmpty(buf), ((tc >> 1) & 1) ^ 1, ab, kStatusWaitAccEmpty)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)buf * p.acc_stride;
+        for (int kb = un.kb0; kb < un.kb1; ++kb) {
+          const int stage = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!wait_bounded(fullA(stage), ph, ab, kStatusWaitFull) ||
+              !wait_bounded(fullB(stage), ph, ab, kStatusWaitFull)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const int rem = p.kg - kb * kBlockK;
+          const int nsteps = rem >= kBlockK ? kBlockK / kMmaK : (rem + kMmaK - 1) / kMmaK;
+          const uint64_t adesc = make_sw128_kmajor_desc(sA_u32 + (uint32_t)stage * kATileBytes);
+          const uint64_t bdesc = make_sw128_kmajor_desc(sB_u32 + (uint32_t)stage * b_bytes);
+          for (int j = 0; j < nsteps; ++j) {
+            // +32 bytes of K per step inside the 128-byte swizzle row: +2 in 16-byte units
+            mma_f8f6f4(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc,
+                       (kb > un.kb0 || j > 0) ? 1u : 0u);
+          }
+          mma_commit(empty(stage));
+          ++it;
+        }
+        if (aborted) break;
+        mma_commit(accFull(buf));
+      }
+      // Every MMA must be complete before TMEM is released.
+      mma_commit(drain_bar);
+      wait_drain(drain_bar, 0, p.timeout_ns, p.status, kStatusWaitDrain);
+    }
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 8) tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
+}
+
+size_t conv_smem_bytes(int block_n, int stages) {
+  return 1024 + (size_t)stages * (kATileBytes + (size_t)block_n * kBlockK) +
+         (size_t)(3 * stages + 5) * 8 + 16;
+}
+
+cudaError_t conv_set_smem_attr(size_t smem_bytes) {
+  cudaError_t e = cudaFuncSetAttribute(conv3d_fp8_tc_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(conv3d_fp8_tc_kernel<false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+}
+
+cudaError_t launch_conv(const ConvParams& p, const CUtensorMap& wmap, bool row_chk, int grid,
+                        cudaStream_t stream) {
+  const size_t smem = conv_smem_bytes(p.block_n, p.stages);
+  if (row_chk)
+    conv3d_fp8_tc_kernel<true><<<grid, kNumThreads, smem, stream>>>(wmap, p);
+  else
+    conv3d_fp8_tc_kernel<false><<<grid, kNumThreads, smem, stream>>>(wmap, p);
+  return cudaGetLastError();
+}
+
+}  // namespace c3d

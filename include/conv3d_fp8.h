@@ -1,0 +1,151 @@
+/*
+ * conv3d_fp8.h -- C ABI of the FP8 (e4m3) implicit-GEMM 3D convolution for one NVIDIA GB300
+ * (sm_103a).
+ *
+ * The operation ("[Fix] conv3d fp8: guard padded M rows in the epilogue store", ROCm/FlyDSL pull
+ * request 969, sections "Problem" and "Root cause"):
+ *
+ *   y[n,k,do,ho,wo] = bf16_rn( sx * sw * sum_{c,t,r,s} x[n, c, do*sd+t-pd, ho*sh+r-ph, wo*sw+s-pw]
+ *                                                     * w[k, c, t, r, s] )
+ *
+ * x holds e4m3 ("float8_e4m3fn") bytes in NCDHW order, w holds e4m3 bytes in KCTRS order, taps
+ * that fall outside the input read zero, and y is bfloat16 in NCDHW order. sx and sw are the
+ * per-tensor fp32 dequantisation scales of x and w. The convolution is evaluated as an implicit
+ * GEMM with M = N*Do*Ho*Wo output positions ("npq"), N_gemm = K output channels and
+ * K_gemm = C*T*R*S, accumulated in fp32 by the tensor cores. M and N are cut into tiles; the rows
+ * and columns that pad the last tiles are never stored: every store is masked on row < npq and on
+ * col < K, which is the guard the page adds so that padded rows can no longer overwrite live
+ * outputs of another column.
+ *
+ * Conventions for every entry point:
+ *   - Returns a conv3d_status. Argument errors are reported before anything is launched.
+ *   - Device pointers are plain CUDA device addresses on the plan's device; the caller owns them.
+ *   - "stream" is a cudaStream_t passed as void*; NULL means the legacy default stream.
+ *   - Nothing here synchronises the device except conv3d_fp8_check and conv3d_fp8_destroy.
+ */
+#ifndef CONV3D_FP8_H
+#define CONV3D_FP8_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct conv3d_fp8_plan_s *conv3d_fp8_plan_t; /* opaque, owned by the library */
+
+typedef enum {
+    CONV3D_OK = 0,
+    CONV3D_EINVAL = 1,       /* bad argument: NULL or misaligned pointer, non-positive or empty
+                                shape, stride/pad that differ from the plan, wrong current device */
+    CONV3D_EUNSUPPORTED = 2, /* a valid convolution this library does not handle: C % 16 != 0,
+                                a device that is not sm_103, sizes beyond 32-bit index ranges */
+    CONV3D_ENOMEM = 3,       /* the plan's device workspace could not be allocated */
+    CONV3D_ECUDA = 4,        /* a CUDA runtime or driver call failed (e.g. a launch error) */
+    CONV3D_EDEVICE = 5       /* a kernel reported an error through the plan's status word: one of
+                                its bounded waits ran out of time and the kernel stopped early */
+} conv3d_status;
+
+/* Optional planning knobs. Zero-initialise and set only what you need. */
+typedef struct {
+    int splits;          /* 0: the library chooses; >= 1: split K_gemm into this many slices
+                            (clamped to the number of 128-wide K blocks) */
+    int block_n;         /* 0: the library chooses; else the N tile, a multiple of 32 in [32,256] */
+    int max_ctas;        /* 0: one persistent CTA per SM; else an upper bound on the grid */
+    int wait_timeout_ms; /* 0: 2000 ms; a bounded wait inside a kernel gives up after this long,
+                            records CONV3D_EDEVICE in the status word and the kernel exits */
+    int debug_flags;     /* test-only: bit 0 makes the weight-tile loader skip its first arrival,
+                            so the MMA warp's bounded wait must run out (exercises the error
+                            path without faulting anything) */
+} conv3d_fp8_options;
+
+/* What a plan (or a would-be plan) decided. */
+typedef struct {
+    int Do, Ho, Wo;           /* output extents: floor((in + 2*pad - filter) / stride) + 1 */
+    long long npq;            /* M = N*Do*Ho*Wo */
+    int k_gemm;               /* C*T*R*S */
+    int block_m, block_n;     /* tile of the GEMM view (block_m is always 128) */
+    int m_tiles, n_tiles;     /* ceil(npq / block_m), ceil(K / block_n) */
+    int k_blocks;             /* ceil(k_gemm / 128) */
+    int splits;               /* K slices; > 1 means the split-K path (fp32 partials + reduce) */
+    int k_blocks_per_split;
+    int stages;               /* shared-memory pipeline depth */
+    int row_chk;              /* 1 when npq % block_m != 0: the row guard is compiled in */
+    int grid;                 /* persistent CTAs launched by the main kernel */
+    int sm_count;
+    size_t workspace_bytes;   /* device workspace the plan owns */
+} conv3d_fp8_plan_info;
+
+/*
+ * Plan a convolution for one shape on `device` (a CUDA ordinal).
+ *   N,C,D,H,W: input extents (NCDHW); K: output channels; T,R,S: filter extents.
+ *   stride[3], pad[3]: per axis (d, h, w); zero padding, dilation 1, one group.
+ * Allocates the plan and its device workspace (packed operands, split-K partials, the status
+ * word). Errors: EINVAL (bad shape, empty output), EUNSUPPORTED (C % 16 != 0, not sm_103, index
+ * ranges beyond 32 bits), ENOMEM, ECUDA. On error *plan is set to NULL.
+ */
+conv3d_status conv3d_fp8_plan(conv3d_fp8_plan_t *plan, int N, int C, int D, int H, int W, int K,
+                              int T, int R, int S, const int stride[3], const int pad[3],
+                              int device);
+
+/* As conv3d_fp8_plan, with planning knobs (opts may be NULL). */
+conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t *plan, int N, int C, int D, int H, int W,
+                                 int K, int T, int R, int S, const int stride[3],
+                                 const int pad[3], int device, const conv3d_fp8_options *opts);
+
+/*
+ * Run the planned convolution, asynchronously on `stream`.
+ *   x_ncdhw: N*C*D*H*W e4m3 bytes, contiguous, 16-byte aligned.
+ *   w_kctrs: K*C*T*R*S e4m3 bytes, contiguous, 16-byte aligned.
+ *   scale_x, scale_w: device pointers to one fp32 each (read on the device, so a run can be
+ *                     captured in a CUDA graph and the scales may change between replays).
+ *   y_ncdhw: N*K*Do*Ho*Wo bfloat16, contiguous, 16-byte aligned; every element is written
+ *            exactly once and its prior contents never leak into the result.
+ *   stride, pad: must equal the plan's (EINVAL otherwise).
+ * The plan's workspace is shared by its runs: at most one run of a plan may be in flight at a
+ * time (use one plan per concurrent stream). Errors: EINVAL, ECUDA (launch failure).
+ * Kernel-side errors are reported later, by conv3d_fp8_check.
+ */
+conv3d_status conv3d_fp8_run(conv3d_fp8_plan_t plan, const void *x_ncdhw, const void *w_kctrs,
+                             const float *scale_x, const float *scale_w, void *y_ncdhw,
+                             const int stride[3], const int pad[3], void *stream);
+
+/*
+ * Measurement hook: while ev_begin / ev_end (cudaEvent_t values passed as void*; either may be
+ * NULL) are set, every run of this plan records ev_begin on its stream immediately before the
+ * main implicit-GEMM kernel and ev_end immediately after it, so a caller can time that kernel
+ * alone. The caller owns the events. Pass NULL, NULL to stop. Errors: EINVAL for a NULL plan.
+ */
+conv3d_status conv3d_fp8_set_timing_events(conv3d_fp8_plan_t plan, void *ev_begin, void *ev_end);
+
+/* Synchronise the plan's device, then report (and clear) its status word: OK or EDEVICE. */
+conv3d_status conv3d_fp8_check(conv3d_fp8_plan_t plan);
+
+/* Fill *info for an existing plan. */
+conv3d_status conv3d_fp8_get_info(conv3d_fp8_plan_t plan, conv3d_fp8_plan_info *info);
+
+/*
+ * Host-only: what conv3d_fp8_plan_ex would decide for this shape on a GPU with `sm_count` SMs.
+ * Touches no device. Same validation and error codes as planning (except ENOMEM / ECUDA).
+ */
+conv3d_status conv3d_fp8_describe(int N, int C, int D, int H, int W, int K, int T, int R, int S,
+                                  const int stride[3], const int pad[3], int sm_count,
+                                  const conv3d_fp8_options *opts, conv3d_fp8_plan_info *info);
+
+/* Bytes of device workspace the plan owns (0 for a NULL plan). */
+size_t conv3d_fp8_workspace_size(conv3d_fp8_plan_t plan);
+
+/* Output extents of the plan. */
+conv3d_status conv3d_fp8_out_dims(conv3d_fp8_plan_t plan, int *Do, int *Ho, int *Wo);
+
+/* Synchronise the plan's device, free its workspace and the plan. NULL is a no-op. */
+void conv3d_fp8_destroy(conv3d_fp8_plan_t plan);
+
+/* Static description of a status code. */
+const char *conv3d_fp8_strerror(conv3d_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONV3D_FP8_H */

@@ -1,0 +1,106 @@
+"""C-ABI checks that need no GPU: the library loads, exports every declared entry point, and its
+host-only planning and validation behave as documented in include/conv3d_fp8.h."""
+import os
+import re
+
+import pytest
+
+from fp8_implicit_gemm_gb300 import build, capi, synth
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "conv3d_fp8.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return capi.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(conv3d_fp8_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("conv3d_fp8_plan", "conv3d_fp8_run", "conv3d_fp8_destroy",
+              "conv3d_fp8_workspace_size", "conv3d_fp8_strerror"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_strerror(lib):
+    for code in range(6):
+        assert capi.conv3d_fp8_strerror(code)
+    assert "unknown" in capi.conv3d_fp8_strerror(99)
+
+
+def _describe(shape, sm=152, **kw):
+    return capi.conv3d_fp8_describe(shape.N, shape.C, shape.D, shape.H, shape.W, shape.K, shape.T,
+                                    shape.R, shape.S, shape.stride, shape.pad, sm, **kw)
+
+
+def test_describe_configs(lib):
+    infos = [_describe(s) for s in synth.CONFIGS]
+    npq = [i["npq"] for i in infos]
+    # stride 2 on 4x16x16 with pad 1 gives a 2x8x8 output: npq = 128
+    assert npq == [288, 3840, 65536, 128, 244800]
+    assert [i["k_gemm"] for i in infos] == [2592, 1728, 3456, 13824, 6912]
+    assert [i["row_chk"] for i in infos] == [1, 0, 0, 0, 1]
+    assert [i["m_tiles"] for i in infos] == [3, 30, 512, 1, 1913]
+    assert [i["block_n"] for i in infos] == [96, 128, 128, 256, 256]
+    # deep and narrow -> split-K; the large layers never split
+    assert infos[3]["splits"] > 1
+    assert infos[2]["splits"] == 1 and infos[4]["splits"] == 1
+    for i in infos:
+        kb = i["k_blocks"]
+        assert i["splits"] * i["k_blocks_per_split"] >= kb
+        assert (i["splits"] - 1) * i["k_blocks_per_split"] < kb  # no empty split
+        assert i["grid"] <= 152 and i["stages"] >= 3
+        assert i["workspace_bytes"] > 0
+
+
+def test_describe_forced_options(lib):
+    s = synth.CONFIGS[1]
+    i = _describe(s, splits=4, block_n=64, max_ctas=10)
+    assert i["splits"] == 4 and i["block_n"] == 64 and i["n_tiles"] == 2 and i["grid"] == 10
+    # more splits than K blocks collapses to one block per split
+    i = _describe(s, splits=10_000)
+    assert i["splits"] == i["k_blocks"] and i["k_blocks_per_split"] == 1
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 16, 4, 4, 4, 16, 3, 3, 3, 1, 1), capi.CONV3D_EINVAL),    # N = 0
+    ((1, 16, 1, 4, 4, 16, 3, 3, 3, 1, 0), capi.CONV3D_EINVAL),    # empty output (D < T, pad 0)
+    ((1, 16, 4, 4, 4, 16, 3, 3, 3, 0, 1), capi.CONV3D_EINVAL),    # stride 0
+    ((1, 16, 4, 4, 4, 16, 3, 3, 3, 1, -1), capi.CONV3D_EINVAL),   # negative pad
+    ((1, 24, 4, 4, 4, 16, 3, 3, 3, 1, 1), capi.CONV3D_EUNSUPPORTED),  # C % 16 != 0
+])
+def test_describe_validation(lib, args, code):
+    N, C, D, H, W, K, T, R, S, st, pd = args
+    assert capi.conv3d_fp8_describe_status(N, C, D, H, W, K, T, R, S, st, pd, 152) == code
+
+
+def test_describe_rejects_bad_block_n(lib):
+    s = synth.CONFIGS[0]
+    for bn in (16, 48, 288):
+        assert capi.conv3d_fp8_describe_status(s.N, s.C, s.D, s.H, s.W, s.K, 3, 3, 3, 1, 1, 152,
+                                               block_n=bn) == capi.CONV3D_EINVAL
+
+
+def test_plan_rejects_bad_shape_before_touching_a_device(lib):
+    with pytest.raises(capi.Conv3dFp8Error) as e:
+        capi.conv3d_fp8_plan(1, 24, 4, 4, 4, 16, 3, 3, 3, 1, 1)
+    assert e.value.status == capi.CONV3D_EUNSUPPORTED
+
+
+def test_null_plan_entry_points(lib):
+    assert capi.conv3d_fp8_workspace_size(None) == 0
+    assert lib.conv3d_fp8_check(None) == capi.CONV3D_EINVAL
+    capi.conv3d_fp8_destroy(None)

@@ -1,0 +1,113 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Small workloads are compared in full; the two large ones (65536 and 244800 output positions) on
+sampled outputs that the oracle computes one by one, in the same launch configuration the
+benchmark times. Every y is pre-filled with NaN, so an element that is never written fails.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_implicit_gemm_gb300 import synth
+from _gpu_common import GpuConv, bits, check_against, sample_indices
+
+pytestmark = pytest.mark.gpu
+
+
+def _full_case(shape, seed, **opts):
+    inp = synth.make_inputs(shape, seed)
+    y64, yb = oracle.conv3d_fp8(inp["x"].numpy(), inp["w"].numpy(), inp["sx"], inp["sw"],
+                                shape.stride, shape.pad)
+    g = GpuConv(shape, inp, **opts)
+    try:
+        out = bits(g.run())
+        assert out.shape == y64.shape
+        return check_against(out, y64, yb, shape.name or str(shape)), g.info
+    finally:
+        g.close()
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 3])
+def test_config_full_output(cfg):
+    res, info = _full_case(synth.CONFIGS[cfg], synth.config_seed(cfg))
+    print(cfg, res, info["splits"], info["block_n"])
+
+
+@pytest.mark.parametrize("cfg", [2, 4])
+def test_config_sampled_outputs(cfg):
+    shape = synth.CONFIGS[cfg]
+    inp = synth.make_config_inputs(cfg)
+    g = GpuConv(shape, inp)
+    try:
+        y = g.run()
+        assert not torch.isnan(y).any().item(), "some outputs never written"
+        idx = sample_indices(g.out_shape, 60000, seed=cfg)
+        y64, yb = oracle.conv3d_fp8_points(inp["x"].numpy(), inp["w"].numpy(), inp["sx"],
+                                           inp["sw"], idx, shape.stride, shape.pad)
+        out = bits(y).ravel()[idx]
+        print(cfg, check_against(out, y64, yb, shape.name))
+    finally:
+        g.close()
+
+
+# Odd shapes: channel counts that are multiples of 16 but not 32 (K_gemm tail of 16 bytes), K not a
+# multiple of the N tile, W = 1, stride 2 on odd sizes, n > 1 tiles that straddle images,
+# 1x1x1 and 1x3x3 filters, pad 0 and 2, anisotropic stride/pad, tiny volumes.
+ODD = [
+    synth.ConvShape(1, 16, 3, 5, 7, 16),
+    synth.ConvShape(2, 48, 4, 6, 5, 80),
+    synth.ConvShape(3, 32, 5, 7, 9, 100, stride=2),
+    synth.ConvShape(1, 64, 6, 9, 1, 32, T=3, R=3, S=1, pad=(1, 1, 0)),
+    synth.ConvShape(2, 16, 4, 4, 4, 48, T=1, R=1, S=1, pad=0),
+    synth.ConvShape(1, 32, 2, 11, 13, 64, T=1, R=3, S=3, pad=(0, 1, 1)),
+    synth.ConvShape(1, 16, 7, 7, 7, 16, pad=2),
+    synth.ConvShape(1, 32, 9, 10, 11, 96, stride=(1, 2, 3), pad=(0, 1, 2)),
+    synth.ConvShape(1, 16, 1, 1, 1, 16, pad=1),
+    synth.ConvShape(2, 128, 3, 17, 19, 256),
+    synth.ConvShape(1, 272, 2, 5, 6, 40),
+]
+
+
+@pytest.mark.parametrize("i", range(len(ODD)))
+def test_odd_shapes(i):
+    res, info = _full_case(ODD[i], 77 + i)
+    print(ODD[i], res, info["splits"], info["block_n"])
+
+
+@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+def test_forced_splits_config1(splits):
+    res, info = _full_case(synth.CONFIGS[1], synth.config_seed(1), splits=splits)
+    assert info["splits"] == splits
+
+
+@pytest.mark.parametrize("block_n", [32, 64, 128, 256])
+def test_forced_block_n(block_n):
+    shape = synth.ConvShape(2, 32, 4, 6, 10, 200)
+    res, info = _full_case(shape, 5, block_n=block_n)
+    assert info["block_n"] == block_n
+
+
+def test_max_ctas_small_grid_many_tiles():
+    # 2 CTAs walk all 30 tiles: exercises the TMEM double buffer and stage-ring wrap-around
+    res, info = _full_case(synth.CONFIGS[1], synth.config_seed(1), max_ctas=2, splits=1)
+    assert info["grid"] == 2
+
+
+def test_split_k_is_reproducible_and_close_across_split_counts():
+    shape = synth.CONFIGS[3]
+    inp = synth.make_config_inputs(3)
+    outs = {}
+    for splits in (1, 4, 27):
+        g = GpuConv(shape, inp, splits=splits)
+        try:
+            a = bits(g.run())
+            b = bits(g.run())
+            assert np.array_equal(a, b), f"splits={splits} not bitwise reproducible"
+            outs[splits] = a
+        finally:
+            g.close()
+    y64, yb = oracle.conv3d_fp8(inp["x"].numpy(), inp["w"].numpy(), inp["sx"], inp["sw"],
+                                shape.stride, shape.pad)
+    for s, a in outs.items():
+        check_against(a, y64, yb, f"splits={s}")

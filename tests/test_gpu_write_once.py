@@ -1,0 +1,110 @@
+"""Every output element is written exactly once, and nothing outside y is touched.
+
+The subject page ("[Fix] conv3d fp8: guard padded M rows in the epilogue store", sections
+"Verification" and "Root cause") found 12 failures in 200 launches of the (1,96,4,8,9,96) case
+because padded M rows of the last tile raced live stores. Here each of 200 launches starts from a
+NaN-filled y: afterwards no NaN may remain, no live element may be zero, and every launch must be
+bitwise identical to the first. y sits between 4 KB guard bands that must survive untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from fp8_implicit_gemm_gb300 import capi, synth
+from _gpu_common import GpuConv, NAN_BF16, bits, check_against, sample_indices
+
+pytestmark = pytest.mark.gpu
+
+REPEATS = 200
+GUARD_ELEMS = 2048  # 4 KB of bf16 on each side
+CANARY = 0x5A5A
+
+
+def _guarded_y(g: GpuConv):
+    numel = int(np.prod(g.out_shape))
+    buf = torch.empty(numel + 2 * GUARD_ELEMS, dtype=torch.bfloat16, device="cuda")
+    buf.view(torch.int16).fill_(CANARY)
+    y = buf[GUARD_ELEMS:GUARD_ELEMS + numel].view(g.out_shape)
+    return buf, y
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
+def test_repeated_launches_write_every_element_once(cfg):
+    shape = synth.CONFIGS[cfg]
+    inp = synth.make_config_inputs(cfg)
+    g = GpuConv(shape, inp)
+    try:
+        buf, y = _guarded_y(g)
+        nan16 = np.int16(np.uint16(NAN_BF16).view(np.int16))
+        first = None
+        for rep in range(REPEATS):
+            y.view(torch.int16).fill_(nan16)
+            g.run(y)
+            if first is None:
+                first = y.clone()
+                assert not torch.isnan(first).any().item()
+            else:
+                assert torch.equal(y.view(torch.int16), first.view(torch.int16)), \
+                    f"launch {rep} differs from launch 0"
+        torch.cuda.synchronize()
+        guard = torch.cat([buf[:GUARD_ELEMS], buf[-GUARD_ELEMS:]]).view(torch.int16)
+        assert bool((guard == CANARY).all().item()), "a store landed outside y"
+        assert capi.conv3d_fp8_check(g.plan) == capi.CONV3D_OK
+        # and the result is right (sampled: the oracle for the large configs is minutes long)
+        idx = sample_indices(g.out_shape, 20000, seed=100 + cfg)
+        y64, yb = oracle.conv3d_fp8_points(inp["x"].numpy(), inp["w"].numpy(), inp["sx"],
+                                           inp["sw"], idx, shape.stride, shape.pad)
+        check_against(bits(first).ravel()[idx], y64, yb, f"config {cfg}")
+        # no live element is zero anywhere (the failure mode of the unguarded padded rows)
+        zeros = (first.float() == 0).nonzero()
+        if zeros.numel():
+            zi = np.ravel_multi_index(tuple(zeros.cpu().numpy().T), g.out_shape)
+            z64, _ = oracle.conv3d_fp8_points(inp["x"].numpy(), inp["w"].numpy(), inp["sx"],
+                                              inp["sw"], zi[:5000], shape.stride, shape.pad)
+            assert np.all(np.abs(z64) <= 2.0 ** -7 * np.abs(z64) + 1e-3)
+    finally:
+        g.close()
+
+
+def test_bounded_wait_reports_instead_of_hanging():
+    """A weight tile that never arrives: the MMA warp's bounded wait runs out, the kernel winds
+    down, the status word says so, and the context stays usable for the next plan."""
+    shape = synth.CONFIGS[0]
+    inp = synth.make_config_inputs(0)
+    bad = GpuConv(shape, inp, debug_flags=1, wait_timeout_ms=200, splits=1)
+    try:
+        bad.run()
+        assert capi.conv3d_fp8_check(bad.plan) == capi.CONV3D_EDEVICE
+        assert capi.conv3d_fp8_check(bad.plan) == capi.CONV3D_OK  # cleared
+    finally:
+        bad.close()
+    good = GpuConv(shape, inp)
+    try:
+        out = bits(good.run())
+        y64, yb = oracle.conv3d_fp8(inp["x"].numpy(), inp["w"].numpy(), inp["sx"], inp["sw"],
+                                    shape.stride, shape.pad)
+        check_against(out, y64, yb, "after a reported timeout")
+        assert capi.conv3d_fp8_check(good.plan) == capi.CONV3D_OK
+    finally:
+        good.close()
+
+
+def test_run_argument_errors_launch_nothing():
+    shape = synth.CONFIGS[0]
+    inp = synth.make_config_inputs(0)
+    g = GpuConv(shape, inp)
+    try:
+        y = g.new_y()
+        s = shape
+        st = capi.conv3d_fp8_run_status(g.plan, g.x, g.w, g.sx, g.sw, y, (2, 2, 2), s.pad)
+        assert st == capi.CONV3D_EINVAL                          # stride differs from the plan
+        st = capi.conv3d_fp8_run_status(g.plan, g.x, g.w, g.sx, g.sw, y.data_ptr() + 2,
+                                        s.stride, s.pad)
+        assert st == capi.CONV3D_EINVAL                          # misaligned y
+        st = capi.conv3d_fp8_run_status(g.plan, 0, g.w, g.sx, g.sw, y, s.stride, s.pad)
+        assert st == capi.CONV3D_EINVAL                          # NULL x
+        torch.cuda.synchronize()
+        assert torch.isnan(y).all().item()                       # nothing was written
+    finally:
+        g.close()
