@@ -271,7 +271,9 @@ conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t* out, int N, int C, int D, in
     delete plan;
     return CONV3D_EUNSUPPORTED;
   }
-  if (conv_set_smem_attr(smem) != cudaSuccess) {
+  // The attribute is per kernel and per device, shared by every plan: grant the device's opt-in
+  // maximum once, so that a later plan with a smaller tile cannot shrink it under this one.
+  if (conv_set_smem_attr((size_t)prop.sharedMemPerBlockOptin) != cudaSuccess) {
     delete plan;
     return CONV3D_ECUDA;
   }

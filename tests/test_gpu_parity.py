@@ -111,3 +111,20 @@ def test_split_k_is_reproducible_and_close_across_split_counts():
                                 shape.stride, shape.pad)
     for s, a in outs.items():
         check_against(a, y64, yb, f"splits={s}")
+
+
+def test_plans_with_different_tiles_coexist():
+    """A plan created after another one (with a different shared-memory footprint) must not break
+    the first one's launches."""
+    s0 = synth.CONFIGS[0]
+    inp = synth.make_config_inputs(0)
+    big = GpuConv(s0, inp, block_n=96, splits=1)      # 7 stages of 28 KB
+    small = GpuConv(s0, inp, block_n=32, splits=1)    # 8 stages of 20 KB
+    try:
+        y64, yb = oracle.conv3d_fp8(inp["x"].numpy(), inp["w"].numpy(), inp["sx"], inp["sw"],
+                                    s0.stride, s0.pad)
+        check_against(bits(big.run()), y64, yb, "first plan after a second was created")
+        check_against(bits(small.run()), y64, yb, "second plan")
+    finally:
+        big.close()
+        small.close()
