@@ -73,6 +73,8 @@ def load() -> ctypes.CDLL:
             lib.conv3d_fp8_run.argtypes = [vp, vp, vp, vp, vp, vp, i3, i3, vp]
             lib.conv3d_fp8_set_timing_events.restype = ci
             lib.conv3d_fp8_set_timing_events.argtypes = [vp, vp, vp]
+            lib.conv3d_fp8_run_noalloc.restype = ci
+            lib.conv3d_fp8_run_noalloc.argtypes = [ci] * 9 + [i3, i3, vp, vp, vp, vp, vp, vp]
             lib.conv3d_fp8_check.restype = ci
             lib.conv3d_fp8_check.argtypes = [vp]
             lib.conv3d_fp8_get_info.restype = ci
@@ -168,6 +170,21 @@ def conv3d_fp8_run_status(plan, x, w, scale_x, scale_w, y, stride, pad, stream=N
     """As conv3d_fp8_run, but returns the status code instead of raising."""
     return load().conv3d_fp8_run(plan, _ptr(x), _ptr(w), _ptr(scale_x), _ptr(scale_w), _ptr(y),
                                  _int3(stride), _int3(pad), _stream(stream))
+
+
+def conv3d_fp8_run_noalloc_status(N, C, D, H, W, K, T, R, S, stride, pad, x, w, scale_x,
+                                  scale_w, y, stream=None) -> int:
+    """Allocation-free run (no plan; scratch in a fixed device array of the library, see
+    include/conv3d_fp8.h). Returns the status code."""
+    return load().conv3d_fp8_run_noalloc(N, C, D, H, W, K, T, R, S, _int3(stride), _int3(pad),
+                                         _ptr(x), _ptr(w), _ptr(scale_x), _ptr(scale_w), _ptr(y),
+                                         _stream(stream))
+
+
+def conv3d_fp8_run_noalloc(N, C, D, H, W, K, T, R, S, stride, pad, x, w, scale_x, scale_w, y,
+                           stream=None) -> None:
+    _raise(conv3d_fp8_run_noalloc_status(N, C, D, H, W, K, T, R, S, stride, pad, x, w, scale_x,
+                                         scale_w, y, stream), "conv3d_fp8_run_noalloc")
 
 
 def conv3d_fp8_set_timing_events(plan, ev_begin, ev_end) -> None:

@@ -404,3 +404,115 @@ const char* conv3d_fp8_strerror(conv3d_status s) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot call cudaMalloc: a host framework whose caching allocator owns the device's
+// memory pool and forbids stray allocations, a plugin interface that hands a kernel its tensors
+// but gives it no way to request memory, or a latency-critical loop that cannot afford the device
+// synchronisation that cudaFree implies. conv3d_fp8_run_noalloc serves them: it runs the same
+// kernels as conv3d_fp8_run, but its scratch (the packed operands, split-K partials and the status
+// word) lives in the fixed-size device array below instead of a plan-owned workspace.
+//
+// The array is reserved by the CUDA runtime when this library's device code is loaded on a GPU and
+// stays reserved until the process exits. Every call on a device shares it and it keeps the last
+// call's contents: each call rewrites everything it reads (the pack kernel writes every byte of
+// the padded operands, partials are written before they are reduced) and clears the status word
+// itself. Two calls whose work overlaps on the GPU (other streams, other host threads) race on the
+// array; serialise them.
+// ------------------------------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[CONV3D_FP8_NOALLOC_SCRATCH_BYTES];
+
+#include <mutex>
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_base[kNoAllocMaxDevices] = {};
+
+// Once per device, with that device current: take the device address of the scratch array (the
+// host-side symbol is only a stand-in and must never reach a kernel) and grant the main kernel the
+// device's opt-in shared memory. Allocates nothing.
+conv3d_status noalloc_setup(int dev, void** base) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_base[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      cudaGetLastError();
+      return CONV3D_ECUDA;
+    }
+    int optin = 0;
+    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        conv_set_smem_attr((size_t)optin) != cudaSuccess) {
+      cudaGetLastError();
+      return CONV3D_ECUDA;
+    }
+    g_noalloc_base[dev] = ptr;
+  }
+  *base = g_noalloc_base[dev];
+  return CONV3D_OK;
+}
+
+}  // namespace
+
+extern "C" conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int W, int K, int T,
+                                                int R, int S, const int stride[3],
+                                                const int pad[3], const void* x, const void* w,
+                                                const float* scale_x, const float* scale_w,
+                                                void* y, void* stream) {
+  if (!x || !w || !scale_x || !scale_w || !y || !stride || !pad) return CONV3D_EINVAL;
+  if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(scale_x, 4) ||
+      !aligned(scale_w, 4))
+    return CONV3D_EINVAL;
+  // Shape errors first, without touching the device.
+  conv3d_fp8_plan_info info{};
+  conv3d_status st =
+      decide(N, C, D, H, W, K, T, R, S, stride, pad, 1, nullptr, &info, nullptr, nullptr);
+  if (st != CONV3D_OK) return st;
+
+  int dev = -1, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return CONV3D_ECUDA;
+  }
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return CONV3D_EUNSUPPORTED;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return CONV3D_ECUDA;
+  if (major != 10 || minor != 3) return CONV3D_EUNSUPPORTED;
+
+  ConvParams p{};
+  Layout L{};
+  st = decide(N, C, D, H, W, K, T, R, S, stride, pad, sms, nullptr, &info, &p, &L);
+  if (st != CONV3D_OK) return st;
+  if (L.total > (size_t)CONV3D_FP8_NOALLOC_SCRATCH_BYTES) return CONV3D_EUNSUPPORTED;
+
+  void* base = nullptr;
+  st = noalloc_setup(dev, &base);
+  if (st != CONV3D_OK) return st;
+  uint8_t* ws = static_cast<uint8_t*>(base);
+  p.xp = ws + L.xp_off;
+  p.wp = ws + L.wp_off;
+  p.partials = L.part_bytes ? reinterpret_cast<float*>(ws + L.part_off) : nullptr;
+  p.status = reinterpret_cast<int*>(ws + L.status_off);
+  p.x = static_cast<const uint8_t*>(x);
+  p.w = static_cast<const uint8_t*>(w);
+  p.y = static_cast<uint16_t*>(y);
+  p.scale_x = scale_x;
+  p.scale_w = scale_w;
+
+  CUtensorMap wmap{};
+  st = encode_weight_map(&wmap, p.wp, K, p.kg, p.block_n);
+  if (st != CONV3D_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(p.status, 0, sizeof(int), s) != cudaSuccess) return CONV3D_ECUDA;
+  if (launch_pack(p, s) != cudaSuccess) return CONV3D_ECUDA;
+  if (launch_conv(p, wmap, info.row_chk != 0, info.grid, s) != cudaSuccess) return CONV3D_ECUDA;
+  if (p.splits > 1 && launch_splitk_reduce(p, info.row_chk != 0, s) != cudaSuccess)
+    return CONV3D_ECUDA;
+  return CONV3D_OK;
+}

@@ -118,6 +118,33 @@ conv3d_status conv3d_fp8_run(conv3d_fp8_plan_t plan, const void *x_ncdhw, const 
  */
 conv3d_status conv3d_fp8_set_timing_events(conv3d_fp8_plan_t plan, void *ev_begin, void *ev_end);
 
+/*
+ * Allocation-free run (no counterpart on the subject page; it exists for callers of this library).
+ * Some callers cannot call cudaMalloc: a host framework whose caching allocator owns the device's
+ * memory pool, a plugin interface that passes tensors in but offers no way to ask for memory, or a
+ * latency-critical loop that cannot take the device synchronisation of cudaFree. This entry point
+ * needs no plan and allocates nothing: it runs the same kernels as conv3d_fp8_run, with their
+ * scratch (packed operands, split-K partials, status word) in a fixed device array of
+ * CONV3D_FP8_NOALLOC_SCRATCH_BYTES that the library's device code reserves on every GPU that
+ * loads it, until the process exits.
+ *   Shape, stride and pad are as for conv3d_fp8_plan (default planning, current device); x, w,
+ *   the scales and y are as for conv3d_fp8_run. The call is asynchronous on `stream`.
+ *   The first call on each device takes the array's device address and sets a kernel attribute;
+ *   make that first call before any stream capture on that device.
+ *   All calls share the one array and it keeps the last call's contents: calls whose work overlaps
+ *   on the GPU race on it, so serialise them. Kernel-side bounded-wait errors are not reported
+ *   here (use a plan and conv3d_fp8_check when you need them).
+ * Errors: EINVAL, EUNSUPPORTED (as for planning, and when the problem needs more scratch than the
+ * array holds: packed x and w plus split-K partials), ECUDA.
+ */
+#define CONV3D_FP8_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int W, int K, int T, int R,
+                                     int S, const int stride[3], const int pad[3],
+                                     const void *x_ncdhw, const void *w_kctrs,
+                                     const float *scale_x, const float *scale_w, void *y_ncdhw,
+                                     void *stream);
+
 /* Synchronise the plan's device, then report (and clear) its status word: OK or EDEVICE. */
 conv3d_status conv3d_fp8_check(conv3d_fp8_plan_t plan);
 
