@@ -19,6 +19,7 @@ struct conv3d_fp8_plan_s {
   int pad[3] = {0, 0, 0};
   ConvParams p{};
   CUtensorMap wmap{};
+  CUtensorMap xmap{};  // im2col map of the packed x (im2col route only)
   conv3d_fp8_plan_info info{};
   void* workspace = nullptr;
   cudaEvent_t ev_begin = nullptr;  // measurement hook, caller-owned
@@ -69,7 +70,23 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   const long long npq = (long long)N * dhw;
   const long long taps = (long long)T * R * S;
   const long long kg = taps * C;
-  const long long Dp = D + 2LL * pad[0], Hp = H + 2LL * pad[1], Wp = W + 2LL * pad[2];
+  conv3d_fp8_options o{};
+  if (opts) o = *opts;
+  if (o.route < 0 || o.route > 2) return CONV3D_EINVAL;
+  // The TMA im2col route needs C in whole 32-byte sub-tile rows and bounding-box corners
+  // (-pad, pad - (filter - 1)) inside the [-16, 15] range of a rank-5 im2col tensor map.
+  bool im2col_ok = (C % 32 == 0);
+  const int filt[3] = {T, R, S};
+  for (int i = 0; i < 3; ++i) {
+    const int lower = -pad[i], upper = pad[i] - (filt[i] - 1);
+    if (lower < -16 || lower > 15 || upper < -16 || upper > 15 || stride[i] > 8) im2col_ok = false;
+  }
+  if (o.route == 2 && !im2col_ok) return CONV3D_EUNSUPPORTED;
+  const int route = (o.route == 1 || !im2col_ok) ? kRouteGather : kRouteIm2col;
+  const int a_cb = C % 128 == 0 ? 128 : (C % 64 == 0 ? 64 : 32);
+  const int halo[3] = {route == kRouteGather ? pad[0] : 0, route == kRouteGather ? pad[1] : 0,
+                       route == kRouteGather ? pad[2] : 0};
+  const long long Dp = D + 2LL * halo[0], Hp = H + 2LL * halo[1], Wp = W + 2LL * halo[2];
   const long long y_elems = npq * K;
   const long long x_elems = (long long)N * C * D * H * W;
   const long long xp_elems = (long long)N * Dp * Hp * Wp * C;
@@ -79,8 +96,6 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
       Hp >= (1LL << 30) || Wp >= (1LL << 30) || K >= (1 << 30) || taps >= (1 << 20))
     return CONV3D_EUNSUPPORTED;
 
-  conv3d_fp8_options o{};
-  if (opts) o = *opts;
   int block_n = o.block_n;
   if (block_n == 0) block_n = (int)std::min<long long>(256, round_up(K, 32));
   if (block_n < 32 || block_n > 256 || block_n % 32 != 0) return CONV3D_EINVAL;
@@ -137,6 +152,7 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   info->grid = (int)grid;
   info->sm_count = sm_count;
   info->workspace_bytes = L.total;
+  info->route = route == kRouteIm2col ? 2 : 1;
 
   if (pp) {
     ConvParams& p = *pp;
@@ -145,6 +161,9 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
     p.sd = stride[0]; p.sh = stride[1]; p.sw = stride[2];
     p.pd = pad[0]; p.ph = pad[1]; p.pw = pad[2];
     p.Do = Do; p.Ho = Ho; p.Wo = Wo;
+    p.route = route;
+    p.a_cb = a_cb;
+    p.pk_pd = halo[0]; p.pk_ph = halo[1]; p.pk_pw = halo[2];
     p.Dp = (int)Dp; p.Hp = (int)Hp; p.Wp = (int)Wp;
     p.dhw = (int)dhw;
     p.npq = (int)npq;
@@ -197,6 +216,48 @@ conv3d_status encode_weight_map(CUtensorMap* map, void* wp, int K, int kg, int b
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, wp, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV3D_OK : CONV3D_ECUDA;
+}
+
+typedef CUresult (*EncodeIm2colFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const int*, const int*,
+                                   cuuint32_t, cuuint32_t, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeIm2colFn get_encode_im2col() {
+  static EncodeIm2colFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeIm2colFn>(ptr);
+  }
+  return fn;
+}
+
+// The packed x as a channels-last 5D tensor (C, W, H, D, N). One load brings 128 consecutive
+// output positions (the traversal walks W, then H, D and N, over the starting pixels of the
+// filter windows: from -pad to extent - 1 + pad - (filter - 1), every `stride`), a_cb channels
+// each, shifted by the tap given with the load; everything outside the tensor reads zero.
+conv3d_status encode_im2col_map(CUtensorMap* map, void* xcl, const ConvParams& p) {
+  EncodeIm2colFn enc = get_encode_im2col();
+  if (!enc) return CONV3D_ECUDA;
+  const cuuint64_t dims[5] = {(cuuint64_t)p.C, (cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)p.D,
+                              (cuuint64_t)p.N};
+  const cuuint64_t strides[4] = {(cuuint64_t)p.C, (cuuint64_t)p.C * p.W,
+                                 (cuuint64_t)p.C * p.W * p.H, (cuuint64_t)p.C * p.W * p.H * p.D};
+  const int lower[3] = {-p.pw, -p.ph, -p.pd};
+  const int upper[3] = {p.pw - (p.S - 1), p.ph - (p.R - 1), p.pd - (p.T - 1)};
+  const cuuint32_t estr[5] = {1, (cuuint32_t)p.sw, (cuuint32_t)p.sh, (cuuint32_t)p.sd, 1};
+  const CUtensorMapSwizzle sw = p.a_cb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : p.a_cb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : CU_TENSOR_MAP_SWIZZLE_32B;
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, xcl, dims, strides, lower, upper,
+                   (cuuint32_t)p.a_cb, (cuuint32_t)kBlockM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? CONV3D_OK : CONV3D_ECUDA;
 }
@@ -293,6 +354,8 @@ conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t* out, int N, int C, int D, in
     return CONV3D_ECUDA;
   }
   st = encode_weight_map(&plan->wmap, plan->p.wp, K, plan->p.kg, plan->p.block_n);
+  if (st == CONV3D_OK && plan->p.route == kRouteIm2col)
+    st = encode_im2col_map(&plan->xmap, plan->p.xp, plan->p);
   if (st != CONV3D_OK) {
     cudaFree(plan->workspace);
     delete plan;
@@ -330,7 +393,8 @@ conv3d_status conv3d_fp8_run(conv3d_fp8_plan_t plan, const void* x, const void* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (launch_pack(p, s) != cudaSuccess) return CONV3D_ECUDA;
   if (plan->ev_begin && cudaEventRecord(plan->ev_begin, s) != cudaSuccess) return CONV3D_ECUDA;
-  if (launch_conv(p, plan->wmap, plan->info.row_chk != 0, plan->info.grid, s) != cudaSuccess)
+  if (launch_conv(p, plan->wmap, plan->xmap, plan->info.row_chk != 0, plan->info.grid, s) !=
+      cudaSuccess)
     return CONV3D_ECUDA;
   if (plan->ev_end && cudaEventRecord(plan->ev_end, s) != cudaSuccess) return CONV3D_ECUDA;
   if (p.splits > 1 && launch_splitk_reduce(p, plan->info.row_chk != 0, s) != cudaSuccess)
@@ -505,13 +569,15 @@ extern "C" conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int 
   p.scale_x = scale_x;
   p.scale_w = scale_w;
 
-  CUtensorMap wmap{};
+  CUtensorMap wmap{}, xmap{};
   st = encode_weight_map(&wmap, p.wp, K, p.kg, p.block_n);
+  if (st == CONV3D_OK && p.route == kRouteIm2col) st = encode_im2col_map(&xmap, p.xp, p);
   if (st != CONV3D_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(p.status, 0, sizeof(int), s) != cudaSuccess) return CONV3D_ECUDA;
   if (launch_pack(p, s) != cudaSuccess) return CONV3D_ECUDA;
-  if (launch_conv(p, wmap, info.row_chk != 0, info.grid, s) != cudaSuccess) return CONV3D_ECUDA;
+  if (launch_conv(p, wmap, xmap, info.row_chk != 0, info.grid, s) != cudaSuccess)
+    return CONV3D_ECUDA;
   if (p.splits > 1 && launch_splitk_reduce(p, info.row_chk != 0, s) != cudaSuccess)
     return CONV3D_ECUDA;
   return CONV3D_OK;

@@ -15,6 +15,12 @@ constexpr int kNumThreads = 320;    // 4 epilogue warps, 4 A-loader warps, 1 TMA
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kMaxStages = 8;
 
+// How the A operand (im2col rows of x) reaches shared memory.
+enum : int {
+  kRouteGather = 0,  // 16-byte cp.async gathers from a zero-padded channels-last copy of x
+  kRouteIm2col = 1,  // TMA im2col loads from an unpadded channels-last copy (C % 32 == 0)
+};
+
 // Status-word bits recorded by kernels whose bounded waits ran out.
 enum : int {
   kStatusWaitFull = 1 << 0,       // MMA warp waiting for operands
@@ -29,7 +35,10 @@ struct ConvParams {
   int N, C, D, H, W, K, T, R, S;
   int sd, sh, sw, pd, ph, pw;
   int Do, Ho, Wo;
-  int Dp, Hp, Wp;        // extents of the zero-padded channels-last copy of x
+  int route;             // kRouteGather or kRouteIm2col (how A reaches shared memory)
+  int a_cb;              // im2col route: channels per A sub-tile (32, 64 or 128 = its row bytes)
+  int pk_pd, pk_ph, pk_pw;  // zero halo of the packed channels-last x (gather route only)
+  int Dp, Hp, Wp;        // extents of the packed channels-last copy of x (halo included)
   int dhw;               // Do*Ho*Wo
   int npq;               // N*dhw, the M of the GEMM view
   int taps;              // T*R*S
@@ -56,8 +65,8 @@ struct ConvParams {
 
 // Launchers (defined in the .cu files). Each returns the CUDA error of its launch.
 cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream);
-cudaError_t launch_conv(const ConvParams& p, const CUtensorMap& wmap, bool row_chk, int grid,
-                        cudaStream_t stream);
+cudaError_t launch_conv(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
+                        bool row_chk, int grid, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ConvParams& p, bool row_chk, cudaStream_t stream);
 size_t conv_smem_bytes(int block_n, int stages);
 cudaError_t conv_set_smem_attr(size_t smem_bytes);

@@ -6,15 +6,18 @@
 // One persistent CTA per SM walks a static list of work units (m-tile, n-tile, K-split). Warp roles:
 //   warps 0-3  epilogue: TMEM -> registers, scale, bf16, stores masked on row < npq and col < K
 //              (warp w owns TMEM lanes 32w..32w+31, i.e. rows 32w..32w+31 of the tile)
-//   warps 4-7  A loader: cp.async 16-byte gathers from the zero-padded channels-last input into the
-//              128-byte-swizzled K-major A stage; rows at or past npq are zero-filled
-//   warp 8     B loader: one TMA 2D tile of the packed weights per stage (out-of-range zero fill);
-//              also owns the TMEM allocation
+//   warp 8     TMA loader: per stage one 2D tile of the packed weights (B) and, on the im2col
+//              route, the A tile as 128/a_cb im2col loads (one per tap and channel block) of 128
+//              consecutive output positions from the channels-last input; the TMA unit zero-fills
+//              taps outside the volume and rows past the last image. Also owns the TMEM allocation.
+//   warps 4-7  gather route only (C % 32 != 0 or paddings beyond the im2col corner range): A by
+//              16-byte cp.async gathers from the zero-padded channels-last input into the
+//              128-byte-swizzled stage; rows at or past npq are zero-filled
 //   warp 9     MMA issuer: 4 x tcgen05.mma (M=128, N=block_n, K=32) per 128-byte K block
-// Stages are handed over with mbarriers: A-full (128 loader arrivals), B-full (TMA bytes),
-// stage-empty (tcgen05.commit). Two TMEM accumulators let the epilogue of one tile overlap the
-// main loop of the next. Every wait is bounded; a wait that runs out records a status bit and
-// the whole CTA winds down without faulting.
+// Stages are handed over with mbarriers: TMA-full (transaction bytes of A and/or B), A-full (128
+// gather arrivals, gather route), stage-empty (tcgen05.commit). Two TMEM accumulators let the
+// epilogue of one tile overlap the main loop of the next. Every wait is bounded; a wait that runs
+// out records a status bit and the whole CTA winds down without faulting.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -27,6 +30,18 @@ constexpr int kLoaderLag = 2;  // cp.async groups kept in flight before a stage 
 
 struct Unit {
   int tile, m_tile, n_tile, split, kb0, kb1;
+};
+
+// Position in the ring of S pipeline stages: stage index and the parity of its current phase.
+struct Ring {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int S) {
+    if (++stage == S) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
 };
 
 __device__ __forceinline__ Unit decode_unit(const ConvParams& p, int u) {
@@ -56,7 +71,8 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64
 
 template <bool kRowChk>
 __global__ void __launch_bounds__(kNumThreads, 1)
-    conv3d_fp8_tc_kernel(const __grid_constant__ CUtensorMap wmap, const ConvParams p) {
+    conv3d_fp8_tc_kernel(const __grid_constant__ CUtensorMap wmap,
+                         const __grid_constant__ CUtensorMap xmap, const ConvParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);  // 1024-aligned stages
@@ -98,13 +114,17 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   if (warp == 8) {
     tmem_alloc(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
     tmem_relinquish();
-    if (lane == 0) prefetch_tensormap(&wmap);
+    if (lane == 0) {
+      prefetch_tensormap(&wmap);
+      if (p.route == kRouteIm2col) prefetch_tensormap(&xmap);
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const AbortState ab{abort_flag, p.status, p.timeout_ns};
+  const bool im2col = p.route == kRouteIm2col;
 
   if (warp < 4) {
     // ------------------------------------------------------------------------------ epilogue
@@ -154,93 +174,140 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       mbar_arrive(accEmpty(buf));
     }
   } else if (warp < 8) {
-    // ------------------------------------------------------------------------------ A loader
-    const int pt = threadIdx.x - 128;
-    const int q = pt & 7;    // 16-byte chunk of the 128-byte K block
-    const int rb = pt >> 3;  // rows rb, rb+16, ..., rb+112
-    const uint32_t row_dst = sA_u32 + (uint32_t)rb * 128u + (uint32_t)((q ^ (rb & 7)) << 4);
-    const int RS = p.R * p.S;
-    uint32_t it = 0, signaled = 0;
-    int inflight = 0;
-    bool aborted = false;
-    for (int u = blockIdx.x; u < p.num_units && !aborted; u += gridDim.x) {
-      const Unit un = decode_unit(p, u);
-      long long rowoff[8];
-      bool rowok[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int m = un.m_tile * kBlockM + rb + 16 * i;
-        rowok[i] = !kRowChk || m < p.npq;
-        const int mm = rowok[i] ? m : 0;
-        const int n = mm / p.dhw;
-        const int pix = mm - n * p.dhw;
-        const int wo = pix % p.Wo;
-        const int t2 = pix / p.Wo;
-        const int ho = t2 % p.Ho;
-        const int od = t2 / p.Ho;
-        rowoff[i] = ((((long long)n * p.Dp + od * p.sd) * p.Hp + ho * p.sh) * p.Wp + wo * p.sw) * p.C;
-      }
-      for (int kb = un.kb0; kb < un.kb1; ++kb) {
-        const int stage = it % S;
-        if (!wait_bounded(empty(stage), ((it / S) & 1) ^ 1, ab, kStatusWaitEmpty)) {
-          aborted = true;
-          break;
-        }
-        const int kk = kb * kBlockK + q * 16;
-        const bool kok = kk < p.kg;
-        long long tapoff = 0;
-        if (kok) {
-          const int tap = kk / p.C;
-          const int c = kk - tap * p.C;
-          const int t = tap / RS;
-          const int rs = tap - t * RS;
-          const int r = rs / p.S;
-          const int s = rs - r * p.S;
-          tapoff = (((long long)t * p.Hp + r) * p.Wp + s) * p.C + c;
-        }
-        const uint32_t dst = row_dst + (uint32_t)stage * kATileBytes;
+    // ------------------------------------------------------------------------------ A gather
+    if (!im2col) {
+      const int pt = threadIdx.x - 128;
+      const int q = pt & 7;    // 16-byte chunk of the 128-byte K block
+      const int rb = pt >> 3;  // rows rb, rb+16, ..., rb+112
+      const uint32_t row_dst = sA_u32 + (uint32_t)rb * 128u + (uint32_t)((q ^ (rb & 7)) << 4);
+      const int RS = p.R * p.S;
+      uint32_t it = 0, signaled = 0;
+      int inflight = 0;
+      bool aborted = false;
+      for (int u = blockIdx.x; u < p.num_units && !aborted; u += gridDim.x) {
+        const Unit un = decode_unit(p, u);
+        long long rowoff[8];
+        bool rowok[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const bool ok = kok && rowok[i];
-          const uint8_t* src = ok ? p.xp + rowoff[i] + tapoff : p.xp;
-          cp_async_16_zfill(dst + (uint32_t)i * 2048u, src, ok ? 16u : 0u);
+          const int m = un.m_tile * kBlockM + rb + 16 * i;
+          rowok[i] = !kRowChk || m < p.npq;
+          const int mm = rowok[i] ? m : 0;
+          const int n = mm / p.dhw;
+          const int pix = mm - n * p.dhw;
+          const int wo = pix % p.Wo;
+          const int t2 = pix / p.Wo;
+          const int ho = t2 % p.Ho;
+          const int od = t2 / p.Ho;
+          rowoff[i] = ((((long long)n * p.Dp + od * p.sd) * p.Hp + ho * p.sh) * p.Wp + wo * p.sw) * p.C;
         }
-        cp_async_commit();
-        ++it;
-        if (++inflight > kLoaderLag) {
-          cp_async_wait_group<kLoaderLag>();
-          fence_proxy_async_smem();
-          mbar_arrive(fullA(signaled % S));
-          ++signaled;
-          --inflight;
-        }
-      }
-    }
-    cp_async_wait_all();
-    fence_proxy_async_smem();
-    if (!aborted) {
-      for (; inflight > 0; --inflight, ++signaled) mbar_arrive(fullA(signaled % S));
-    }
-  } else if (warp == 8) {
-    // ------------------------------------------------------------------------------ B loader
-    if (lane == 0) {
-      uint32_t it = 0;
-      const bool skip_first = (p.debug_flags & 1) != 0;
-      for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-        const Unit un = decode_unit(p, u);
-        bool aborted = false;
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
           const int stage = it % S;
           if (!wait_bounded(empty(stage), ((it / S) & 1) ^ 1, ab, kStatusWaitEmpty)) {
             aborted = true;
             break;
           }
+          const int kk = kb * kBlockK + q * 16;
+          const bool kok = kk < p.kg;
+          long long tapoff = 0;
+          if (kok) {
+            const int tap = kk / p.C;
+            const int c = kk - tap * p.C;
+            const int t = tap / RS;
+            const int rs = tap - t * RS;
+            const int r = rs / p.S;
+            const int s = rs - r * p.S;
+            tapoff = (((long long)t * p.Hp + r) * p.Wp + s) * p.C + c;
+          }
+          const uint32_t dst = row_dst + (uint32_t)stage * kATileBytes;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const bool ok = kok && rowok[i];
+            const uint8_t* src = ok ? p.xp + rowoff[i] + tapoff : p.xp;
+            cp_async_16_zfill(dst + (uint32_t)i * 2048u, src, ok ? 16u : 0u);
+          }
+          cp_async_commit();
+          ++it;
+          if (++inflight > kLoaderLag) {
+            cp_async_wait_group<kLoaderLag>();
+            fence_proxy_async_smem();
+            mbar_arrive(fullA(signaled % S));
+            ++signaled;
+            --inflight;
+          }
+        }
+      }
+      cp_async_wait_all();
+      fence_proxy_async_smem();
+      if (!aborted) {
+        for (; inflight > 0; --inflight, ++signaled) mbar_arrive(fullA(signaled % S));
+      }
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------------------------ TMA loader
+    if (lane == 0) {
+      uint32_t it = 0;
+      Ring ring;
+      const bool skip_first = (p.debug_flags & 1) != 0;
+      const int RS = p.R * p.S;
+      for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        const Unit un = decode_unit(p, u);
+        // im2col start pixel of the tile's first output position (the TMA walks the next 127)
+        int n0 = 0, w0 = 0, h0 = 0, d0 = 0;
+        if (im2col) {
+          const int m0 = un.m_tile * kBlockM;
+          n0 = m0 / p.dhw;
+          const int pix = m0 - n0 * p.dhw;
+          const int ow = pix % p.Wo;
+          const int t2 = pix / p.Wo;
+          w0 = ow * p.sw - p.pw;
+          h0 = (t2 % p.Ho) * p.sh - p.ph;
+          d0 = (t2 / p.Ho) * p.sd - p.pd;
+        }
+        // (tap, channel) of the unit's first A sub-tile; later ones follow by counting
+        int c = 0, ts = 0, tr = 0, tt = 0;
+        if (im2col) {
+          const int kk = un.kb0 * kBlockK;
+          const int tap = kk / p.C;
+          c = kk - tap * p.C;
+          tt = tap / RS;
+          const int rs = tap - tt * RS;
+          tr = rs / p.S;
+          ts = rs - tr * p.S;
+        }
+        bool aborted = false;
+        for (int kb = un.kb0; kb < un.kb1; ++kb) {
+          const int stage = ring.stage;
+          if (!wait_bounded(empty(stage), ring.phase ^ 1u, ab, kStatusWaitEmpty)) {
+            aborted = true;
+            break;
+          }
+          const int kk0 = kb * kBlockK;
+          const int nsub = im2col ? min(kBlockK, p.kg - kk0) / p.a_cb : 0;
           if (!(skip_first && it == 0)) {
-            mbar_arrive_expect_tx(fullB(stage), b_bytes);
-            tma_load_2d(sB_u32 + (uint32_t)stage * b_bytes, &wmap, fullB(stage), kb * kBlockK,
+            mbar_arrive_expect_tx(fullB(stage), b_bytes + (uint32_t)(nsub * p.a_cb * kBlockM));
+            tma_load_2d(sB_u32 + (uint32_t)stage * b_bytes, &wmap, fullB(stage), kk0,
                         un.n_tile * p.block_n);
           }
+          const uint32_t a_dst = sA_u32 + (uint32_t)stage * kATileBytes;
+          for (int q = 0; q < nsub; ++q) {
+            if (!(skip_first && it == 0))
+              tma_load_im2col_5d(a_dst + (uint32_t)(q * kBlockM * p.a_cb), &xmap, fullB(stage), c,
+                                 w0, h0, d0, n0, (uint16_t)ts, (uint16_t)tr, (uint16_t)tt);
+            c += p.a_cb;
+            if (c == p.C) {
+              c = 0;
+              if (++ts == p.S) {
+                ts = 0;
+                if (++tr == p.R) {
+                  tr = 0;
+                  ++tt;
+                }
+              }
+            }
+          }
           ++it;
+          ring.next(S);
         }
         if (aborted) break;
       }
@@ -256,7 +323,22 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     // ------------------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc = make_idesc_e4m3_f32(kBlockM, (uint32_t)p.block_n);
-      uint32_t it = 0, tc = 0;
+      // A rows are 128 bytes (SW128) on the gather route, a_cb bytes on the im2col route. K step
+      // j covers bytes [32j, 32j+32) of the 128-byte K block: in A it lies in sub-tile 32j / a_cb
+      // at byte 32j % a_cb of each row, in B at byte 32j of each 128-byte row. Everything that
+      // does not depend on the stage is computed once, so issuing a block is a few adds.
+      const uint32_t a_cb = im2col ? (uint32_t)p.a_cb : (uint32_t)kBlockK;
+      const uint32_t a_layout =
+          a_cb == 128 ? kLayoutSw128 : (a_cb == 64 ? kLayoutSw64 : kLayoutSw32);
+      const uint64_t adesc0 = make_kmajor_desc(sA_u32, a_cb, a_layout);
+      const uint64_t bdesc0 = make_sw128_kmajor_desc(sB_u32);
+      uint32_t a_step[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        a_step[j] = (((uint32_t)(j * kMmaK) / a_cb) * kBlockM * a_cb + (uint32_t)(j * kMmaK) % a_cb) >> 4;
+      const uint32_t a_stage16 = kATileBytes >> 4, b_stage16 = b_bytes >> 4;
+      uint32_t tc = 0;
+      Ring ring;
       bool aborted = false;
       for (int u = blockIdx.x; u < p.num_units && !aborted; u += gridDim.x, ++tc) {
         const Unit un = decode_unit(p, u);
@@ -265,25 +347,32 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)buf * p.acc_stride;
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
-          const int stage = it % S;
-          const uint32_t ph = (it / S) & 1;
-          if (!wait_bounded(fullA(stage), ph, ab, kStatusWaitFull) ||
+          const int stage = ring.stage;
+          const uint32_t ph = ring.phase;
+          if ((!im2col && !wait_bounded(fullA(stage), ph, ab, kStatusWaitFull)) ||
               !wait_bounded(fullB(stage), ph, ab, kStatusWaitFull)) {
             aborted = true;
             break;
           }
           tc_fence_after();
+          const uint64_t adesc = adesc0 + (uint64_t)((uint32_t)stage * a_stage16);
+          const uint64_t bdesc = bdesc0 + (uint64_t)((uint32_t)stage * b_stage16);
+          const uint32_t acc0 = kb > un.kb0 ? 1u : 0u;
           const int rem = p.kg - kb * kBlockK;
-          const int nsteps = rem >= kBlockK ? kBlockK / kMmaK : (rem + kMmaK - 1) / kMmaK;
-          const uint64_t adesc = make_sw128_kmajor_desc(sA_u32 + (uint32_t)stage * kATileBytes);
-          const uint64_t bdesc = make_sw128_kmajor_desc(sB_u32 + (uint32_t)stage * b_bytes);
-          for (int j = 0; j < nsteps; ++j) {
-            // +32 bytes of K per step inside the 128-byte swizzle row: +2 in 16-byte units
-            mma_f8f6f4(d_tmem, adesc + 2u * j, bdesc + 2u * j, idesc,
-                       (kb > un.kb0 || j > 0) ? 1u : 0u);
+          if (rem >= kBlockK) {
+            mma_f8f6f4(d_tmem, adesc + a_step[0], bdesc, idesc, acc0);
+            mma_f8f6f4(d_tmem, adesc + a_step[1], bdesc + 2u, idesc, 1u);
+            mma_f8f6f4(d_tmem, adesc + a_step[2], bdesc + 4u, idesc, 1u);
+            mma_f8f6f4(d_tmem, adesc + a_step[3], bdesc + 6u, idesc, 1u);
+          } else {
+            const int nsteps = (rem + kMmaK - 1) / kMmaK;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (j < nsteps)
+                mma_f8f6f4(d_tmem, adesc + a_step[j], bdesc + 2u * j, idesc, j > 0 ? 1u : acc0);
           }
           mma_commit(empty(stage));
-          ++it;
+          ring.next(S);
         }
         if (aborted) break;
         mma_commit(accFull(buf));
@@ -314,13 +403,13 @@ cudaError_t conv_set_smem_attr(size_t smem_bytes) {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
 }
 
-cudaError_t launch_conv(const ConvParams& p, const CUtensorMap& wmap, bool row_chk, int grid,
-                        cudaStream_t stream) {
+cudaError_t launch_conv(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
+                        bool row_chk, int grid, cudaStream_t stream) {
   const size_t smem = conv_smem_bytes(p.block_n, p.stages);
   if (row_chk)
-    conv3d_fp8_tc_kernel<true><<<grid, kNumThreads, smem, stream>>>(wmap, p);
+    conv3d_fp8_tc_kernel<true><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
   else
-    conv3d_fp8_tc_kernel<false><<<grid, kNumThreads, smem, stream>>>(wmap, p);
+    conv3d_fp8_tc_kernel<false><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
   return cudaGetLastError();
 }
 

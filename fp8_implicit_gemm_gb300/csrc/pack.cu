@@ -2,10 +2,11 @@
 //
 // The GEMM view orders K_gemm as (tap, channel) with the channel innermost, so that one row of the
 // A tile for one tap is C contiguous bytes of one input pixel. The caller's x is NCDHW (channel
-// outermost), so it is copied once per run into a channels-last buffer with an explicit zero halo
-// of `pad` pixels on every spatial side; with the halo in memory an A-tile row needs no bounds
-// test, only the padded-row test (row < npq). The weights are re-laid from KCTRS to K x taps x C
-// to match.
+// outermost), so it is copied once per run into a channels-last buffer. For the TMA im2col route
+// the copy is plain NDHWC (the TMA unit zero-fills taps outside the volume); for the cp.async
+// gather route it carries an explicit zero halo of `pad` pixels on every spatial side, so that an
+// A-tile row needs no bounds test, only the padded-row test (row < npq). The weights are re-laid
+// from KCTRS to K x taps x C to match.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -31,7 +32,7 @@ __global__ void __launch_bounds__(256) pack_kernel(ConvParams p, long long x_ite
       const int hp = (int)(prow % p.Hp);
       const int dp = (int)((prow / p.Hp) % p.Dp);
       const int n = (int)(prow / ((long long)p.Hp * p.Dp));
-      const int d = dp - p.pd, h = hp - p.ph, w = wpos - p.pw;
+      const int d = dp - p.pk_pd, h = hp - p.pk_ph, w = wpos - p.pk_pw;
       if (d >= 0 && d < p.D && h >= 0 && h < p.H && w >= 0 && w < p.W) {
         const long long plane = (long long)p.D * p.H * p.W;
         const uint8_t* src =

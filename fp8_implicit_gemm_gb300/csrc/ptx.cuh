@@ -99,6 +99,19 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// im2col load of a channels-last 5D tensor (C, W, H, D, N): `pixels per column` consecutive output
+// positions starting at the pixel (w, h, d, n), each shifted by the filter tap (ow, oh, od), with
+// `channels per pixel` channels from channel c; positions outside the tensor read zero.
+__device__ __forceinline__ void tma_load_im2col_5d(uint32_t dst, const CUtensorMap* map,
+                                                   uint32_t bar, int c, int w, int h, int d, int n,
+                                                   uint16_t ow, uint16_t oh, uint16_t od) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.im2col.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], {%8, %9, %10};" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c), "r"(w), "r"(h), "r"(d), "r"(n), "r"(bar),
+      "h"(ow), "h"(oh), "h"(od)
+      : "memory");
+}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -157,18 +170,25 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor for a K-major operand tile written with the 128-byte swizzle:
-// rows of 128 bytes, 8-row atoms of 1024 bytes stacked contiguously (stride-dimension offset
-// 1024 B), leading-dimension offset unused for this layout, descriptor version 1 (bits 46-47),
-// layout type 2 = SWIZZLE_128B (bits 61-63). The tile base must be 1024-byte aligned.
-__device__ __forceinline__ uint64_t make_sw128_kmajor_desc(uint32_t smem_addr) {
+// Layout-type field (bits 61-63) of a shared-memory matrix descriptor.
+enum : uint32_t { kLayoutSw128 = 2, kLayoutSw64 = 4, kLayoutSw32 = 6 };
+
+// Shared-memory matrix descriptor for a K-major operand tile whose rows are `row_bytes` (32, 64
+// or 128) bytes long and were written with the matching swizzle: 8-row atoms of 8*row_bytes
+// stacked contiguously (stride-dimension offset), leading-dimension offset unused for swizzled
+// K-major layouts, descriptor version 1 (bits 46-47). The atom base must be aligned to its size.
+__device__ __forceinline__ uint64_t make_kmajor_desc(uint32_t smem_addr, uint32_t row_bytes,
+                                                     uint32_t layout) {
   uint64_t d = 0;
   d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);   // start address, bits 0-13
   d |= static_cast<uint64_t>(1u) << 16;                       // leading byte offset (unused)
-  d |= static_cast<uint64_t>(1024u >> 4) << 32;               // stride byte offset, bits 32-45
+  d |= static_cast<uint64_t>((8u * row_bytes) >> 4) << 32;    // stride byte offset, bits 32-45
   d |= static_cast<uint64_t>(1u) << 46;                       // version
-  d |= static_cast<uint64_t>(2u) << 61;                       // SWIZZLE_128B
+  d |= static_cast<uint64_t>(layout) << 61;                   // swizzle mode
   return d;
+}
+__device__ __forceinline__ uint64_t make_sw128_kmajor_desc(uint32_t smem_addr) {
+  return make_kmajor_desc(smem_addr, 128u, kLayoutSw128);
 }
 
 // Instruction descriptor of tcgen05.mma kind::f8f6f4: D fp32 (bits 4-5 = 1), A and B e4m3

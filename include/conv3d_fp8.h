@@ -57,6 +57,10 @@ typedef struct {
     int debug_flags;     /* test-only: bit 0 makes the weight-tile loader skip its first arrival,
                             so the MMA warp's bounded wait must run out (exercises the error
                             path without faulting anything) */
+    int route;           /* 0: the library chooses; 1: A by cp.async gathers from a zero-padded
+                            channels-last copy of x; 2: A by TMA im2col loads (EUNSUPPORTED
+                            unless C % 32 == 0, strides <= 8 and -16 <= -pad, pad - (filter-1)
+                            <= 15 on every axis) */
 } conv3d_fp8_options;
 
 /* What a plan (or a would-be plan) decided. */
@@ -74,6 +78,7 @@ typedef struct {
     int grid;                 /* persistent CTAs launched by the main kernel */
     int sm_count;
     size_t workspace_bytes;   /* device workspace the plan owns */
+    int route;                /* 1: cp.async gather route, 2: TMA im2col route (as in options) */
 } conv3d_fp8_plan_info;
 
 /*

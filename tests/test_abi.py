@@ -66,6 +66,21 @@ def test_describe_configs(lib):
         assert i["workspace_bytes"] > 0
 
 
+def test_describe_routes(lib):
+    # every workload has C % 32 == 0 and unit paddings: TMA im2col
+    assert all(_describe(s)["route"] == 2 for s in synth.CONFIGS)
+    odd = synth.ConvShape(1, 48, 4, 4, 4, 16)
+    assert _describe(odd)["route"] == 1                         # C % 32 != 0 -> gather
+    assert capi.conv3d_fp8_describe_status(1, 48, 4, 4, 4, 16, 3, 3, 3, 1, 1, 152,
+                                           route=2) == capi.CONV3D_EUNSUPPORTED
+    assert _describe(synth.CONFIGS[0], route=1)["route"] == 1   # forced gather
+    big_pad = synth.ConvShape(1, 32, 4, 4, 4, 16, pad=17)       # corner beyond [-16, 15]
+    assert _describe(big_pad)["route"] == 1
+    # the gather route's packed copy carries the zero halo, the im2col one does not
+    s = synth.CONFIGS[2]
+    assert _describe(s, route=1)["workspace_bytes"] > _describe(s, route=2)["workspace_bytes"]
+
+
 def test_describe_forced_options(lib):
     s = synth.CONFIGS[1]
     i = _describe(s, splits=4, block_n=64, max_ctas=10)

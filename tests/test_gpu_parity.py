@@ -28,10 +28,15 @@ def _full_case(shape, seed, **opts):
         g.close()
 
 
+ROUTES = {"gather": 1, "im2col": 2}
+
+
+@pytest.mark.parametrize("route", ["gather", "im2col"])
 @pytest.mark.parametrize("cfg", [0, 1, 3])
-def test_config_full_output(cfg):
-    res, info = _full_case(synth.CONFIGS[cfg], synth.config_seed(cfg))
-    print(cfg, res, info["splits"], info["block_n"])
+def test_config_full_output(cfg, route):
+    res, info = _full_case(synth.CONFIGS[cfg], synth.config_seed(cfg), route=ROUTES[route])
+    assert info["route"] == ROUTES[route]
+    print(cfg, route, res, info["splits"], info["block_n"])
 
 
 @pytest.mark.parametrize("cfg", [2, 4])
@@ -72,7 +77,13 @@ ODD = [
 @pytest.mark.parametrize("i", range(len(ODD)))
 def test_odd_shapes(i):
     res, info = _full_case(ODD[i], 77 + i)
-    print(ODD[i], res, info["splits"], info["block_n"])
+    print(ODD[i], res, info["splits"], info["block_n"], info["route"])
+
+
+@pytest.mark.parametrize("i", [i for i, s in enumerate(ODD) if s.C % 32 == 0])
+def test_odd_shapes_gather_route(i):
+    res, info = _full_case(ODD[i], 77 + i, route=ROUTES["gather"])
+    assert info["route"] == ROUTES["gather"]
 
 
 @pytest.mark.parametrize("splits", [1, 2, 3, 7])
