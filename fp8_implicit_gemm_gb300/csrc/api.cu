@@ -72,7 +72,7 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   const long long kg = taps * C;
   conv3d_fp8_options o{};
   if (opts) o = *opts;
-  if (o.route < 0 || o.route > 2) return CONV3D_EINVAL;
+  if (o.route < 0 || o.route > 3 || o.cta_pair < 0 || o.cta_pair > 2) return CONV3D_EINVAL;
   // The TMA im2col route needs C in whole 32-byte sub-tile rows and bounding-box corners
   // (-pad, pad - (filter - 1)) inside the [-16, 15] range of a rank-5 im2col tensor map.
   bool im2col_ok = (C % 32 == 0);
@@ -82,10 +82,28 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
     if (lower < -16 || lower > 15 || upper < -16 || upper > 15 || stride[i] > 8) im2col_ok = false;
   }
   if (o.route == 2 && !im2col_ok) return CONV3D_EUNSUPPORTED;
-  const int route = (o.route == 1 || !im2col_ok) ? kRouteGather : kRouteIm2col;
+  // The padded-grid route (CTA pairs only) needs stride 1 on every axis, whole 32-byte channel
+  // blocks and an A tile of 128 + S - 1 <= 256 rows. By default it is taken when the rows of the
+  // padded grid that are not outputs cost at most 30% extra MMA work.
+  const bool grid_ok = C % 32 == 0 && stride[0] == 1 && stride[1] == 1 && stride[2] == 1 &&
+                       S <= 129 && o.cta_pair != 1;
+  if (o.route == 3 && !grid_ok) return CONV3D_EUNSUPPORTED;
+  const double grid_overhead =
+      (double)(H + 2LL * pad[1]) * (double)(W + 2LL * pad[2]) / ((double)Ho * (double)Wo);
+  int route;
+  if (o.route == 1)
+    route = kRouteGather;
+  else if (o.route == 2)
+    route = kRouteIm2col;
+  else if (o.route == 3)
+    route = kRouteGrid;
+  else if (grid_ok && grid_overhead <= 1.3 && npq > kBlockM)
+    route = kRouteGrid;
+  else
+    route = im2col_ok ? kRouteIm2col : kRouteGather;
   const int a_cb = C % 128 == 0 ? 128 : (C % 64 == 0 ? 64 : 32);
-  const int halo[3] = {route == kRouteGather ? pad[0] : 0, route == kRouteGather ? pad[1] : 0,
-                       route == kRouteGather ? pad[2] : 0};
+  const bool halo_on = route != kRouteIm2col;  // gather and grid routes read a zero-padded copy
+  const int halo[3] = {halo_on ? pad[0] : 0, halo_on ? pad[1] : 0, halo_on ? pad[2] : 0};
   const long long Dp = D + 2LL * halo[0], Hp = H + 2LL * halo[1], Wp = W + 2LL * halo[2];
   const long long y_elems = npq * K;
   const long long x_elems = (long long)N * C * D * H * W;
@@ -100,16 +118,32 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   if (block_n == 0) block_n = (int)std::min<long long>(256, round_up(K, 32));
   if (block_n < 32 || block_n > 256 || block_n % 32 != 0) return CONV3D_EINVAL;
 
-  const long long m_tiles = ceil_div(npq, kBlockM);
+  // CTA pairs (cta_group::2, 256-row tiles) run the im2col and padded-grid routes; by default
+  // the im2col route uses them whenever the problem has more than one 128-row tile.
+  if (o.cta_pair == 2 && route == kRouteGather) return CONV3D_EUNSUPPORTED;
+  const bool pair = route == kRouteGrid ||
+                    (route == kRouteIm2col &&
+                     (o.cta_pair == 2 || (o.cta_pair == 0 && npq > kBlockM)));
+  const int block_m = pair ? 2 * kBlockM : kBlockM;
+  const long long slots = pair ? std::max(1, sm_count / 2) : sm_count;  // co-resident units
+
+  // grid route: the tiles of one image cover the first Do planes of its padded output grid
+  const long long tiles_per_image =
+      route == kRouteGrid ? ceil_div((long long)Do * Hp * Wp, block_m) : 0;
+  const long long m_tiles = route == kRouteGrid ? N * tiles_per_image : ceil_div(npq, block_m);
   const long long n_tiles = ceil_div(K, block_n);
-  const long long k_blocks = ceil_div(kg, kBlockK);
+  // K blocks: 128 bytes of K_gemm, or on the grid route one (t, r, channel block) group of S taps
+  const long long k_blocks =
+      route == kRouteGrid ? (long long)T * R * (C / a_cb) : ceil_div(kg, kBlockK);
+  if (route == kRouteGrid && (long long)N * Dp * Hp * Wp + 256 >= (1LL << 31))
+    return CONV3D_EUNSUPPORTED;
   const long long tiles = m_tiles * n_tiles;
   long long splits = o.splits;
   if (splits < 0) return CONV3D_EINVAL;
   if (splits == 0) {
     splits = 1;
-    if (tiles * 2 <= sm_count && k_blocks >= 8)
-      splits = std::max<long long>(1, std::min<long long>(sm_count / tiles, k_blocks / 4));
+    if (tiles * 2 <= slots && k_blocks >= 8)
+      splits = std::max<long long>(1, std::min<long long>(slots / tiles, k_blocks / 4));
   }
   splits = std::min(splits, k_blocks);
   const long long kbps = ceil_div(k_blocks, splits);
@@ -117,11 +151,16 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   const long long units = tiles * splits;
   if (units >= (1LL << 31)) return CONV3D_EUNSUPPORTED;
 
-  const long long stage_bytes = kATileBytes + (long long)block_n * kBlockK;
+  long long stage_bytes = kATileBytes + (long long)(pair ? block_n / 2 : block_n) * kBlockK;
+  if (route == kRouteGrid)
+    stage_bytes = round_up((long long)(kBlockM + S - 1) * a_cb, 1024) +
+                  round_up((long long)S * (block_n / 2) * a_cb, 1024);
   const int stages = (int)std::min<long long>(kMaxStages, kSmemBudget / stage_bytes);
-  if (stages < 3) return CONV3D_EUNSUPPORTED;
-  long long grid = std::min<long long>(units, sm_count);
-  if (o.max_ctas > 0) grid = std::min<long long>(grid, o.max_ctas);
+  if (stages < (route == kRouteGrid ? 2 : 3)) return CONV3D_EUNSUPPORTED;
+  long long grid = std::min<long long>(units, slots);
+  if (o.max_ctas > 0)
+    grid = std::min<long long>(grid, pair ? std::max(1, o.max_ctas / 2) : o.max_ctas);
+  if (pair) grid *= 2;  // two CTAs per unit
   if (o.max_ctas < 0 || o.wait_timeout_ms < 0) return CONV3D_EINVAL;
 
   Layout L{};
@@ -130,7 +169,7 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   L.wp_off = (size_t)round_up((long long)L.xp_off + L.xp_bytes, 256);
   L.wp_bytes = (size_t)(K * kg);
   L.part_off = (size_t)round_up((long long)L.wp_off + L.wp_bytes, 256);
-  L.part_bytes = splits > 1 ? (size_t)(tiles * splits * block_n * kBlockM * 4) : 0;
+  L.part_bytes = splits > 1 ? (size_t)(tiles * splits * block_n * block_m * 4) : 0;
   L.status_off = (size_t)round_up((long long)L.part_off + L.part_bytes, 256);
   L.total = L.status_off + 256;
 
@@ -140,7 +179,7 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   info->Wo = Wo;
   info->npq = npq;
   info->k_gemm = (int)kg;
-  info->block_m = kBlockM;
+  info->block_m = block_m;
   info->block_n = block_n;
   info->m_tiles = (int)m_tiles;
   info->n_tiles = (int)n_tiles;
@@ -148,11 +187,12 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   info->splits = (int)splits;
   info->k_blocks_per_split = (int)kbps;
   info->stages = stages;
-  info->row_chk = (npq % kBlockM) != 0;
+  info->row_chk = route == kRouteGrid ? 1 : (npq % block_m) != 0;
   info->grid = (int)grid;
   info->sm_count = sm_count;
   info->workspace_bytes = L.total;
-  info->route = route == kRouteIm2col ? 2 : 1;
+  info->route = route == kRouteGrid ? 3 : (route == kRouteIm2col ? 2 : 1);
+  info->cta_pair = pair ? 2 : 1;
 
   if (pp) {
     ConvParams& p = *pp;
@@ -166,9 +206,12 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
     p.pk_pd = halo[0]; p.pk_ph = halo[1]; p.pk_pw = halo[2];
     p.Dp = (int)Dp; p.Hp = (int)Hp; p.Wp = (int)Wp;
     p.dhw = (int)dhw;
+    p.tiles_per_image = (int)tiles_per_image;
     p.npq = (int)npq;
     p.taps = (int)taps;
     p.kg = (int)kg;
+    p.pair = pair ? 1 : 0;
+    p.block_m = block_m;
     p.block_n = block_n;
     p.m_tiles = (int)m_tiles;
     p.n_tiles = (int)n_tiles;
@@ -205,17 +248,24 @@ EncodeTiledFn get_encode_tiled() {
   return fn;
 }
 
-// The packed weights as a 2D tensor [K rows][kg bytes]; a box is one 128-byte K block of
-// block_n rows, written to shared memory with the 128-byte swizzle the MMA descriptor expects.
-conv3d_status encode_weight_map(CUtensorMap* map, void* wp, int K, int kg, int block_n) {
+CUtensorMapSwizzle swizzle_for(int row_bytes) {
+  return row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+         : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                           : CU_TENSOR_MAP_SWIZZLE_32B;
+}
+
+// A 2D byte tensor [rows][cols] (row pitch = cols); a box is box_cols bytes of box_rows rows,
+// written to shared memory with the swizzle of its row width.
+conv3d_status encode_2d(CUtensorMap* map, void* base, long long rows, long long cols, int box_cols,
+                        int box_rows) {
   EncodeTiledFn enc = get_encode_tiled();
   if (!enc) return CONV3D_ECUDA;
-  const cuuint64_t dims[2] = {(cuuint64_t)kg, (cuuint64_t)K};
-  const cuuint64_t strides[1] = {(cuuint64_t)kg};
-  const cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)block_n};
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, wp, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(box_cols),
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? CONV3D_OK : CONV3D_ECUDA;
 }
@@ -260,6 +310,22 @@ conv3d_status encode_im2col_map(CUtensorMap* map, void* xcl, const ConvParams& p
                    (cuuint32_t)p.a_cb, (cuuint32_t)kBlockM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? CONV3D_OK : CONV3D_ECUDA;
+}
+
+// Tensor maps of a plan. B: the packed weights [K][kg]; a box is one K block (128 bytes, or a_cb
+// bytes of one tap on the grid route) of block_n rows (block_n / 2 per CTA of a pair).
+// A: im2col map of the unpadded channels-last x (im2col route), or 2D tiles of 128 + S - 1 rows
+// of the padded channels-last x viewed as [N*Dp*Hp*Wp][C] (grid route).
+conv3d_status encode_maps(CUtensorMap* wmap, CUtensorMap* xmap, const ConvParams& p) {
+  const int b_rows = p.pair ? p.block_n / 2 : p.block_n;
+  const int b_cols = p.route == kRouteGrid ? p.a_cb : kBlockK;
+  conv3d_status st = encode_2d(wmap, p.wp, p.K, p.kg, b_cols, b_rows);
+  if (st != CONV3D_OK) return st;
+  if (p.route == kRouteIm2col) return encode_im2col_map(xmap, p.xp, p);
+  if (p.route == kRouteGrid)
+    return encode_2d(xmap, p.xp, (long long)p.N * p.Dp * p.Hp * p.Wp, p.C, p.a_cb,
+                     kBlockM + p.S - 1);
+  return CONV3D_OK;
 }
 
 struct DeviceGuard {
@@ -327,7 +393,8 @@ conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t* out, int N, int C, int D, in
     plan->stride[i] = stride[i];
     plan->pad[i] = pad[i];
   }
-  const size_t smem = conv_smem_bytes(plan->p.block_n, plan->p.stages);
+  const size_t smem = plan->p.pair ? conv_pair_smem_bytes(plan->p)
+                                    : conv_smem_bytes(plan->p.block_n, plan->p.stages);
   if ((int)smem > prop.sharedMemPerBlockOptin) {
     delete plan;
     return CONV3D_EUNSUPPORTED;
@@ -353,9 +420,11 @@ conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t* out, int N, int C, int D, in
     delete plan;
     return CONV3D_ECUDA;
   }
-  st = encode_weight_map(&plan->wmap, plan->p.wp, K, plan->p.kg, plan->p.block_n);
-  if (st == CONV3D_OK && plan->p.route == kRouteIm2col)
-    st = encode_im2col_map(&plan->xmap, plan->p.xp, plan->p);
+  if (plan->p.pair) {  // never more clusters than can be resident at once
+    const int clusters = conv_pair_max_active_clusters(plan->p);
+    if (clusters > 0 && plan->info.grid > 2 * clusters) plan->info.grid = 2 * clusters;
+  }
+  st = encode_maps(&plan->wmap, &plan->xmap, plan->p);
   if (st != CONV3D_OK) {
     cudaFree(plan->workspace);
     delete plan;
@@ -569,9 +638,12 @@ extern "C" conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int 
   p.scale_x = scale_x;
   p.scale_w = scale_w;
 
+  if (p.pair) {  // never more clusters than can be resident at once
+    const int clusters = conv_pair_max_active_clusters(p);
+    if (clusters > 0 && info.grid > 2 * clusters) info.grid = 2 * clusters;
+  }
   CUtensorMap wmap{}, xmap{};
-  st = encode_weight_map(&wmap, p.wp, K, p.kg, p.block_n);
-  if (st == CONV3D_OK && p.route == kRouteIm2col) st = encode_im2col_map(&xmap, p.xp, p);
+  st = encode_maps(&wmap, &xmap, p);
   if (st != CONV3D_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(p.status, 0, sizeof(int), s) != cudaSuccess) return CONV3D_ECUDA;

@@ -19,6 +19,9 @@ constexpr int kMaxStages = 8;
 enum : int {
   kRouteGather = 0,  // 16-byte cp.async gathers from a zero-padded channels-last copy of x
   kRouteIm2col = 1,  // TMA im2col loads from an unpadded channels-last copy (C % 32 == 0)
+  kRouteGrid = 2,    // stride 1: M indexes the zero-padded output grid, so every tap is a row
+                     // shift of one 2D view of the padded channels-last copy; one TMA tile of
+                     // 128 + S - 1 rows feeds the S taps along W (CTA pairs only)
 };
 
 // Status-word bits recorded by kernels whose bounded waits ran out.
@@ -40,10 +43,13 @@ struct ConvParams {
   int pk_pd, pk_ph, pk_pw;  // zero halo of the packed channels-last x (gather route only)
   int Dp, Hp, Wp;        // extents of the packed channels-last copy of x (halo included)
   int dhw;               // Do*Ho*Wo
+  int tiles_per_image;   // padded-grid route: M tiles per image (rows of d < Do planes only)
   int npq;               // N*dhw, the M of the GEMM view
   int taps;              // T*R*S
   int kg;                // taps*C, the K of the GEMM view
   // tiling
+  int pair;              // 1: CTA-pair kernel (cta_group::2, block_m = 256); 0: one-CTA kernel
+  int block_m;           // M tile: 128 (one CTA) or 256 (CTA pair)
   int block_n;           // N tile (multiple of 32, <= 256)
   int m_tiles, n_tiles, k_blocks, splits, kb_per_split, num_units;
   int stages;
@@ -57,7 +63,7 @@ struct ConvParams {
   uint16_t* y;           // bf16 NCDHW (caller's)
   const float* scale_x;
   const float* scale_w;
-  float* partials;       // fp32 [tile][split][block_n][128] when splits > 1 (workspace)
+  float* partials;       // fp32 [tile][split][block_n][block_m] when splits > 1 (workspace)
   int* status;           // status word (workspace)
   unsigned long long timeout_ns;
   int debug_flags;
@@ -69,6 +75,11 @@ cudaError_t launch_conv(const ConvParams& p, const CUtensorMap& wmap, const CUte
                         bool row_chk, int grid, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ConvParams& p, bool row_chk, cudaStream_t stream);
 size_t conv_smem_bytes(int block_n, int stages);
-cudaError_t conv_set_smem_attr(size_t smem_bytes);
+cudaError_t conv_set_smem_attr(size_t smem_bytes);  // both kernels
+cudaError_t launch_conv_pair(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
+                             bool row_chk, int grid, cudaStream_t stream);
+size_t conv_pair_smem_bytes(const ConvParams& p);
+cudaError_t conv_pair_set_smem_attr(size_t smem_bytes);
+int conv_pair_max_active_clusters(const ConvParams& p);  // 0 if the query fails
 
 }  // namespace c3d

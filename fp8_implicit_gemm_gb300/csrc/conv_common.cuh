@@ -1,0 +1,178 @@
+// conv_common.cuh -- device pieces shared by the one-CTA and the CTA-pair implicit-GEMM kernels
+// and by the split-K reduction.
+#pragma once
+#include <cuda_bf16.h>
+
+#include "conv3d_fp8_internal.h"
+#include "ptx.cuh"
+
+namespace c3d {
+
+// One work unit: an M tile of block_m rows, an N tile of block_n channels and a slice [kb0, kb1)
+// of the K blocks. Units are numbered split-fastest, then n-tile, then m-tile.
+struct Unit {
+  int tile, m_tile, n_tile, split, kb0, kb1;
+};
+
+__device__ __forceinline__ Unit decode_unit(const ConvParams& p, int u) {
+  Unit r;
+  r.split = u % p.splits;
+  r.tile = u / p.splits;
+  r.n_tile = r.tile % p.n_tiles;
+  r.m_tile = r.tile / p.n_tiles;
+  r.kb0 = r.split * p.kb_per_split;
+  r.kb1 = min(r.kb0 + p.kb_per_split, p.k_blocks);
+  return r;
+}
+
+// Position in the ring of S pipeline stages: stage index and the parity of its current phase.
+struct Ring {
+  int stage = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int S) {
+    if (++stage == S) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Wait used only while winding down: ignores the abort flag, still bounded.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
+                                           int* status, int code) {
+  if (mbar_try_wait_cluster(bar, parity)) return;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if ((++spins & 63u) == 0 && globaltimer_ns() - t0 > timeout_ns) {
+      atomicOr(status, code);
+      return;
+    }
+  }
+}
+
+// Busy-wait for `ns` nanoseconds (used only on the abort path, to let copies in flight land).
+__device__ __forceinline__ void sleep_ns_bounded(uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 < ns) {
+  }
+}
+
+// Where accumulator row `row_in_tile` of M tile `m_tile` lands in y: whether it is a real output
+// and the NCDHW offset of its channel-0 element (channel k adds k * dhw).
+//  - output-position routes: row m = m_tile * block_m + row_in_tile is output position m of the
+//    GEMM view; it is real iff m < npq (the row guard of the subject page);
+//  - padded-grid route: rows index the zero-padded output grid of one image, tile by tile
+//    (tiles_per_image tiles per image, none straddling two images); position (d, h, w) of that grid
+//    is real iff d < Do, h < Ho and w < Wo.
+struct RowDest {
+  bool valid;
+  long long y_off;
+};
+__device__ __forceinline__ RowDest row_dest(const ConvParams& p, int m_tile, int row_in_tile) {
+  RowDest r;
+  if (p.route == kRouteGrid) {
+    const int n = m_tile / p.tiles_per_image;
+    const int mg = (m_tile - n * p.tiles_per_image) * p.block_m + row_in_tile;
+    const int hw = p.Hp * p.Wp;
+    const int d = mg / hw;
+    const int rem = mg - d * hw;
+    const int h = rem / p.Wp;
+    const int w = rem - h * p.Wp;
+    r.valid = d < p.Do && h < p.Ho && w < p.Wo;
+    r.y_off = r.valid ? (long long)n * p.K * p.dhw + ((long long)d * p.Ho + h) * p.Wo + w : 0;
+  } else {
+    const int m = m_tile * p.block_m + row_in_tile;
+    r.valid = m < p.npq;
+    const int n = m / p.dhw;
+    r.y_off = r.valid ? (long long)n * p.K * p.dhw + (m - n * p.dhw) : 0;
+  }
+  return r;
+}
+
+// Epilogue of one thread: its accumulator row (TMEM lane) of one unit, `trow` = TMEM address of the
+// row's first column in the current buffer. `row_in_tile` is the row within the unit's block_m
+// rows. Without split-K: y = bf16(acc * scale), stored only if the row is a real output and
+// col < K. With split-K: the raw fp32 row goes to the unit's slice of the partials,
+// [tile][split][block_n][block_m]. kRowChk = false compiles the row test out (every row real).
+template <bool kRowChk>
+__device__ __forceinline__ void epilogue_row(const ConvParams& p, const Unit& un, uint32_t trow,
+                                             int row_in_tile, float scale) {
+  const int n0 = un.n_tile * p.block_n;
+  if (p.splits == 1) {
+    const RowDest dst = row_dest(p, un.m_tile, row_in_tile);
+    const bool row_ok = !kRowChk || dst.valid;
+    uint16_t* ybase = p.y + dst.y_off;
+    for (int cc = 0; cc < p.block_n; cc += 32) {
+      if (n0 + cc >= p.K) break;  // warp-uniform
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(trow + cc, r);
+      tmem_ld_wait();
+      if (row_ok) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int col = n0 + cc + j;
+          if (col < p.K) {
+            const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(r[j]) * scale);
+            ybase[(long long)col * p.dhw] = *reinterpret_cast<const uint16_t*>(&b);
+          }
+        }
+      }
+    }
+  } else {
+    float* dst = p.partials +
+                 ((long long)(un.tile * p.splits + un.split) * p.block_n) * p.block_m + row_in_tile;
+    for (int cc = 0; cc < p.block_n; cc += 32) {
+      uint32_t r[32];
+      tmem_ld_32x32b_x32(trow + cc, r);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        __stcg(dst + (long long)(cc + j) * p.block_m, __uint_as_float(r[j]));
+    }
+  }
+}
+
+// The (tap, channel) walk of the im2col loads, in K_gemm order: channel fastest by a_cb, then
+// s, r, t.
+struct TapWalk {
+  int c = 0, s = 0, r = 0, t = 0;
+  __device__ __forceinline__ void start(const ConvParams& p, int kk) {
+    const int tap = kk / p.C;
+    c = kk - tap * p.C;
+    const int RS = p.R * p.S;
+    t = tap / RS;
+    const int rs = tap - t * RS;
+    r = rs / p.S;
+    s = rs - r * p.S;
+  }
+  __device__ __forceinline__ void next(const ConvParams& p) {
+    c += p.a_cb;
+    if (c == p.C) {
+      c = 0;
+      if (++s == p.S) {
+        s = 0;
+        if (++r == p.R) {
+          r = 0;
+          ++t;
+        }
+      }
+    }
+  }
+};
+
+// im2col start pixel (w, h, d, n) of output position m: the filter window's corner.
+struct StartPixel {
+  int w, h, d, n;
+  __device__ __forceinline__ void set(const ConvParams& p, int m) {
+    n = m / p.dhw;
+    const int pix = m - n * p.dhw;
+    const int ow = pix % p.Wo;
+    const int t2 = pix / p.Wo;
+    w = ow * p.sw - p.pw;
+    h = (t2 % p.Ho) * p.sh - p.ph;
+    d = (t2 / p.Ho) * p.sd - p.pd;
+  }
+};
+
+}  // namespace c3d

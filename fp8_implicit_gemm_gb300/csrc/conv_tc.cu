@@ -1,4 +1,5 @@
-// conv_tc.cu -- the implicit-GEMM main kernel: tcgen05 FP8 MMAs with TMEM accumulators.
+// conv_tc.cu -- the implicit-GEMM main kernel on one CTA: tcgen05 FP8 MMAs (M = 128) with TMEM
+// accumulators.
 //
 // GEMM view (the subject page, "Root cause"): row = output position (npq = N*Do*Ho*Wo rows),
 // col = output channel (K columns), reduction over K_gemm = (tap, channel) of T*R*S*C.
@@ -19,55 +20,12 @@
 // epilogue of one tile overlap the main loop of the next. Every wait is bounded; a wait that runs
 // out records a status bit and the whole CTA winds down without faulting.
 #include <cuda_runtime.h>
-#include <cuda_bf16.h>
 
-#include "conv3d_fp8_internal.h"
-#include "ptx.cuh"
+#include "conv_common.cuh"
 
 namespace c3d {
 
 constexpr int kLoaderLag = 2;  // cp.async groups kept in flight before a stage is signalled full
-
-struct Unit {
-  int tile, m_tile, n_tile, split, kb0, kb1;
-};
-
-// Position in the ring of S pipeline stages: stage index and the parity of its current phase.
-struct Ring {
-  int stage = 0;
-  uint32_t phase = 0;
-  __device__ __forceinline__ void next(int S) {
-    if (++stage == S) {
-      stage = 0;
-      phase ^= 1u;
-    }
-  }
-};
-
-__device__ __forceinline__ Unit decode_unit(const ConvParams& p, int u) {
-  Unit r;
-  r.split = u % p.splits;
-  r.tile = u / p.splits;
-  r.n_tile = r.tile % p.n_tiles;
-  r.m_tile = r.tile / p.n_tiles;
-  r.kb0 = r.split * p.kb_per_split;
-  r.kb1 = min(r.kb0 + p.kb_per_split, p.k_blocks);
-  return r;
-}
-
-// Wait used only while winding down: ignores the abort flag, still bounded.
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, uint64_t timeout_ns,
-                                           int* status, int code) {
-  if (mbar_try_wait(bar, parity)) return;
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t spins = 0;
-  while (!mbar_try_wait(bar, parity)) {
-    if ((++spins & 63u) == 0 && globaltimer_ns() - t0 > timeout_ns) {
-      atomicOr(status, code);
-      return;
-    }
-  }
-}
 
 template <bool kRowChk>
 __global__ void __launch_bounds__(kNumThreads, 1)
@@ -128,7 +86,6 @@ __global__ void __launch_bounds__(kNumThreads, 1)
 
   if (warp < 4) {
     // ------------------------------------------------------------------------------ epilogue
-    const int e = threadIdx.x;  // tile row == TMEM lane
     const float scale = __ldg(p.scale_x) * __ldg(p.scale_w);
     uint32_t tc = 0;
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tc) {
@@ -136,40 +93,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int buf = tc & 1;
       if (!wait_bounded(accFull(buf), (tc >> 1) & 1, ab, kStatusWaitAccFull)) break;
       tc_fence_after();
-      const uint32_t trow = tmem_base + (uint32_t)buf * p.acc_stride + ((uint32_t)(warp * 32) << 16);
-      const int n0 = un.n_tile * p.block_n;
-      if (p.splits == 1) {
-        const int m = un.m_tile * kBlockM + e;
-        const bool row_ok = !kRowChk || m < p.npq;
-        const int n = m / p.dhw;
-        const int pix = m - n * p.dhw;
-        uint16_t* ybase = p.y + (long long)n * p.K * p.dhw + pix;
-        for (int cc = 0; cc < p.block_n; cc += 32) {
-          if (n0 + cc >= p.K) break;  // warp-uniform
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(trow + cc, r);
-          tmem_ld_wait();
-          if (row_ok) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int col = n0 + cc + j;
-              if (col < p.K) {
-                const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(r[j]) * scale);
-                ybase[(long long)col * p.dhw] = *reinterpret_cast<const uint16_t*>(&b);
-              }
-            }
-          }
-        }
-      } else {
-        float* dst = p.partials + ((long long)(un.tile * p.splits + un.split) * p.block_n) * kBlockM + e;
-        for (int cc = 0; cc < p.block_n; cc += 32) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(trow + cc, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) __stcg(dst + (long long)(cc + j) * kBlockM, __uint_as_float(r[j]));
-        }
-      }
+      const uint32_t trow =
+          tmem_base + (uint32_t)buf * p.acc_stride + ((uint32_t)(warp * 32) << 16);
+      epilogue_row<kRowChk>(p, un, trow, threadIdx.x, scale);
       tc_fence_before();
       mbar_arrive(accEmpty(buf));
     }
@@ -181,7 +107,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       const int rb = pt >> 3;  // rows rb, rb+16, ..., rb+112
       const uint32_t row_dst = sA_u32 + (uint32_t)rb * 128u + (uint32_t)((q ^ (rb & 7)) << 4);
       const int RS = p.R * p.S;
-      uint32_t it = 0, signaled = 0;
+      Ring ring;
+      uint32_t signaled = 0;
       int inflight = 0;
       bool aborted = false;
       for (int u = blockIdx.x; u < p.num_units && !aborted; u += gridDim.x) {
@@ -199,11 +126,12 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const int t2 = pix / p.Wo;
           const int ho = t2 % p.Ho;
           const int od = t2 / p.Ho;
-          rowoff[i] = ((((long long)n * p.Dp + od * p.sd) * p.Hp + ho * p.sh) * p.Wp + wo * p.sw) * p.C;
+          rowoff[i] =
+              ((((long long)n * p.Dp + od * p.sd) * p.Hp + ho * p.sh) * p.Wp + wo * p.sw) * p.C;
         }
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
-          const int stage = it % S;
-          if (!wait_bounded(empty(stage), ((it / S) & 1) ^ 1, ab, kStatusWaitEmpty)) {
+          const int stage = ring.stage;
+          if (!wait_bounded(empty(stage), ring.phase ^ 1u, ab, kStatusWaitEmpty)) {
             aborted = true;
             break;
           }
@@ -227,7 +155,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
             cp_async_16_zfill(dst + (uint32_t)i * 2048u, src, ok ? 16u : 0u);
           }
           cp_async_commit();
-          ++it;
+          ring.next(S);
           if (++inflight > kLoaderLag) {
             cp_async_wait_group<kLoaderLag>();
             fence_proxy_async_smem();
@@ -249,31 +177,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       uint32_t it = 0;
       Ring ring;
       const bool skip_first = (p.debug_flags & 1) != 0;
-      const int RS = p.R * p.S;
       for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
         const Unit un = decode_unit(p, u);
-        // im2col start pixel of the tile's first output position (the TMA walks the next 127)
-        int n0 = 0, w0 = 0, h0 = 0, d0 = 0;
+        StartPixel px{};
+        TapWalk walk;
         if (im2col) {
-          const int m0 = un.m_tile * kBlockM;
-          n0 = m0 / p.dhw;
-          const int pix = m0 - n0 * p.dhw;
-          const int ow = pix % p.Wo;
-          const int t2 = pix / p.Wo;
-          w0 = ow * p.sw - p.pw;
-          h0 = (t2 % p.Ho) * p.sh - p.ph;
-          d0 = (t2 / p.Ho) * p.sd - p.pd;
-        }
-        // (tap, channel) of the unit's first A sub-tile; later ones follow by counting
-        int c = 0, ts = 0, tr = 0, tt = 0;
-        if (im2col) {
-          const int kk = un.kb0 * kBlockK;
-          const int tap = kk / p.C;
-          c = kk - tap * p.C;
-          tt = tap / RS;
-          const int rs = tap - tt * RS;
-          tr = rs / p.S;
-          ts = rs - tr * p.S;
+          px.set(p, un.m_tile * kBlockM);  // the TMA walks the next 127 output positions
+          walk.start(p, un.kb0 * kBlockK);
         }
         bool aborted = false;
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
@@ -284,34 +194,26 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           }
           const int kk0 = kb * kBlockK;
           const int nsub = im2col ? min(kBlockK, p.kg - kk0) / p.a_cb : 0;
-          if (!(skip_first && it == 0)) {
+          const bool skip = skip_first && it == 0;
+          if (!skip) {
             mbar_arrive_expect_tx(fullB(stage), b_bytes + (uint32_t)(nsub * p.a_cb * kBlockM));
             tma_load_2d(sB_u32 + (uint32_t)stage * b_bytes, &wmap, fullB(stage), kk0,
                         un.n_tile * p.block_n);
           }
           const uint32_t a_dst = sA_u32 + (uint32_t)stage * kATileBytes;
           for (int q = 0; q < nsub; ++q) {
-            if (!(skip_first && it == 0))
-              tma_load_im2col_5d(a_dst + (uint32_t)(q * kBlockM * p.a_cb), &xmap, fullB(stage), c,
-                                 w0, h0, d0, n0, (uint16_t)ts, (uint16_t)tr, (uint16_t)tt);
-            c += p.a_cb;
-            if (c == p.C) {
-              c = 0;
-              if (++ts == p.S) {
-                ts = 0;
-                if (++tr == p.R) {
-                  tr = 0;
-                  ++tt;
-                }
-              }
-            }
+            if (!skip)
+              tma_load_im2col_5d(a_dst + (uint32_t)(q * kBlockM * p.a_cb), &xmap, fullB(stage),
+                                 walk.c, px.w, px.h, px.d, px.n, (uint16_t)walk.s,
+                                 (uint16_t)walk.r, (uint16_t)walk.t);
+            walk.next(p);
           }
           ++it;
           ring.next(S);
         }
         if (aborted) break;
       }
-      // Before the CTA may exit, every weight tile this thread requested must have landed.
+      // Before the CTA may exit, every tile this thread requested must have landed.
       const uint32_t first = it > (uint32_t)S ? it - (uint32_t)S : 0u;
       for (uint32_t j = first; j < it; ++j) {
         if (skip_first && j == 0) continue;
@@ -335,7 +237,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       uint32_t a_step[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        a_step[j] = (((uint32_t)(j * kMmaK) / a_cb) * kBlockM * a_cb + (uint32_t)(j * kMmaK) % a_cb) >> 4;
+        a_step[j] =
+            (((uint32_t)(j * kMmaK) / a_cb) * kBlockM * a_cb + (uint32_t)(j * kMmaK) % a_cb) >> 4;
       const uint32_t a_stage16 = kATileBytes >> 4, b_stage16 = b_bytes >> 4;
       uint32_t tc = 0;
       Ring ring;
@@ -398,13 +301,16 @@ size_t conv_smem_bytes(int block_n, int stages) {
 cudaError_t conv_set_smem_attr(size_t smem_bytes) {
   cudaError_t e = cudaFuncSetAttribute(conv3d_fp8_tc_kernel<true>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(conv3d_fp8_tc_kernel<false>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(conv3d_fp8_tc_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+  if (e == cudaSuccess) e = conv_pair_set_smem_attr(smem_bytes);
+  return e;
 }
 
 cudaError_t launch_conv(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
                         bool row_chk, int grid, cudaStream_t stream) {
+  if (p.pair) return launch_conv_pair(p, wmap, xmap, row_chk, grid, stream);
   const size_t smem = conv_smem_bytes(p.block_n, p.stages);
   if (row_chk)
     conv3d_fp8_tc_kernel<true><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);

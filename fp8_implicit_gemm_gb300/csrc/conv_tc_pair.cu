@@ -1,0 +1,356 @@
+// conv_tc_pair.cu -- the implicit-GEMM main kernel on CTA pairs: tcgen05.mma.cta_group::2 with
+// M = 256 rows per unit, 128 per CTA.
+//
+// Same GEMM view and work units as the one-CTA kernel, with block_m = 256. A cluster of two CTAs
+// (on two SMs) owns one unit at a time:
+//   - each CTA's TMA warp loads its own 128 A rows and its half of the unit's B tile
+//     (block_n / 2 weight rows) into its own shared memory, and completes the LEADER's (rank 0)
+//     stage barrier, which the leader's TMA warp armed with both CTAs' transaction bytes;
+//   - the leader's MMA warp issues tcgen05.mma.cta_group::2 (M=256, N=block_n, K=32): A rows and B
+//     halves are read from both CTAs' shared memory at the same offsets and each CTA's TMEM
+//     receives its own 128 accumulator rows; tcgen05.commit multicasts the stage-empty and
+//     accumulator-full signals to both CTAs;
+//   - each CTA's epilogue warps drain their own TMEM rows (stores masked on real output rows and
+//     col < K) and release the accumulator on the leader's barrier (256 arrivals).
+// Compared with one CTA per 128-row tile, every SM stores and reads only half of the B tile per
+// K block, so shared-memory traffic per MMA cycle drops from 192 to 128 bytes and more stages fit.
+//
+// kGrid (stride-1 convolutions): the rows of a unit are 256 consecutive positions of the
+// zero-padded output grid of one image, so the A rows of tap (t, r, s) are rows
+// (t*Hp + r)*Wp + s further down one 2D view [N*Dp*Hp*Wp][C] of the padded channels-last input.
+// A stage holds one (t, r, channel block): a single TMA tile of 128 + S - 1 rows serves the S taps
+// along W (their MMA descriptors start s rows into it; the 128-byte swizzle is a function of the
+// shared-memory address, so the shifted start reads the rows TMA wrote there), plus the S matching
+// B tiles. That cuts the bytes each SM's TMA unit must bring in per MMA by about a third, which is
+// what bounds the output-position route. Rows of the grid that are not outputs (h >= Ho, w >= Wo,
+// d >= Do) are computed and never stored.
+// Every wait is bounded; a wait that runs out records a status bit and both CTAs wind down.
+#include <cuda_runtime.h>
+
+#include "conv_common.cuh"
+
+namespace c3d {
+
+constexpr uint64_t kAbortSettleNs = 2ull * 1000 * 1000;  // let copies in flight land on abort
+
+// Shared-memory footprint of one pipeline stage of the pair kernel (per CTA).
+__host__ __device__ inline void pair_stage_bytes(const ConvParams& p, bool grid, uint32_t* a_bytes,
+                                                 uint32_t* b_bytes) {
+  const uint32_t half_n = (uint32_t)p.block_n / 2;
+  if (grid) {
+    const uint32_t rows = (uint32_t)kBlockM + (uint32_t)p.S - 1;
+    *a_bytes = ((rows * (uint32_t)p.a_cb) + 1023u) & ~1023u;
+    *b_bytes = (((uint32_t)p.S * half_n * (uint32_t)p.a_cb) + 1023u) & ~1023u;
+  } else {
+    *a_bytes = (uint32_t)kATileBytes;
+    *b_bytes = half_n * (uint32_t)kBlockK;
+  }
+}
+
+template <bool kRowChk, bool kGrid>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
+    conv3d_fp8_tc_pair_kernel(const __grid_constant__ CUtensorMap wmap,
+                              const __grid_constant__ CUtensorMap xmap, const ConvParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_u32 = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);  // 1024-aligned stages
+
+  const int S = p.stages;
+  const int half_n = p.block_n / 2;
+  uint32_t a_bytes, b_bytes;  // per stage: A rows, this CTA's half of the B tile(s)
+  pair_stage_bytes(p, kGrid, &a_bytes, &b_bytes);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + (size_t)S * a_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)S * b_bytes);
+  // bars: full[S] (leader's is used), empty[S], accFull[2], accEmpty[2] (leader's), drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const uint32_t sA_u32 = smem_u32(sA), sB_u32 = smem_u32(sB);
+  const uint32_t bars_u32 = smem_u32(bars);
+  auto full = [&](int s) { return bars_u32 + 8u * s; };
+  auto empty = [&](int s) { return bars_u32 + 8u * (S + s); };
+  auto accFull = [&](int b) { return bars_u32 + 8u * (2 * S + b); };
+  auto accEmpty = [&](int b) { return bars_u32 + 8u * (2 * S + 2 + b); };
+  const uint32_t drain_bar = bars_u32 + 8u * (2 * S + 4);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const uint32_t leader_bars = map_to_cta(bars_u32, 0);  // the leader's barriers, cluster window
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(empty(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accFull(b), 1);
+      mbar_init(accEmpty(b), 2 * 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc_pair(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
+    tmem_relinquish_pair();
+    if (lane == 0) {
+      prefetch_tensormap(&wmap);
+      prefetch_tensormap(&xmap);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before anyone signals across the pair
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const AbortState ab{abort_flag, p.status, p.timeout_ns};
+  const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
+  const int row_base = (int)rank * kBlockM;  // this CTA's rows within the 256-row unit
+
+  if (warp < 4) {
+    // ------------------------------------------------------------------------------ epilogue
+    const float scale = __ldg(p.scale_x) * __ldg(p.scale_w);
+    uint32_t tc = 0;
+    for (int u = cluster_id; u < p.num_units; u += num_clusters, ++tc) {
+      const Unit un = decode_unit(p, u);
+      const int buf = tc & 1;
+      if (!wait_bounded<true>(accFull(buf), (tc >> 1) & 1, ab, kStatusWaitAccFull)) break;
+      tc_fence_after();
+      const uint32_t trow =
+          tmem_base + (uint32_t)buf * p.acc_stride + ((uint32_t)(warp * 32) << 16);
+      epilogue_row<kRowChk>(p, un, trow, row_base + threadIdx.x, scale);
+      tc_fence_before();
+      mbar_arrive_cluster(leader_bars + (accEmpty(buf) - bars_u32));
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------------------------------------ TMA loader
+    if (lane == 0) {
+      uint32_t it = 0;
+      Ring ring;
+      const bool skip_first = (p.debug_flags & 1) != 0;
+      for (int u = cluster_id; u < p.num_units; u += num_clusters) {
+        const Unit un = decode_unit(p, u);
+        bool aborted = false;
+        if (kGrid) {
+          // first padded-grid row of this CTA's 128 rows, as a row of the [N*Dp*Hp*Wp][C] view
+          const int n = un.m_tile / p.tiles_per_image;
+          const int xrow0 = n * p.Dp * p.Hp * p.Wp +
+                            (un.m_tile - n * p.tiles_per_image) * p.block_m + row_base;
+          const int ncb = p.C / p.a_cb;
+          int tt, tr, cb;  // (t, r, channel block) of the unit's first group
+          {
+            const int trg = un.kb0 / ncb;
+            cb = un.kb0 - trg * ncb;
+            tt = trg / p.R;
+            tr = trg - tt * p.R;
+          }
+          const uint32_t tx = 2u * ((uint32_t)(kBlockM + p.S - 1) * (uint32_t)p.a_cb +
+                                    (uint32_t)(p.S * half_n * p.a_cb));
+          for (int g = un.kb0; g < un.kb1; ++g) {
+            const int stage = ring.stage;
+            if (!wait_bounded<true>(empty(stage), ring.phase ^ 1u, ab, kStatusWaitEmpty)) {
+              aborted = true;
+              break;
+            }
+            if (!(skip_first && it == 0)) {
+              const uint32_t bar = leader_bars + (full(stage) - bars_u32);
+              if (leader) mbar_arrive_expect_tx(full(stage), tx);
+              const int c0 = cb * p.a_cb;
+              tma_load_2d_pair(sA_u32 + (uint32_t)stage * a_bytes, &xmap, bar, c0,
+                               xrow0 + (tt * p.Hp + tr) * p.Wp);
+              const int k_tap0 = ((tt * p.R + tr) * p.S) * p.C + c0;
+              const uint32_t b_dst = sB_u32 + (uint32_t)stage * b_bytes;
+              for (int ss = 0; ss < p.S; ++ss)
+                tma_load_2d_pair(b_dst + (uint32_t)(ss * half_n * p.a_cb), &wmap, bar,
+                                 k_tap0 + ss * p.C, un.n_tile * p.block_n + (int)rank * half_n);
+            }
+            if (++cb == ncb) {
+              cb = 0;
+              if (++tr == p.R) {
+                tr = 0;
+                ++tt;
+              }
+            }
+            ++it;
+            ring.next(S);
+          }
+          if (aborted) break;
+          continue;
+        }
+        StartPixel px{};
+        px.set(p, un.m_tile * p.block_m + row_base);  // the TMA walks the next 127 positions
+        TapWalk walk;
+        walk.start(p, un.kb0 * kBlockK);
+        for (int kb = un.kb0; kb < un.kb1; ++kb) {
+          const int stage = ring.stage;
+          if (!wait_bounded<true>(empty(stage), ring.phase ^ 1u, ab, kStatusWaitEmpty)) {
+            aborted = true;
+            break;
+          }
+          const int kk0 = kb * kBlockK;
+          const int nsub = min(kBlockK, p.kg - kk0) / p.a_cb;
+          const bool skip = skip_first && it == 0;
+          const uint32_t bar = leader_bars + (full(stage) - bars_u32);
+          if (!skip) {
+            if (leader)  // arm the stage with the bytes of both CTAs' copies
+              mbar_arrive_expect_tx(full(stage),
+                                    2u * (b_bytes + (uint32_t)(nsub * p.a_cb * kBlockM)));
+            tma_load_2d_pair(sB_u32 + (uint32_t)stage * b_bytes, &wmap, bar, kk0,
+                             un.n_tile * p.block_n + (int)rank * half_n);
+          }
+          const uint32_t a_dst = sA_u32 + (uint32_t)stage * a_bytes;
+          for (int q = 0; q < nsub; ++q) {
+            if (!skip)
+              tma_load_im2col_5d_pair(a_dst + (uint32_t)(q * kBlockM * p.a_cb), &xmap, bar,
+                                      walk.c, px.w, px.h, px.d, px.n, (uint16_t)walk.s,
+                                      (uint16_t)walk.r, (uint16_t)walk.t);
+            walk.next(p);
+          }
+          ++it;
+          ring.next(S);
+        }
+        if (aborted) break;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ------------------------------------------------------------------------------ MMA issuer
+    if (lane == 0 && leader) {
+      const uint32_t idesc = make_idesc_e4m3_f32(2 * kBlockM, (uint32_t)p.block_n);
+      const uint32_t a_cb = (uint32_t)p.a_cb;
+      const uint32_t a_layout =
+          a_cb == 128 ? kLayoutSw128 : (a_cb == 64 ? kLayoutSw64 : kLayoutSw32);
+      const uint64_t adesc0 = make_kmajor_desc(sA_u32, a_cb, a_layout);
+      const uint64_t bdesc0 = make_sw128_kmajor_desc(sB_u32);
+      uint32_t a_step[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        a_step[j] =
+            (((uint32_t)(j * kMmaK) / a_cb) * kBlockM * a_cb + (uint32_t)(j * kMmaK) % a_cb) >> 4;
+      const uint32_t a_stage16 = a_bytes >> 4, b_stage16 = b_bytes >> 4;
+      // padded-grid route: tap s starts s rows (s * a_cb bytes) into the A tile and at
+      // s * half_n * a_cb bytes in the B stage; K step j adds 32 j bytes to both
+      const uint32_t steps_cb = a_cb / kMmaK;
+      const uint32_t b_tap16 = ((uint32_t)half_n * a_cb) >> 4, a_row16 = a_cb >> 4;
+      uint32_t tc = 0;
+      Ring ring;
+      bool aborted = false;
+      for (int u = cluster_id; u < p.num_units && !aborted; u += num_clusters, ++tc) {
+        const Unit un = decode_unit(p, u);
+        const int buf = tc & 1;
+        if (!wait_bounded<true>(accEmpty(buf), ((tc >> 1) & 1) ^ 1, ab, kStatusWaitAccEmpty))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)buf * p.acc_stride;
+        for (int kb = un.kb0; kb < un.kb1; ++kb) {
+          const int stage = ring.stage;
+          if (!wait_bounded<true>(full(stage), ring.phase, ab, kStatusWaitFull)) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t adesc = adesc0 + (uint64_t)((uint32_t)stage * a_stage16);
+          const uint32_t acc0 = kb > un.kb0 ? 1u : 0u;
+          if (kGrid) {
+            const uint64_t bdesc_g = make_kmajor_desc(sB_u32 + (uint32_t)stage * b_bytes, a_cb,
+                                                      a_layout);
+            uint32_t acc = acc0;
+            for (int ss = 0; ss < p.S; ++ss)
+              for (uint32_t j = 0; j < steps_cb; ++j) {
+                mma_f8f6f4_pair(d_tmem, adesc + (uint64_t)(ss * a_row16 + 2u * j),
+                                bdesc_g + (uint64_t)(ss * b_tap16 + 2u * j), idesc, acc);
+                acc = 1u;
+              }
+          } else {
+            const uint64_t bdesc = bdesc0 + (uint64_t)((uint32_t)stage * b_stage16);
+            const int rem = p.kg - kb * kBlockK;
+            if (rem >= kBlockK) {
+              mma_f8f6f4_pair(d_tmem, adesc + a_step[0], bdesc, idesc, acc0);
+              mma_f8f6f4_pair(d_tmem, adesc + a_step[1], bdesc + 2u, idesc, 1u);
+              mma_f8f6f4_pair(d_tmem, adesc + a_step[2], bdesc + 4u, idesc, 1u);
+              mma_f8f6f4_pair(d_tmem, adesc + a_step[3], bdesc + 6u, idesc, 1u);
+            } else {
+              const int nsteps = (rem + kMmaK - 1) / kMmaK;
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                if (j < nsteps)
+                  mma_f8f6f4_pair(d_tmem, adesc + a_step[j], bdesc + 2u * j, idesc,
+                                  j > 0 ? 1u : acc0);
+            }
+          }
+          mma_commit_pair(empty(stage), 0x3);
+          ring.next(S);
+        }
+        if (aborted) break;
+        mma_commit_pair(accFull(buf), 0x3);
+      }
+      // Every MMA of the pair must be complete before TMEM is released.
+      mma_commit_pair(drain_bar, 0x1);
+      wait_drain(drain_bar, 0, p.timeout_ns, p.status, kStatusWaitDrain);
+    }
+    __syncwarp();
+  }
+
+  if (*abort_flag) sleep_ns_bounded(kAbortSettleNs);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // neither CTA leaves while the other may still signal or read its memory
+  tc_fence_after();
+  if (warp == 8) tmem_dealloc_pair(tmem_base, (uint32_t)p.tmem_cols);
+}
+
+size_t conv_pair_smem_bytes(const ConvParams& p) {
+  uint32_t a_bytes, b_bytes;
+  pair_stage_bytes(p, p.route == kRouteGrid, &a_bytes, &b_bytes);
+  return 1024 + (size_t)p.stages * (a_bytes + b_bytes) + (size_t)(2 * p.stages + 5) * 8 + 16;
+}
+
+cudaError_t conv_pair_set_smem_attr(size_t smem_bytes) {
+  const int v = (int)smem_bytes;
+  cudaError_t e = cudaFuncSetAttribute(conv3d_fp8_tc_pair_kernel<true, false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, v);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(conv3d_fp8_tc_pair_kernel<false, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, v);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(conv3d_fp8_tc_pair_kernel<true, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, v);
+  return e;
+}
+
+cudaError_t launch_conv_pair(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
+                             bool row_chk, int grid, cudaStream_t stream) {
+  const size_t smem = conv_pair_smem_bytes(p);
+  if (p.route == kRouteGrid)  // grid rows that are not outputs always need the row test
+    conv3d_fp8_tc_pair_kernel<true, true><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
+  else if (row_chk)
+    conv3d_fp8_tc_pair_kernel<true, false><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
+  else
+    conv3d_fp8_tc_pair_kernel<false, false><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
+  return cudaGetLastError();
+}
+
+int conv_pair_max_active_clusters(const ConvParams& p) {
+  cudaLaunchConfig_t cfg{};
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = 2;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kNumThreads, 1, 1);
+  cfg.dynamicSmemBytes = conv_pair_smem_bytes(p);
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, conv3d_fp8_tc_pair_kernel<true, false>, &cfg) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+}  // namespace c3d

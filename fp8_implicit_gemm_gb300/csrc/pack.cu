@@ -10,7 +10,7 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
-#include "conv3d_fp8_internal.h"
+#include "conv_common.cuh"
 
 namespace c3d {
 
@@ -75,35 +75,33 @@ cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream) {
 
 // Split-K reduction: y = bf16(scale * sum_{split = 0..splits-1} partial[split]) in ascending split
 // order, so the result is bitwise reproducible for a fixed plan. One thread per (tile, column,
-// row); the stores carry the same guards as the main epilogue (row < npq, col < K).
+// row); the stores carry the same guards as the main epilogue (real output row, col < K).
 template <bool kRowChk>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(ConvParams p) {
-  const long long per_tile = (long long)p.block_n * kBlockM;
+  const long long per_tile = (long long)p.block_n * p.block_m;
   const long long total = (long long)p.m_tiles * p.n_tiles * per_tile;
   const float scale = __ldg(p.scale_x) * __ldg(p.scale_w);
   for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < total;
        g += (long long)gridDim.x * blockDim.x) {
-    const int row = (int)(g % kBlockM);
-    const int col_l = (int)((g / kBlockM) % p.block_n);
+    const int row = (int)(g % p.block_m);
+    const int col_l = (int)((g / p.block_m) % p.block_n);
     const long long tile = g / per_tile;
     const int n_tile = (int)(tile % p.n_tiles);
     const int m_tile = (int)(tile / p.n_tiles);
-    const int m = m_tile * kBlockM + row;
     const int col = n_tile * p.block_n + col_l;
-    if (kRowChk && m >= p.npq) continue;
     if (col >= p.K) continue;
-    const float* src = p.partials + ((tile * p.splits) * p.block_n + col_l) * kBlockM + row;
+    const RowDest dst = row_dest(p, m_tile, row);
+    if (kRowChk && !dst.valid) continue;
+    const float* src = p.partials + ((tile * p.splits) * p.block_n + col_l) * p.block_m + row;
     float acc = 0.0f;
     for (int s = 0; s < p.splits; ++s) acc += __ldcg(src + (long long)s * per_tile);
-    const int n = m / p.dhw;
-    const int pix = m - n * p.dhw;
     const __nv_bfloat16 b = __float2bfloat16_rn(acc * scale);
-    p.y[((long long)n * p.K + col) * p.dhw + pix] = *reinterpret_cast<const uint16_t*>(&b);
+    p.y[dst.y_off + (long long)col * p.dhw] = *reinterpret_cast<const uint16_t*>(&b);
   }
 }
 
 cudaError_t launch_splitk_reduce(const ConvParams& p, bool row_chk, cudaStream_t stream) {
-  const long long total = (long long)p.m_tiles * p.n_tiles * p.block_n * kBlockM;
+  const long long total = (long long)p.m_tiles * p.n_tiles * p.block_n * p.block_m;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -60,7 +60,12 @@ typedef struct {
     int route;           /* 0: the library chooses; 1: A by cp.async gathers from a zero-padded
                             channels-last copy of x; 2: A by TMA im2col loads (EUNSUPPORTED
                             unless C % 32 == 0, strides <= 8 and -16 <= -pad, pad - (filter-1)
-                            <= 15 on every axis) */
+                            <= 15 on every axis); 3: padded-grid route, stride 1 and CTA pairs
+                            only: M runs over the zero-padded output grid and one TMA tile of
+                            128 + S - 1 rows feeds the S taps along W (EUNSUPPORTED unless every
+                            stride is 1 and C % 32 == 0) */
+    int cta_pair;        /* 0: the library chooses; 1: one CTA per 128-row tile; 2: CTA pairs on
+                            256-row tiles (tcgen05 cta_group::2; not on the gather route) */
 } conv3d_fp8_options;
 
 /* What a plan (or a would-be plan) decided. */
@@ -68,17 +73,20 @@ typedef struct {
     int Do, Ho, Wo;           /* output extents: floor((in + 2*pad - filter) / stride) + 1 */
     long long npq;            /* M = N*Do*Ho*Wo */
     int k_gemm;               /* C*T*R*S */
-    int block_m, block_n;     /* tile of the GEMM view (block_m is always 128) */
-    int m_tiles, n_tiles;     /* ceil(npq / block_m), ceil(K / block_n) */
-    int k_blocks;             /* ceil(k_gemm / 128) */
+    int block_m, block_n;     /* tile of the GEMM view (block_m: 128, or 256 for CTA pairs) */
+    int m_tiles, n_tiles;     /* ceil(npq / block_m) (padded-grid route: N * ceil(Do*Hp*Wp /
+                                 block_m) over the padded grid), ceil(K / block_n) */
+    int k_blocks;             /* ceil(k_gemm / 128); on the padded-grid route the number of
+                                 (t, r, channel block) groups, each S taps wide */
     int splits;               /* K slices; > 1 means the split-K path (fp32 partials + reduce) */
     int k_blocks_per_split;
     int stages;               /* shared-memory pipeline depth */
     int row_chk;              /* 1 when npq % block_m != 0: the row guard is compiled in */
-    int grid;                 /* persistent CTAs launched by the main kernel */
+    int grid;                 /* persistent CTAs launched by the main kernel (2 per pair) */
     int sm_count;
     size_t workspace_bytes;   /* device workspace the plan owns */
-    int route;                /* 1: cp.async gather route, 2: TMA im2col route (as in options) */
+    int route;                /* 1: gather, 2: TMA im2col, 3: padded grid (as in options) */
+    int cta_pair;             /* 1: one CTA per tile, 2: CTA pairs (as in options) */
 } conv3d_fp8_plan_info;
 
 /*

@@ -52,9 +52,21 @@ def test_describe_configs(lib):
     # stride 2 on 4x16x16 with pad 1 gives a 2x8x8 output: npq = 128
     assert npq == [288, 3840, 65536, 128, 244800]
     assert [i["k_gemm"] for i in infos] == [2592, 1728, 3456, 13824, 6912]
-    assert [i["row_chk"] for i in infos] == [1, 0, 0, 0, 1]
-    assert [i["m_tiles"] for i in infos] == [3, 30, 512, 1, 1913]
+    # CTA pairs (256-row tiles) wherever there is more than one 128-row tile; stride-1 layers whose
+    # padded output grid adds at most 30% rows take the padded-grid route
+    assert [i["cta_pair"] for i in infos] == [2, 2, 2, 1, 2]
+    assert [i["block_m"] for i in infos] == [256, 256, 256, 128, 256]
+    assert [i["route"] for i in infos] == [2, 3, 3, 2, 3]
+    # grid route: N * ceil(Do*Hp*Wp / 256) tiles, (t, r, channel block) groups as K blocks
+    assert [i["m_tiles"] for i in infos] == [2, 2 * 10, 273, 1, 990]
+    assert [i["k_blocks"] for i in infos] == [21, 9, 9, 108, 18]
+    assert [i["row_chk"] for i in infos] == [1, 1, 1, 0, 1]
     assert [i["block_n"] for i in infos] == [96, 128, 128, 256, 256]
+    single = [_describe(s, cta_pair=1) for s in synth.CONFIGS]
+    assert [i["m_tiles"] for i in single] == [3, 30, 512, 1, 1913]
+    assert [i["row_chk"] for i in single] == [1, 0, 0, 0, 1]
+    for i in infos:
+        assert i["grid"] % (2 if i["cta_pair"] == 2 else 1) == 0
     # deep and narrow -> split-K; the large layers never split
     assert infos[3]["splits"] > 1
     assert infos[2]["splits"] == 1 and infos[4]["splits"] == 1
@@ -67,23 +79,42 @@ def test_describe_configs(lib):
 
 
 def test_describe_routes(lib):
-    # every workload has C % 32 == 0 and unit paddings: TMA im2col
-    assert all(_describe(s)["route"] == 2 for s in synth.CONFIGS)
+    # every workload has C % 32 == 0 and unit paddings: TMA im2col unless the padded grid applies
+    assert all(_describe(s, route=2)["route"] == 2 for s in synth.CONFIGS)
+    assert capi.conv3d_fp8_describe_status(1, 512, 4, 16, 16, 512, 3, 3, 3, 2, 1, 152,
+                                           route=3) == capi.CONV3D_EUNSUPPORTED  # stride 2
+    assert capi.conv3d_fp8_describe_status(1, 128, 4, 8, 8, 64, 3, 3, 3, 1, 1, 152, route=3,
+                                           cta_pair=1) == capi.CONV3D_EUNSUPPORTED  # one CTA
+    assert _describe(synth.CONFIGS[0], route=3)["route"] == 3
     odd = synth.ConvShape(1, 48, 4, 4, 4, 16)
     assert _describe(odd)["route"] == 1                         # C % 32 != 0 -> gather
     assert capi.conv3d_fp8_describe_status(1, 48, 4, 4, 4, 16, 3, 3, 3, 1, 1, 152,
                                            route=2) == capi.CONV3D_EUNSUPPORTED
     assert _describe(synth.CONFIGS[0], route=1)["route"] == 1   # forced gather
     big_pad = synth.ConvShape(1, 32, 4, 4, 4, 16, pad=17)       # corner beyond [-16, 15]
-    assert _describe(big_pad)["route"] == 1
-    # the gather route's packed copy carries the zero halo, the im2col one does not
+    assert _describe(big_pad, cta_pair=1)["route"] == 1          # im2col impossible -> gather
+    assert _describe(big_pad)["route"] == 3                      # the padded grid takes any pad
+    # the gather and grid routes' packed copy carries the zero halo, the im2col one does not
     s = synth.CONFIGS[2]
     assert _describe(s, route=1)["workspace_bytes"] > _describe(s, route=2)["workspace_bytes"]
+    assert _describe(s, route=3)["workspace_bytes"] == _describe(s, route=1)["workspace_bytes"]
+
+
+def test_describe_pair_rules(lib):
+    odd = synth.ConvShape(1, 48, 4, 4, 4, 16)                      # gather route: no pairs
+    assert _describe(odd)["cta_pair"] == 1
+    assert capi.conv3d_fp8_describe_status(1, 48, 4, 4, 4, 16, 3, 3, 3, 1, 1, 152,
+                                           cta_pair=2) == capi.CONV3D_EUNSUPPORTED
+    i = _describe(synth.CONFIGS[3], cta_pair=2)                    # forced on a single tile
+    assert i["cta_pair"] == 2 and i["m_tiles"] == 1 and i["row_chk"] == 1
+    assert _describe(synth.CONFIGS[4], cta_pair=1)["route"] == 2   # no grid route on one CTA
+    i = _describe(synth.CONFIGS[4], max_ctas=9)                    # pairs round the cap down
+    assert i["grid"] == 8
 
 
 def test_describe_forced_options(lib):
     s = synth.CONFIGS[1]
-    i = _describe(s, splits=4, block_n=64, max_ctas=10)
+    i = _describe(s, splits=4, block_n=64, max_ctas=10, cta_pair=1)
     assert i["splits"] == 4 and i["block_n"] == 64 and i["n_tiles"] == 2 and i["grid"] == 10
     # more splits than K blocks collapses to one block per split
     i = _describe(s, splits=10_000)

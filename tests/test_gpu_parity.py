@@ -28,22 +28,30 @@ def _full_case(shape, seed, **opts):
         g.close()
 
 
-ROUTES = {"gather": 1, "im2col": 2}
+ROUTES = {"gather": 1, "im2col": 2, "grid": 3}
+# (route, kernel): the cp.async gather route runs on one CTA, im2col on one CTA or on CTA pairs,
+# the padded-grid route on CTA pairs
+KERNELS = {"gather-1cta": dict(route=1, cta_pair=1), "im2col-1cta": dict(route=2, cta_pair=1),
+           "im2col-pair": dict(route=2, cta_pair=2), "grid-pair": dict(route=3, cta_pair=2)}
 
 
-@pytest.mark.parametrize("route", ["gather", "im2col"])
+@pytest.mark.parametrize("kernel", list(KERNELS))
 @pytest.mark.parametrize("cfg", [0, 1, 3])
-def test_config_full_output(cfg, route):
-    res, info = _full_case(synth.CONFIGS[cfg], synth.config_seed(cfg), route=ROUTES[route])
-    assert info["route"] == ROUTES[route]
-    print(cfg, route, res, info["splits"], info["block_n"])
+def test_config_full_output(cfg, kernel):
+    if kernel == "grid-pair" and cfg == 3:
+        pytest.skip("the padded-grid route needs stride 1")
+    res, info = _full_case(synth.CONFIGS[cfg], synth.config_seed(cfg), **KERNELS[kernel])
+    assert info["route"] == KERNELS[kernel]["route"]
+    assert info["cta_pair"] == KERNELS[kernel]["cta_pair"]
+    print(cfg, kernel, res, info["splits"], info["block_n"])
 
 
+@pytest.mark.parametrize("kernel", ["auto", "im2col-1cta", "im2col-pair"])
 @pytest.mark.parametrize("cfg", [2, 4])
-def test_config_sampled_outputs(cfg):
+def test_config_sampled_outputs(cfg, kernel):
     shape = synth.CONFIGS[cfg]
     inp = synth.make_config_inputs(cfg)
-    g = GpuConv(shape, inp)
+    g = GpuConv(shape, inp, **KERNELS.get(kernel, {}))
     try:
         y = g.run()
         assert not torch.isnan(y).any().item(), "some outputs never written"
@@ -86,22 +94,43 @@ def test_odd_shapes_gather_route(i):
     assert info["route"] == ROUTES["gather"]
 
 
+@pytest.mark.parametrize("i", [i for i, s in enumerate(ODD)
+                               if s.C % 32 == 0 and s.stride == (1, 1, 1)])
+def test_odd_shapes_grid_route(i):
+    res, info = _full_case(ODD[i], 77 + i, route=3)
+    assert info["route"] == 3
+
+
+@pytest.mark.parametrize("i", [i for i, s in enumerate(ODD) if s.C % 32 == 0])
+def test_odd_shapes_one_cta(i):
+    res, info = _full_case(ODD[i], 77 + i, cta_pair=1)
+    assert info["cta_pair"] == 1
+
+
+@pytest.mark.parametrize("kernel", ["im2col-1cta", "im2col-pair", "grid-pair"])
 @pytest.mark.parametrize("splits", [1, 2, 3, 7])
-def test_forced_splits_config1(splits):
-    res, info = _full_case(synth.CONFIGS[1], synth.config_seed(1), splits=splits)
-    assert info["splits"] == splits
+def test_forced_splits_config1(splits, kernel):
+    res, info = _full_case(synth.CONFIGS[1], synth.config_seed(1), splits=splits, **KERNELS[kernel])
+    # a split count is normalised so that no split is empty: ceil(kb / ceil(kb / requested));
+    # the grid route has 9 K groups on this layer, the others 14 K blocks
+    kb = info["k_blocks"]
+    per = -(-kb // min(splits, kb))
+    assert info["splits"] == -(-kb // per)
 
 
+@pytest.mark.parametrize("kernel", ["im2col-1cta", "im2col-pair", "grid-pair"])
 @pytest.mark.parametrize("block_n", [32, 64, 128, 256])
-def test_forced_block_n(block_n):
+def test_forced_block_n(block_n, kernel):
     shape = synth.ConvShape(2, 32, 4, 6, 10, 200)
-    res, info = _full_case(shape, 5, block_n=block_n)
+    res, info = _full_case(shape, 5, block_n=block_n, **KERNELS[kernel])
     assert info["block_n"] == block_n
 
 
-def test_max_ctas_small_grid_many_tiles():
-    # 2 CTAs walk all 30 tiles: exercises the TMEM double buffer and stage-ring wrap-around
-    res, info = _full_case(synth.CONFIGS[1], synth.config_seed(1), max_ctas=2, splits=1)
+@pytest.mark.parametrize("kernel", ["im2col-1cta", "im2col-pair", "grid-pair"])
+def test_max_ctas_small_grid_many_tiles(kernel):
+    # 2 CTAs (one pair) walk all tiles: exercises the TMEM double buffer and stage-ring wrap-around
+    res, info = _full_case(synth.CONFIGS[1], synth.config_seed(1), max_ctas=2, splits=1,
+                           **KERNELS[kernel])
     assert info["grid"] == 2
 
 
@@ -109,13 +138,13 @@ def test_split_k_is_reproducible_and_close_across_split_counts():
     shape = synth.CONFIGS[3]
     inp = synth.make_config_inputs(3)
     outs = {}
-    for splits in (1, 4, 27):
-        g = GpuConv(shape, inp, splits=splits)
+    for splits, pair in ((1, 1), (4, 1), (27, 1), (27, 2)):
+        g = GpuConv(shape, inp, splits=splits, cta_pair=pair)
         try:
             a = bits(g.run())
             b = bits(g.run())
             assert np.array_equal(a, b), f"splits={splits} not bitwise reproducible"
-            outs[splits] = a
+            outs[(splits, pair)] = a
         finally:
             g.close()
     y64, yb = oracle.conv3d_fp8(inp["x"].numpy(), inp["w"].numpy(), inp["sx"], inp["sw"],
@@ -129,8 +158,8 @@ def test_plans_with_different_tiles_coexist():
     the first one's launches."""
     s0 = synth.CONFIGS[0]
     inp = synth.make_config_inputs(0)
-    big = GpuConv(s0, inp, block_n=96, splits=1)      # 7 stages of 28 KB
-    small = GpuConv(s0, inp, block_n=32, splits=1)    # 8 stages of 20 KB
+    big = GpuConv(s0, inp, block_n=96, splits=1, cta_pair=1)   # 7 stages of 28 KB
+    small = GpuConv(s0, inp, block_n=32, splits=1, cta_pair=2)  # pairs, 8 stages of 18 KB
     try:
         y64, yb = oracle.conv3d_fp8(inp["x"].numpy(), inp["w"].numpy(), inp["sx"], inp["sw"],
                                     s0.stride, s0.pad)

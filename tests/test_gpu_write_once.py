@@ -67,12 +67,14 @@ def test_repeated_launches_write_every_element_once(cfg):
         g.close()
 
 
-def test_bounded_wait_reports_instead_of_hanging():
-    """A weight tile that never arrives: the MMA warp's bounded wait runs out, the kernel winds
-    down, the status word says so, and the context stays usable for the next plan."""
+@pytest.mark.parametrize("kernel", [dict(cta_pair=1, route=2), dict(cta_pair=2, route=2),
+                                    dict(cta_pair=2, route=3)])
+def test_bounded_wait_reports_instead_of_hanging(kernel):
+    """A stage that never arrives: the MMA warp's bounded wait runs out, the kernel winds down
+    (on CTA pairs: both CTAs), the status word says so, and the context stays usable."""
     shape = synth.CONFIGS[0]
     inp = synth.make_config_inputs(0)
-    bad = GpuConv(shape, inp, debug_flags=1, wait_timeout_ms=200, splits=1)
+    bad = GpuConv(shape, inp, debug_flags=1, wait_timeout_ms=200, splits=1, **kernel)
     try:
         bad.run()
         assert capi.conv3d_fp8_check(bad.plan) == capi.CONV3D_EDEVICE
