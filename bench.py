@@ -39,7 +39,8 @@ if ROOT not in sys.path:
 DEFAULT_CONFIG = 4
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
-MAIN_KERNEL_SOURCES = ["conv_tc.cu", "ptx.cuh", "conv3d_fp8_internal.h"]
+MAIN_KERNEL_SOURCES = ["conv_tc.cu", "conv_tc_pair.cu", "conv_common.cuh", "ptx.cuh",
+                       "conv3d_fp8_internal.h"]
 
 
 def log(*a):
@@ -371,7 +372,8 @@ def run_ours(args):
                 "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                 "peak_source": f"{peaks_kind} copy bandwidth"}
     roof["traffic"] = traffic
-    roof["kernel"] = "conv3d_fp8_tc_kernel"
+    roof["kernel"] = ("conv3d_fp8_tc_pair_kernel" if info["cta_pair"] == 2
+                      else "conv3d_fp8_tc_kernel")
     roof["kernel_ms"] = round(mean_kern_ms, 5)
     roof["alg_flop"] = fig["flop"]
     roof["alg_bytes"] = fig["alg_bytes"]
@@ -400,8 +402,9 @@ def run_ours(args):
                    "W": shape.W, "K": shape.K, "filter": [shape.T, shape.R, shape.S],
                    "stride": list(shape.stride), "pad": list(shape.pad), "npq": fig["npq"],
                    "gflop_per_step": round(fig["flop"] / 1e9, 3),
-                   "plan": {k: info[k] for k in ("block_n", "m_tiles", "n_tiles", "splits",
-                                                 "stages", "grid", "row_chk")},
+                   "plan": {k: info[k] for k in ("route", "cta_pair", "block_m", "block_n",
+                                                 "m_tiles", "n_tiles", "splits", "stages", "grid",
+                                                 "row_chk")},
                    "l2": f"flushed between steps ({flush.numel() >> 20} MiB write outside the "
                          "per-step events)",
                    "parallelism": f"replicas x{dist.world}"},

@@ -14,41 +14,139 @@
 
 namespace c3d {
 
-// One thread writes 16 channels (16 bytes) of one padded pixel, or 16 channels of one tap of one
-// filter. Pixels run fastest across threads so that each of the 16 byte loads of a warp is a
-// contiguous run along W of the NCDHW input.
-__global__ void __launch_bounds__(256) pack_kernel(ConvParams p, long long x_items,
-                                                   long long w_items) {
-  const long long total = x_items + w_items;
+// Work of the pack kernel, as consecutive index ranges of one grid-stride loop:
+//   [0, x_items)          interior of x: with W % 4 == 0, one item = 16 channels x 4 pixels (16
+//                         aligned 4-byte loads, a byte transpose in registers, four 16-byte
+//                         stores); otherwise one item = 16 channels x 1 pixel (16 byte loads)
+//   + halo_row_items      16-byte zero chunks of the padded rows (d or h in the halo)
+//   + halo_side_items     16-byte zero chunks of the W-halo pixels of interior rows
+//   + w_items             16 channels of one tap of one filter
+// Pixels (or pixel quads) run fastest across threads, so each load of a warp is a contiguous run
+// along W of the NCDHW input.
+struct PackPlan {
+  long long x_items, halo_row_items, halo_side_items, w_items;
+  bool quad;  // W % 4 == 0: 4-pixel items
+};
+
+__host__ __device__ inline PackPlan pack_plan(const ConvParams& p) {
+  PackPlan q;
+  const long long cq = p.C / 16;
+  q.quad = (p.W % 4) == 0;
+  q.x_items = (long long)p.N * p.D * p.H * cq * (q.quad ? p.W / 4 : p.W);
+  const long long halo_rows_per_image = (long long)p.Dp * p.Hp - (long long)p.D * p.H;
+  q.halo_row_items = (long long)p.N * halo_rows_per_image * p.Wp * cq;
+  q.halo_side_items = (long long)p.N * p.D * p.H * (p.Wp - p.W) * cq;
+  q.w_items = (long long)p.K * p.taps * cq;
+  return q;
+}
+
+// Byte transpose of a 4x4 block: v[c] holds pixels 0..3 of channel c; o[j] gets channels 0..3 of
+// pixel j.
+__device__ __forceinline__ void transpose4x4(const uint32_t v[4], uint32_t o[4]) {
+  const uint32_t t0 = __byte_perm(v[0], v[1], 0x5140), t1 = __byte_perm(v[2], v[3], 0x5140);
+  const uint32_t t2 = __byte_perm(v[0], v[1], 0x7362), t3 = __byte_perm(v[2], v[3], 0x7362);
+  o[0] = __byte_perm(t0, t1, 0x5410);
+  o[1] = __byte_perm(t0, t1, 0x7632);
+  o[2] = __byte_perm(t2, t3, 0x5410);
+  o[3] = __byte_perm(t2, t3, 0x7632);
+}
+
+__global__ void __launch_bounds__(256) pack_kernel(ConvParams p, PackPlan q) {
+  const long long e1 = q.x_items, e2 = e1 + q.halo_row_items, e3 = e2 + q.halo_side_items;
+  const long long total = e3 + q.w_items;
   const int cq_n = p.C >> 4;
+  const long long plane = (long long)p.D * p.H * p.W;
   for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < total;
        g += (long long)gridDim.x * blockDim.x) {
-    uint32_t v[4] = {0u, 0u, 0u, 0u};
-    if (g < x_items) {
-      const int wpos = (int)(g % p.Wp);
-      long long rest = g / p.Wp;
+    if (g < e1) {
+      // interior: (pixel or quad fastest, then channel chunk, then (n, d, h) row)
+      const int per_row = q.quad ? p.W / 4 : p.W;
+      const int wi = (int)(g % per_row);
+      const long long rest = g / per_row;
       const int cq = (int)(rest % cq_n);
-      const long long prow = rest / cq_n;         // (n, dp, hp) of the padded volume
-      const int hp = (int)(prow % p.Hp);
-      const int dp = (int)((prow / p.Hp) % p.Dp);
-      const int n = (int)(prow / ((long long)p.Hp * p.Dp));
-      const int d = dp - p.pk_pd, h = hp - p.pk_ph, w = wpos - p.pk_pw;
-      if (d >= 0 && d < p.D && h >= 0 && h < p.H && w >= 0 && w < p.W) {
-        const long long plane = (long long)p.D * p.H * p.W;
-        const uint8_t* src =
-            p.x + ((long long)n * p.C + cq * 16) * plane + ((long long)d * p.H + h) * p.W + w;
+      const long long row = rest / cq_n;  // n*D*H + d*H + h
+      const int h = (int)(row % p.H);
+      const int d = (int)((row / p.H) % p.D);
+      const int n = (int)(row / ((long long)p.H * p.D));
+      const uint8_t* src = p.x + ((long long)n * p.C + cq * 16) * plane +
+                           ((long long)d * p.H + h) * p.W;
+      uint8_t* dst_row = p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) *
+                                     p.Wp + p.pk_pw) * p.C + cq * 16;
+      if (q.quad) {
+        uint32_t v[16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j >> 2] |= (uint32_t)__ldg(src + j * plane) << ((j & 3) * 8);
+        for (int j = 0; j < 16; ++j)
+          v[j] = __ldg(reinterpret_cast<const uint32_t*>(src + j * plane) + wi);
+        uint32_t o[4][4];  // o[pixel][word of 4 channels]
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          uint32_t t[4];
+          transpose4x4(v + 4 * b, t);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) o[j][b] = t[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(dst_row + (long long)(4 * wi + j) * p.C) =
+              make_uint4(o[j][0], o[j][1], o[j][2], o[j][3]);
+      } else {
+        uint32_t v[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          v[j >> 2] |= (uint32_t)__ldg(src + j * plane + wi) << ((j & 3) * 8);
+        *reinterpret_cast<uint4*>(dst_row + (long long)wi * p.C) = make_uint4(v[0], v[1], v[2], v[3]);
       }
-      uint4* dst = reinterpret_cast<uint4*>(p.xp + (prow * p.Wp + wpos) * p.C + cq * 16);
-      *dst = make_uint4(v[0], v[1], v[2], v[3]);
+    } else if (g < e2) {
+      // zero chunks of a halo row: halo planes first, then the halo rows of interior planes
+      const long long gi = g - e1;
+      const long long per_row = (long long)p.Wp * cq_n;
+      const long long r = (gi / per_row);
+      const long long chunk = gi - r * per_row;
+      const long long halo_rows_per_image = (long long)p.Dp * p.Hp - (long long)p.D * p.H;
+      const int n = (int)(r / halo_rows_per_image);
+      long long rr = r - (long long)n * halo_rows_per_image;
+      const long long front = (long long)p.pk_pd * p.Hp;
+      int dp, hp;
+      if (rr < front) {
+        dp = (int)(rr / p.Hp);
+        hp = (int)(rr % p.Hp);
+      } else if (rr < 2 * front) {
+        rr -= front;
+        dp = p.pk_pd + p.D + (int)(rr / p.Hp);
+        hp = (int)(rr % p.Hp);
+      } else {
+        rr -= 2 * front;
+        const int side = 2 * p.pk_ph;
+        const int kk = (int)(rr % side);
+        dp = p.pk_pd + (int)(rr / side);
+        hp = kk < p.pk_ph ? kk : p.H + kk;
+      }
+      *reinterpret_cast<uint4*>(p.xp + (((long long)n * p.Dp + dp) * p.Hp + hp) * p.Wp * p.C +
+                                chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
+    } else if (g < e3) {
+      // zero chunks of the W-halo pixels of interior rows
+      const long long gi = g - e2;
+      const int side = p.Wp - p.W;
+      const long long per_row = (long long)side * cq_n;
+      const long long row = gi / per_row;  // n*D*H + d*H + h
+      const long long rem = gi - row * per_row;
+      const int kk = (int)(rem / cq_n);
+      const int cq = (int)(rem - (long long)kk * cq_n);
+      const int wp = kk < p.pk_pw ? kk : p.W + kk;
+      const int h = (int)(row % p.H);
+      const int d = (int)((row / p.H) % p.D);
+      const int n = (int)(row / ((long long)p.H * p.D));
+      *reinterpret_cast<uint4*>(
+          p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) * p.Wp + wp) * p.C +
+          cq * 16) = make_uint4(0u, 0u, 0u, 0u);
     } else {
-      const long long gw = g - x_items;
+      const long long gw = g - e3;
       const int tap = (int)(gw % p.taps);
       const long long rest = gw / p.taps;
       const int cq = (int)(rest % cq_n);
       const int k = (int)(rest / cq_n);
       const uint8_t* src = p.w + ((long long)k * p.C + cq * 16) * p.taps + tap;
+      uint32_t v[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j >> 2] |= (uint32_t)__ldg(src + j * p.taps) << ((j & 3) * 8);
       uint4* dst =
@@ -59,9 +157,8 @@ __global__ void __launch_bounds__(256) pack_kernel(ConvParams p, long long x_ite
 }
 
 cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream) {
-  const long long x_items = (long long)p.N * p.Dp * p.Hp * p.Wp * (p.C / 16);
-  const long long w_items = (long long)p.K * p.taps * (p.C / 16);
-  const long long total = x_items + w_items;
+  const PackPlan q = pack_plan(p);
+  const long long total = q.x_items + q.halo_row_items + q.halo_side_items + q.w_items;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -69,7 +166,7 @@ cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream) {
   const long long cap = (long long)sms * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  pack_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, x_items, w_items);
+  pack_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, q);
   return cudaGetLastError();
 }
 
