@@ -224,6 +224,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
           a_cb == 128 ? kLayoutSw128 : (a_cb == 64 ? kLayoutSw64 : kLayoutSw32);
       const uint64_t adesc0 = make_kmajor_desc(sA_u32, a_cb, a_layout);
       const uint64_t bdesc0 = make_sw128_kmajor_desc(sB_u32);
+      const uint64_t bdesc_g0 = make_kmajor_desc(sB_u32, a_cb, a_layout);  // grid route's B
       uint32_t a_step[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j)
@@ -254,15 +255,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
           const uint64_t adesc = adesc0 + (uint64_t)((uint32_t)stage * a_stage16);
           const uint32_t acc0 = kb > un.kb0 ? 1u : 0u;
           if (kGrid) {
-            const uint64_t bdesc_g = make_kmajor_desc(sB_u32 + (uint32_t)stage * b_bytes, a_cb,
-                                                      a_layout);
+            // The issuing thread must keep pace with the tensor pipe (one N=256 MMA per 128
+            // cycles): per tap, the K steps go out as straight-line code with constant descriptor
+            // offsets, and the per-tap offsets advance by one add each.
+            uint64_t a_tap = adesc;
+            uint64_t b_tap = bdesc_g0 + (uint64_t)((uint32_t)stage * b_stage16);
             uint32_t acc = acc0;
-            for (int ss = 0; ss < p.S; ++ss)
-              for (uint32_t j = 0; j < steps_cb; ++j) {
-                mma_f8f6f4_pair(d_tmem, adesc + (uint64_t)(ss * a_row16 + 2u * j),
-                                bdesc_g + (uint64_t)(ss * b_tap16 + 2u * j), idesc, acc);
-                acc = 1u;
+            for (int ss = 0; ss < p.S; ++ss) {
+              if (steps_cb == 4) {
+                mma_f8f6f4_pair(d_tmem, a_tap, b_tap, idesc, acc);
+                mma_f8f6f4_pair(d_tmem, a_tap + 2u, b_tap + 2u, idesc, 1u);
+                mma_f8f6f4_pair(d_tmem, a_tap + 4u, b_tap + 4u, idesc, 1u);
+                mma_f8f6f4_pair(d_tmem, a_tap + 6u, b_tap + 6u, idesc, 1u);
+              } else if (steps_cb == 2) {
+                mma_f8f6f4_pair(d_tmem, a_tap, b_tap, idesc, acc);
+                mma_f8f6f4_pair(d_tmem, a_tap + 2u, b_tap + 2u, idesc, 1u);
+              } else {
+                mma_f8f6f4_pair(d_tmem, a_tap, b_tap, idesc, acc);
               }
+              acc = 1u;
+              a_tap += a_row16;
+              b_tap += b_tap16;
+            }
           } else {
             const uint64_t bdesc = bdesc0 + (uint64_t)((uint32_t)stage * b_stage16);
             const int rem = p.kg - kb * kBlockK;
