@@ -43,7 +43,7 @@ class PlanInfo(ctypes.Structure):
                 ("k_blocks_per_split", ctypes.c_int), ("stages", ctypes.c_int),
                 ("row_chk", ctypes.c_int), ("grid", ctypes.c_int), ("sm_count", ctypes.c_int),
                 ("workspace_bytes", ctypes.c_size_t), ("route", ctypes.c_int),
-                ("cta_pair", ctypes.c_int)]
+                ("cta_pair", ctypes.c_int), ("full_tiles", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -45,15 +45,21 @@ int next_pow2(int v) {
   return r;
 }
 
+// Whether some tiles are split along K (their fp32 partials then need the reduction kernel).
+bool has_split_tiles(const ConvParams& p) {
+  return p.full_tiles < (long long)p.m_tiles * p.n_tiles;
+}
+
 struct Layout {
   size_t xp_off, xp_bytes, wp_off, wp_bytes, part_off, part_bytes, status_off, total;
 };
 
-// Validation and every tiling decision, with no device access.
+// Validation and every tiling decision, with no device access. `pair_slots` > 0 caps the number
+// of CTA pairs that can be resident at once (the device's cluster occupancy), when known.
 conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int S,
                      const int stride[3], const int pad[3], int sm_count,
                      const conv3d_fp8_options* opts, conv3d_fp8_plan_info* info, ConvParams* pp,
-                     Layout* lay) {
+                     Layout* lay, int pair_slots = 0) {
   if (!stride || !pad || !info) return CONV3D_EINVAL;
   if (N <= 0 || C <= 0 || D <= 0 || H <= 0 || W <= 0 || K <= 0 || T <= 0 || R <= 0 || S <= 0)
     return CONV3D_EINVAL;
@@ -125,7 +131,11 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
                     (route == kRouteIm2col &&
                      (o.cta_pair == 2 || (o.cta_pair == 0 && npq > kBlockM)));
   const int block_m = pair ? 2 * kBlockM : kBlockM;
-  const long long slots = pair ? std::max(1, sm_count / 2) : sm_count;  // co-resident units
+  // co-resident units: one per SM, or one per CTA pair; a CTA cap given in the options counts
+  long long slots = pair ? std::max(1, sm_count / 2) : sm_count;
+  if (pair && pair_slots > 0) slots = std::min<long long>(slots, pair_slots);
+  if (o.max_ctas > 0)
+    slots = std::min<long long>(slots, pair ? std::max(1, o.max_ctas / 2) : o.max_ctas);
 
   // grid route: the tiles of one image cover the first Do planes of its padded output grid
   const long long tiles_per_image =
@@ -140,15 +150,28 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   const long long tiles = m_tiles * n_tiles;
   long long splits = o.splits;
   if (splits < 0) return CONV3D_EINVAL;
+  // Tiles 0..full_tiles-1 are computed whole; the rest are split along K. By default: with fewer
+  // than half as many tiles as slots, every tile is split to fill the machine; with more tiles
+  // than slots, only the tiles of a last, mostly idle wave are split, over the slots that wave
+  // would leave idle. A split count in the options splits every tile that many ways.
+  long long full_tiles = 0;
   if (splits == 0) {
     splits = 1;
-    if (tiles * 2 <= slots && k_blocks >= 8)
+    if (tiles * 2 <= slots && k_blocks >= 8) {
       splits = std::max<long long>(1, std::min<long long>(slots / tiles, k_blocks / 4));
+    } else if (tiles > slots && k_blocks >= 4) {
+      const long long tail = tiles % slots;
+      if (tail > 0 && tail * 2 <= slots) {
+        full_tiles = tiles - tail;
+        splits = std::min<long long>(slots / tail, k_blocks);
+      }
+    }
   }
   splits = std::min(splits, k_blocks);
   const long long kbps = ceil_div(k_blocks, splits);
   splits = ceil_div(k_blocks, kbps);  // every split owns at least one K block
-  const long long units = tiles * splits;
+  if (splits == 1) full_tiles = tiles;
+  const long long units = full_tiles + (tiles - full_tiles) * splits;
   if (units >= (1LL << 31)) return CONV3D_EUNSUPPORTED;
 
   long long stage_bytes = kATileBytes + (long long)(pair ? block_n / 2 : block_n) * kBlockK;
@@ -158,8 +181,6 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   const int stages = (int)std::min<long long>(kMaxStages, kSmemBudget / stage_bytes);
   if (stages < (route == kRouteGrid ? 2 : 3)) return CONV3D_EUNSUPPORTED;
   long long grid = std::min<long long>(units, slots);
-  if (o.max_ctas > 0)
-    grid = std::min<long long>(grid, pair ? std::max(1, o.max_ctas / 2) : o.max_ctas);
   if (pair) grid *= 2;  // two CTAs per unit
   if (o.max_ctas < 0 || o.wait_timeout_ms < 0) return CONV3D_EINVAL;
 
@@ -169,7 +190,7 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   L.wp_off = (size_t)round_up((long long)L.xp_off + L.xp_bytes, 256);
   L.wp_bytes = (size_t)(K * kg);
   L.part_off = (size_t)round_up((long long)L.wp_off + L.wp_bytes, 256);
-  L.part_bytes = splits > 1 ? (size_t)(tiles * splits * block_n * block_m * 4) : 0;
+  L.part_bytes = (size_t)((tiles - full_tiles) * splits * block_n * block_m * 4);
   L.status_off = (size_t)round_up((long long)L.part_off + L.part_bytes, 256);
   L.total = L.status_off + 256;
 
@@ -186,6 +207,7 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   info->k_blocks = (int)k_blocks;
   info->splits = (int)splits;
   info->k_blocks_per_split = (int)kbps;
+  info->full_tiles = (int)full_tiles;
   info->stages = stages;
   info->row_chk = route == kRouteGrid ? 1 : (npq % block_m) != 0;
   info->grid = (int)grid;
@@ -218,6 +240,7 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
     p.k_blocks = (int)k_blocks;
     p.splits = (int)splits;
     p.kb_per_split = (int)kbps;
+    p.full_tiles = (int)full_tiles;
     p.num_units = (int)units;
     p.stages = stages;
     p.acc_stride = std::max(32, next_pow2(block_n));
@@ -388,6 +411,17 @@ conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t* out, int N, int C, int D, in
     delete plan;
     return st;
   }
+  if (plan->p.pair) {  // plan for the CTA pairs the device can actually hold at once
+    const int clusters = conv_pair_max_active_clusters(plan->p);
+    if (clusters > 0 && clusters < prop.multiProcessorCount / 2) {
+      st = decide(N, C, D, H, W, K, T, R, S, stride, pad, prop.multiProcessorCount, opts,
+                  &plan->info, &plan->p, &L, clusters);
+      if (st != CONV3D_OK) {
+        delete plan;
+        return st;
+      }
+    }
+  }
   plan->device = device;
   for (int i = 0; i < 3; ++i) {
     plan->stride[i] = stride[i];
@@ -465,9 +499,9 @@ conv3d_status conv3d_fp8_run(conv3d_fp8_plan_t plan, const void* x, const void* 
   if (launch_conv(p, plan->wmap, plan->xmap, plan->info.row_chk != 0, plan->info.grid, s) !=
       cudaSuccess)
     return CONV3D_ECUDA;
-  if (plan->ev_end && cudaEventRecord(plan->ev_end, s) != cudaSuccess) return CONV3D_ECUDA;
-  if (p.splits > 1 && launch_splitk_reduce(p, plan->info.row_chk != 0, s) != cudaSuccess)
+  if (has_split_tiles(p) && launch_splitk_reduce(p, plan->info.row_chk != 0, s) != cudaSuccess)
     return CONV3D_ECUDA;
+  if (plan->ev_end && cudaEventRecord(plan->ev_end, s) != cudaSuccess) return CONV3D_ECUDA;
   return CONV3D_OK;
 }
 
@@ -622,6 +656,13 @@ extern "C" conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int 
   Layout L{};
   st = decide(N, C, D, H, W, K, T, R, S, stride, pad, sms, nullptr, &info, &p, &L);
   if (st != CONV3D_OK) return st;
+  if (p.pair) {  // plan for the CTA pairs the device can actually hold at once
+    const int clusters = conv_pair_max_active_clusters(p);
+    if (clusters > 0 && clusters < sms / 2) {
+      st = decide(N, C, D, H, W, K, T, R, S, stride, pad, sms, nullptr, &info, &p, &L, clusters);
+      if (st != CONV3D_OK) return st;
+    }
+  }
   if (L.total > (size_t)CONV3D_FP8_NOALLOC_SCRATCH_BYTES) return CONV3D_EUNSUPPORTED;
 
   void* base = nullptr;
@@ -650,7 +691,7 @@ extern "C" conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int 
   if (launch_pack(p, s) != cudaSuccess) return CONV3D_ECUDA;
   if (launch_conv(p, wmap, xmap, info.row_chk != 0, info.grid, s) != cudaSuccess)
     return CONV3D_ECUDA;
-  if (p.splits > 1 && launch_splitk_reduce(p, info.row_chk != 0, s) != cudaSuccess)
+  if (has_split_tiles(p) && launch_splitk_reduce(p, info.row_chk != 0, s) != cudaSuccess)
     return CONV3D_ECUDA;
   return CONV3D_OK;
 }

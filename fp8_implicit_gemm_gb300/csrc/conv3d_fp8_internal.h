@@ -52,6 +52,8 @@ struct ConvParams {
   int block_m;           // M tile: 128 (one CTA) or 256 (CTA pair)
   int block_n;           // N tile (multiple of 32, <= 256)
   int m_tiles, n_tiles, k_blocks, splits, kb_per_split, num_units;
+  int full_tiles;        // tiles 0..full_tiles-1 are computed whole (one unit each, bf16 out);
+                         // the others are split `splits` ways along K into fp32 partials
   int stages;
   int tmem_cols;         // allocated TMEM columns (power of two)
   int acc_stride;        // TMEM column offset between the two accumulator buffers
@@ -63,7 +65,7 @@ struct ConvParams {
   uint16_t* y;           // bf16 NCDHW (caller's)
   const float* scale_x;
   const float* scale_w;
-  float* partials;       // fp32 [tile][split][block_n][block_m] when splits > 1 (workspace)
+  float* partials;       // fp32 [tile - full_tiles][split][block_n][block_m] (workspace)
   int* status;           // status word (workspace)
   unsigned long long timeout_ns;
   int debug_flags;

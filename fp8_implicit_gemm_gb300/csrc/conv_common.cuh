@@ -9,19 +9,30 @@
 namespace c3d {
 
 // One work unit: an M tile of block_m rows, an N tile of block_n channels and a slice [kb0, kb1)
-// of the K blocks. Units are numbered split-fastest, then n-tile, then m-tile.
+// of the K blocks. The first full_tiles units are whole tiles (part = -1); after them come the
+// remaining tiles, each split `splits` ways along K, split-fastest (part = index of the unit's
+// fp32 partial slice). Tiles are numbered n-tile fastest.
 struct Unit {
-  int tile, m_tile, n_tile, split, kb0, kb1;
+  int tile, m_tile, n_tile, split, kb0, kb1, part;
 };
 
 __device__ __forceinline__ Unit decode_unit(const ConvParams& p, int u) {
   Unit r;
-  r.split = u % p.splits;
-  r.tile = u / p.splits;
+  if (u < p.full_tiles) {
+    r.tile = u;
+    r.split = 0;
+    r.part = -1;
+    r.kb0 = 0;
+    r.kb1 = p.k_blocks;
+  } else {
+    r.part = u - p.full_tiles;
+    r.split = r.part % p.splits;
+    r.tile = p.full_tiles + r.part / p.splits;
+    r.kb0 = r.split * p.kb_per_split;
+    r.kb1 = min(r.kb0 + p.kb_per_split, p.k_blocks);
+  }
   r.n_tile = r.tile % p.n_tiles;
   r.m_tile = r.tile / p.n_tiles;
-  r.kb0 = r.split * p.kb_per_split;
-  r.kb1 = min(r.kb0 + p.kb_per_split, p.k_blocks);
   return r;
 }
 
@@ -92,14 +103,14 @@ __device__ __forceinline__ RowDest row_dest(const ConvParams& p, int m_tile, int
 
 // Epilogue of one thread: its accumulator row (TMEM lane) of one unit, `trow` = TMEM address of the
 // row's first column in the current buffer. `row_in_tile` is the row within the unit's block_m
-// rows. Without split-K: y = bf16(acc * scale), stored only if the row is a real output and
-// col < K. With split-K: the raw fp32 row goes to the unit's slice of the partials,
-// [tile][split][block_n][block_m]. kRowChk = false compiles the row test out (every row real).
+// rows. A whole tile: y = bf16(acc * scale), stored only if the row is a real output and
+// col < K. A split unit: the raw fp32 row goes to the unit's slice of the partials,
+// [part][block_n][block_m]. kRowChk = false compiles the row test out (every row real).
 template <bool kRowChk>
 __device__ __forceinline__ void epilogue_row(const ConvParams& p, const Unit& un, uint32_t trow,
                                              int row_in_tile, float scale) {
   const int n0 = un.n_tile * p.block_n;
-  if (p.splits == 1) {
+  if (un.part < 0) {
     const RowDest dst = row_dest(p, un.m_tile, row_in_tile);
     const bool row_ok = !kRowChk || dst.valid;
     uint16_t* ybase = p.y + dst.y_off;
@@ -120,8 +131,7 @@ __device__ __forceinline__ void epilogue_row(const ConvParams& p, const Unit& un
       }
     }
   } else {
-    float* dst = p.partials +
-                 ((long long)(un.tile * p.splits + un.split) * p.block_n) * p.block_m + row_in_tile;
+    float* dst = p.partials + ((long long)un.part * p.block_n) * p.block_m + row_in_tile;
     for (int cc = 0; cc < p.block_n; cc += 32) {
       uint32_t r[32];
       tmem_ld_32x32b_x32(trow + cc, r);

@@ -170,26 +170,28 @@ cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream) {
   return cudaGetLastError();
 }
 
-// Split-K reduction: y = bf16(scale * sum_{split = 0..splits-1} partial[split]) in ascending split
-// order, so the result is bitwise reproducible for a fixed plan. One thread per (tile, column,
-// row); the stores carry the same guards as the main epilogue (real output row, col < K).
+// Split-K reduction of the split tiles (full_tiles..m_tiles*n_tiles-1):
+// y = bf16(scale * sum_{split = 0..splits-1} partial[split]) in ascending split order, so the
+// result is bitwise reproducible for a fixed plan. One thread per (tile, column, row); the stores
+// carry the same guards as the main epilogue (real output row, col < K).
 template <bool kRowChk>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(ConvParams p) {
   const long long per_tile = (long long)p.block_n * p.block_m;
-  const long long total = (long long)p.m_tiles * p.n_tiles * per_tile;
+  const long long total = ((long long)p.m_tiles * p.n_tiles - p.full_tiles) * per_tile;
   const float scale = __ldg(p.scale_x) * __ldg(p.scale_w);
   for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < total;
        g += (long long)gridDim.x * blockDim.x) {
     const int row = (int)(g % p.block_m);
     const int col_l = (int)((g / p.block_m) % p.block_n);
-    const long long tile = g / per_tile;
+    const long long t = g / per_tile;  // index among the split tiles
+    const long long tile = p.full_tiles + t;
     const int n_tile = (int)(tile % p.n_tiles);
     const int m_tile = (int)(tile / p.n_tiles);
     const int col = n_tile * p.block_n + col_l;
     if (col >= p.K) continue;
     const RowDest dst = row_dest(p, m_tile, row);
     if (kRowChk && !dst.valid) continue;
-    const float* src = p.partials + ((tile * p.splits) * p.block_n + col_l) * p.block_m + row;
+    const float* src = p.partials + ((t * p.splits) * p.block_n + col_l) * p.block_m + row;
     float acc = 0.0f;
     for (int s = 0; s < p.splits; ++s) acc += __ldcg(src + (long long)s * per_tile);
     const __nv_bfloat16 b = __float2bfloat16_rn(acc * scale);
@@ -198,7 +200,9 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(ConvParams p) {
 }
 
 cudaError_t launch_splitk_reduce(const ConvParams& p, bool row_chk, cudaStream_t stream) {
-  const long long total = (long long)p.m_tiles * p.n_tiles * p.block_n * p.block_m;
+  const long long total =
+      ((long long)p.m_tiles * p.n_tiles - p.full_tiles) * p.block_n * p.block_m;
+  if (total <= 0) return cudaSuccess;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

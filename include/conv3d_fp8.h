@@ -78,7 +78,7 @@ typedef struct {
                                  block_m) over the padded grid), ceil(K / block_n) */
     int k_blocks;             /* ceil(k_gemm / 128); on the padded-grid route the number of
                                  (t, r, channel block) groups, each S taps wide */
-    int splits;               /* K slices; > 1 means the split-K path (fp32 partials + reduce) */
+    int splits;               /* K slices of each split tile (fp32 partials + a reduction) */
     int k_blocks_per_split;
     int stages;               /* shared-memory pipeline depth */
     int row_chk;              /* 1 when npq % block_m != 0: the row guard is compiled in */
@@ -87,6 +87,10 @@ typedef struct {
     size_t workspace_bytes;   /* device workspace the plan owns */
     int route;                /* 1: gather, 2: TMA im2col, 3: padded grid (as in options) */
     int cta_pair;             /* 1: one CTA per tile, 2: CTA pairs (as in options) */
+    int full_tiles;           /* tiles computed whole; the other m_tiles*n_tiles - full_tiles
+                                 are split `splits` ways. With splits == 1 every tile is whole;
+                                 a split count in the options splits every tile; by default
+                                 only the tiles of a mostly idle last wave are split */
 } conv3d_fp8_plan_info;
 
 /*
@@ -126,8 +130,9 @@ conv3d_status conv3d_fp8_run(conv3d_fp8_plan_t plan, const void *x_ncdhw, const 
 /*
  * Measurement hook: while ev_begin / ev_end (cudaEvent_t values passed as void*; either may be
  * NULL) are set, every run of this plan records ev_begin on its stream immediately before the
- * main implicit-GEMM kernel and ev_end immediately after it, so a caller can time that kernel
- * alone. The caller owns the events. Pass NULL, NULL to stop. Errors: EINVAL for a NULL plan.
+ * main implicit-GEMM kernel and ev_end immediately after it, or after the reduction of its
+ * split tiles when it has some, so a caller can time the GEMM apart from the operand packing.
+ * The caller owns the events. Pass NULL, NULL to stop. Errors: EINVAL for a NULL plan.
  */
 conv3d_status conv3d_fp8_set_timing_events(conv3d_fp8_plan_t plan, void *ev_begin, void *ev_end);
 

@@ -67,9 +67,10 @@ def test_describe_configs(lib):
     assert [i["row_chk"] for i in single] == [1, 0, 0, 0, 1]
     for i in infos:
         assert i["grid"] % (2 if i["cta_pair"] == 2 else 1) == 0
-    # deep and narrow -> split-K; the large layers never split
-    assert infos[3]["splits"] > 1
-    assert infos[2]["splits"] == 1 and infos[4]["splits"] == 1
+    # deep and narrow -> every tile split along K; the 65536-position layer fills its waves well
+    # enough to compute every tile whole
+    assert infos[3]["splits"] > 1 and infos[3]["full_tiles"] == 0
+    assert infos[2]["splits"] == 1 and infos[2]["full_tiles"] == infos[2]["m_tiles"]
     for i in infos:
         kb = i["k_blocks"]
         assert i["splits"] * i["k_blocks_per_split"] >= kb
@@ -96,8 +97,8 @@ def test_describe_routes(lib):
     assert _describe(big_pad)["route"] == 3                      # the padded grid takes any pad
     # the gather and grid routes' packed copy carries the zero halo, the im2col one does not
     s = synth.CONFIGS[2]
-    assert _describe(s, route=1)["workspace_bytes"] > _describe(s, route=2)["workspace_bytes"]
-    assert _describe(s, route=3)["workspace_bytes"] == _describe(s, route=1)["workspace_bytes"]
+    ws = {r: _describe(s, route=r, splits=1)["workspace_bytes"] for r in (1, 2, 3)}
+    assert ws[1] > ws[2] and ws[3] == ws[1]
 
 
 def test_describe_pair_rules(lib):
@@ -110,6 +111,26 @@ def test_describe_pair_rules(lib):
     assert _describe(synth.CONFIGS[4], cta_pair=1)["route"] == 2   # no grid route on one CTA
     i = _describe(synth.CONFIGS[4], max_ctas=9)                    # pairs round the cap down
     assert i["grid"] == 8
+
+
+def test_describe_tail_split(lib):
+    # large layer on 76 CTA pairs: 990 tiles = 13 full waves + 2 tiles; those 2 are split along K
+    # over the idle pairs of the last wave (18 groups of taps: one per split, 36 units)
+    i = _describe(synth.CONFIGS[4])
+    assert i["full_tiles"] == 13 * 76 and i["splits"] == 18 and i["k_blocks_per_split"] == 1
+    units = i["full_tiles"] + (i["m_tiles"] * i["n_tiles"] - i["full_tiles"]) * i["splits"]
+    assert units == 13 * 76 + 36 and i["grid"] == 152
+    assert i["workspace_bytes"] >= 36 * 256 * 256 * 4               # fp32 partials of the tail
+    # a CTA cap changes the waves: 75 pairs -> 13 waves + 15 tiles, split 5 ways (4 groups each)
+    i = _describe(synth.CONFIGS[4], max_ctas=150)
+    assert i["full_tiles"] == 13 * 75 and i["splits"] == 5 and i["k_blocks_per_split"] == 4
+    # a last wave more than half full is left alone (one CTA per tile: 1913 = 12 * 152 + 89)
+    i = _describe(synth.CONFIGS[4], cta_pair=1)
+    assert i["full_tiles"] == i["m_tiles"] == 1913 and i["splits"] == 1
+    # a split count in the options applies to every tile
+    assert _describe(synth.CONFIGS[4], splits=1)["full_tiles"] == 990
+    i = _describe(synth.CONFIGS[4], splits=3)
+    assert i["full_tiles"] == 0 and i["splits"] == 3
 
 
 def test_describe_forced_options(lib):

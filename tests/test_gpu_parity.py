@@ -134,6 +134,20 @@ def test_max_ctas_small_grid_many_tiles(kernel):
     assert info["grid"] == 2
 
 
+# A CTA cap that leaves a mostly idle last wave: its tiles are split along K over the idle slots
+# while the others are computed whole, in one launch (whole tiles store bf16, split tiles fp32
+# partials that the reduction then sums).
+TAIL_CASES = {"gather-1cta": 12, "im2col-1cta": 12, "im2col-pair": 12, "grid-pair": 16}
+
+
+@pytest.mark.parametrize("kernel", list(TAIL_CASES))
+def test_tail_tiles_split_along_k(kernel):
+    res, info = _full_case(synth.CONFIGS[1], synth.config_seed(1), max_ctas=TAIL_CASES[kernel],
+                           **KERNELS[kernel])
+    tiles = info["m_tiles"] * info["n_tiles"]
+    assert 0 < info["full_tiles"] < tiles and info["splits"] > 1, info
+
+
 def test_split_k_is_reproducible_and_close_across_split_counts():
     shape = synth.CONFIGS[3]
     inp = synth.make_config_inputs(3)
