@@ -32,7 +32,8 @@ class Conv3dFp8Error(RuntimeError):
 class Options(ctypes.Structure):
     _fields_ = [("splits", ctypes.c_int), ("block_n", ctypes.c_int), ("max_ctas", ctypes.c_int),
                 ("wait_timeout_ms", ctypes.c_int), ("debug_flags", ctypes.c_int),
-                ("route", ctypes.c_int), ("cta_pair", ctypes.c_int)]
+                ("route", ctypes.c_int), ("cta_pair", ctypes.c_int),
+                ("input_layout", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):

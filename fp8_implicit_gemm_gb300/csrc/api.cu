@@ -19,7 +19,8 @@ struct conv3d_fp8_plan_s {
   int pad[3] = {0, 0, 0};
   ConvParams p{};
   CUtensorMap wmap{};
-  CUtensorMap xmap{};  // im2col map of the packed x (im2col route only)
+  CUtensorMap xmap{};  // A tensor map (TMA routes)
+  const void* xmap_src = nullptr;  // caller's x the A map was last encoded for (channels-last x)
   conv3d_fp8_plan_info info{};
   void* workspace = nullptr;
   cudaEvent_t ev_begin = nullptr;  // measurement hook, caller-owned
@@ -78,7 +79,10 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   const long long kg = taps * C;
   conv3d_fp8_options o{};
   if (opts) o = *opts;
-  if (o.route < 0 || o.route > 3 || o.cta_pair < 0 || o.cta_pair > 2) return CONV3D_EINVAL;
+  if (o.route < 0 || o.route > 3 || o.cta_pair < 0 || o.cta_pair > 2 || o.input_layout < 0 ||
+      o.input_layout > 1)
+    return CONV3D_EINVAL;
+  const bool x_cl = o.input_layout == 1;  // the caller's x is channels-last
   // The TMA im2col route needs C in whole 32-byte sub-tile rows and bounding-box corners
   // (-pad, pad - (filter - 1)) inside the [-16, 15] range of a rank-5 im2col tensor map.
   bool im2col_ok = (C % 32 == 0);
@@ -89,10 +93,13 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   }
   if (o.route == 2 && !im2col_ok) return CONV3D_EUNSUPPORTED;
   // The padded-grid route (CTA pairs only) needs stride 1 on every axis, whole 32-byte channel
-  // blocks and an A tile of 128 + S - 1 <= 256 rows. By default it is taken when the rows of the
-  // padded grid that are not outputs cost at most 30% extra MMA work.
+  // blocks and an A tile of 128 + S - 1 <= 256 rows; reading a channels-last x of the caller it
+  // also needs pads up to 15 (its im2col bounding box runs from -pad to extent - 1 + pad). By
+  // default it is taken when the rows of the padded grid that are not outputs cost at most 30%
+  // extra MMA work.
   const bool grid_ok = C % 32 == 0 && stride[0] == 1 && stride[1] == 1 && stride[2] == 1 &&
-                       S <= 129 && o.cta_pair != 1;
+                       S <= 129 && o.cta_pair != 1 &&
+                       (!x_cl || (pad[0] <= 15 && pad[1] <= 15 && pad[2] <= 15));
   if (o.route == 3 && !grid_ok) return CONV3D_EUNSUPPORTED;
   const double grid_overhead =
       (double)(H + 2LL * pad[1]) * (double)(W + 2LL * pad[2]) / ((double)Ho * (double)Wo);
@@ -108,16 +115,21 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   else
     route = im2col_ok ? kRouteIm2col : kRouteGather;
   const int a_cb = C % 128 == 0 ? 128 : (C % 64 == 0 ? 64 : 32);
-  const bool halo_on = route != kRouteIm2col;  // gather and grid routes read a zero-padded copy
+  // A zero-padded channels-last copy of x for the gather route, and for the padded-grid route
+  // when the library transposes x anyway; the TMA routes read a channels-last x of the caller
+  // directly (no copy at all), and the im2col route's copy needs no halo.
+  const bool keep_copy = !x_cl || route == kRouteGather;
+  const bool halo_on = route == kRouteGather || (route == kRouteGrid && !x_cl);
   const int halo[3] = {halo_on ? pad[0] : 0, halo_on ? pad[1] : 0, halo_on ? pad[2] : 0};
   const long long Dp = D + 2LL * halo[0], Hp = H + 2LL * halo[1], Wp = W + 2LL * halo[2];
+  const long long Dg = D + 2LL * pad[0], Hg = H + 2LL * pad[1], Wg = W + 2LL * pad[2];
   const long long y_elems = npq * K;
   const long long x_elems = (long long)N * C * D * H * W;
-  const long long xp_elems = (long long)N * Dp * Hp * Wp * C;
+  const long long xp_elems = keep_copy ? (long long)N * Dp * Hp * Wp * C : 0;
   // 32-bit limits of the index arithmetic inside the kernels.
   if (npq + kBlockM >= (1LL << 31) || kg + kBlockK >= (1LL << 31) || y_elems >= (1LL << 40) ||
-      x_elems >= (1LL << 40) || xp_elems >= (1LL << 40) || Dp >= (1LL << 30) ||
-      Hp >= (1LL << 30) || Wp >= (1LL << 30) || K >= (1 << 30) || taps >= (1 << 20))
+      x_elems >= (1LL << 40) || xp_elems >= (1LL << 40) || Dg >= (1LL << 30) ||
+      Hg >= (1LL << 30) || Wg >= (1LL << 30) || K >= (1 << 30) || taps >= (1 << 20))
     return CONV3D_EUNSUPPORTED;
 
   int block_n = o.block_n;
@@ -137,15 +149,15 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   if (o.max_ctas > 0)
     slots = std::min<long long>(slots, pair ? std::max(1, o.max_ctas / 2) : o.max_ctas);
 
-  // grid route: the tiles of one image cover the first Do planes of its padded output grid
+  // grid route: the tiles of one image cover the first Do planes of its padded grid
   const long long tiles_per_image =
-      route == kRouteGrid ? ceil_div((long long)Do * Hp * Wp, block_m) : 0;
+      route == kRouteGrid ? ceil_div((long long)Do * Hg * Wg, block_m) : 0;
   const long long m_tiles = route == kRouteGrid ? N * tiles_per_image : ceil_div(npq, block_m);
   const long long n_tiles = ceil_div(K, block_n);
   // K blocks: 128 bytes of K_gemm, or on the grid route one (t, r, channel block) group of S taps
   const long long k_blocks =
       route == kRouteGrid ? (long long)T * R * (C / a_cb) : ceil_div(kg, kBlockK);
-  if (route == kRouteGrid && (long long)N * Dp * Hp * Wp + 256 >= (1LL << 31))
+  if (route == kRouteGrid && (long long)N * Dg * Hg * Wg + 256 >= (1LL << 31))
     return CONV3D_EUNSUPPORTED;
   const long long tiles = m_tiles * n_tiles;
   long long splits = o.splits;
@@ -227,6 +239,9 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
     p.a_cb = a_cb;
     p.pk_pd = halo[0]; p.pk_ph = halo[1]; p.pk_pw = halo[2];
     p.Dp = (int)Dp; p.Hp = (int)Hp; p.Wp = (int)Wp;
+    p.Dg = (int)Dg; p.Hg = (int)Hg; p.Wg = (int)Wg;
+    p.x_cl = x_cl ? 1 : 0;
+    p.a_grid_im2col = route == kRouteGrid && x_cl ? 1 : 0;
     p.dhw = (int)dhw;
     p.tiles_per_image = (int)tiles_per_image;
     p.npq = (int)npq;
@@ -312,11 +327,14 @@ EncodeIm2colFn get_encode_im2col() {
   return fn;
 }
 
-// The packed x as a channels-last 5D tensor (C, W, H, D, N). One load brings 128 consecutive
-// output positions (the traversal walks W, then H, D and N, over the starting pixels of the
-// filter windows: from -pad to extent - 1 + pad - (filter - 1), every `stride`), a_cb channels
-// each, shifted by the tap given with the load; everything outside the tensor reads zero.
-conv3d_status encode_im2col_map(CUtensorMap* map, void* xcl, const ConvParams& p) {
+// The packed x as a channels-last 5D tensor (C, W, H, D, N), read in im2col mode; everything
+// outside the tensor reads zero. im2col route: one load brings 128 consecutive output positions
+// (the traversal walks W, then H, D and N, over the starting pixels of the filter windows: from
+// -pad to extent - 1 + pad - (filter - 1), every `stride`), a_cb channels each, shifted by the
+// tap given with the load. Padded-grid route: the traversal walks the whole zero-padded grid
+// (from -pad to extent - 1 + pad, stride 1) and one load brings 128 + S - 1 consecutive grid
+// positions, shifted by the (r, t) of the load; the S taps along W are row offsets into it.
+conv3d_status encode_im2col_map(CUtensorMap* map, void* xcl, const ConvParams& p, bool grid) {
   EncodeIm2colFn enc = get_encode_im2col();
   if (!enc) return CONV3D_ECUDA;
   const cuuint64_t dims[5] = {(cuuint64_t)p.C, (cuuint64_t)p.W, (cuuint64_t)p.H, (cuuint64_t)p.D,
@@ -324,31 +342,52 @@ conv3d_status encode_im2col_map(CUtensorMap* map, void* xcl, const ConvParams& p
   const cuuint64_t strides[4] = {(cuuint64_t)p.C, (cuuint64_t)p.C * p.W,
                                  (cuuint64_t)p.C * p.W * p.H, (cuuint64_t)p.C * p.W * p.H * p.D};
   const int lower[3] = {-p.pw, -p.ph, -p.pd};
-  const int upper[3] = {p.pw - (p.S - 1), p.ph - (p.R - 1), p.pd - (p.T - 1)};
+  int upper[3] = {p.pw - (p.S - 1), p.ph - (p.R - 1), p.pd - (p.T - 1)};
+  if (grid) {
+    upper[0] = p.pw;
+    upper[1] = p.ph;
+    upper[2] = p.pd;
+  }
+  const cuuint32_t rows = grid ? (cuuint32_t)(kBlockM + p.S - 1) : (cuuint32_t)kBlockM;
   const cuuint32_t estr[5] = {1, (cuuint32_t)p.sw, (cuuint32_t)p.sh, (cuuint32_t)p.sd, 1};
   const CUtensorMapSwizzle sw = p.a_cb == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
                                 : p.a_cb == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
                                                : CU_TENSOR_MAP_SWIZZLE_32B;
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, xcl, dims, strides, lower, upper,
-                   (cuuint32_t)p.a_cb, (cuuint32_t)kBlockM, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                   (cuuint32_t)p.a_cb, rows, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? CONV3D_OK : CONV3D_ECUDA;
 }
 
+// Whether the A tensor map reads the caller's x (a channels-last x on a TMA route), so that it is
+// encoded per run rather than once per plan.
+bool xmap_reads_caller_x(const ConvParams& p) { return p.x_cl && p.route != kRouteGather; }
+
+// A tensor map of a plan: im2col map of the unpadded channels-last x (the im2col route, and the
+// padded-grid route reading a channels-last x of the caller), or 2D tiles of 128 + S - 1 rows of
+// the zero-padded copy viewed as [N*Dg*Hg*Wg][C] (padded-grid route). `x_cl` is the caller's
+// channels-last x, used when the map reads it.
+conv3d_status encode_xmap(CUtensorMap* xmap, const ConvParams& p, const void* x_cl) {
+  void* src = xmap_reads_caller_x(p) ? const_cast<void*>(x_cl) : static_cast<void*>(p.xp);
+  if (p.route == kRouteIm2col) return encode_im2col_map(xmap, src, p, false);
+  if (p.route == kRouteGrid) {
+    if (p.a_grid_im2col) return encode_im2col_map(xmap, src, p, true);
+    return encode_2d(xmap, src, (long long)p.N * p.Dg * p.Hg * p.Wg, p.C, p.a_cb,
+                     kBlockM + p.S - 1);
+  }
+  return CONV3D_OK;
+}
+
 // Tensor maps of a plan. B: the packed weights [K][kg]; a box is one K block (128 bytes, or a_cb
-// bytes of one tap on the grid route) of block_n rows (block_n / 2 per CTA of a pair).
-// A: im2col map of the unpadded channels-last x (im2col route), or 2D tiles of 128 + S - 1 rows
-// of the padded channels-last x viewed as [N*Dp*Hp*Wp][C] (grid route).
+// bytes of one tap on the grid route) of block_n rows (block_n / 2 per CTA of a pair). A: as
+// above, unless it reads the caller's x (then each run encodes it).
 conv3d_status encode_maps(CUtensorMap* wmap, CUtensorMap* xmap, const ConvParams& p) {
   const int b_rows = p.pair ? p.block_n / 2 : p.block_n;
   const int b_cols = p.route == kRouteGrid ? p.a_cb : kBlockK;
   conv3d_status st = encode_2d(wmap, p.wp, p.K, p.kg, b_cols, b_rows);
   if (st != CONV3D_OK) return st;
-  if (p.route == kRouteIm2col) return encode_im2col_map(xmap, p.xp, p);
-  if (p.route == kRouteGrid)
-    return encode_2d(xmap, p.xp, (long long)p.N * p.Dp * p.Hp * p.Wp, p.C, p.a_cb,
-                     kBlockM + p.S - 1);
-  return CONV3D_OK;
+  if (xmap_reads_caller_x(p)) return CONV3D_OK;
+  return encode_xmap(xmap, p, nullptr);
 }
 
 struct DeviceGuard {
@@ -445,7 +484,7 @@ conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t* out, int N, int C, int D, in
     return CONV3D_ENOMEM;
   }
   uint8_t* ws = static_cast<uint8_t*>(plan->workspace);
-  plan->p.xp = ws + L.xp_off;
+  plan->p.xp = L.xp_bytes ? ws + L.xp_off : nullptr;
   plan->p.wp = ws + L.wp_off;
   plan->p.partials = L.part_bytes ? reinterpret_cast<float*>(ws + L.part_off) : nullptr;
   plan->p.status = reinterpret_cast<int*>(ws + L.status_off);
@@ -494,6 +533,11 @@ conv3d_status conv3d_fp8_run(conv3d_fp8_plan_t plan, const void* x, const void* 
   p.scale_x = scale_x;
   p.scale_w = scale_w;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (xmap_reads_caller_x(p) && plan->xmap_src != x) {
+    const conv3d_status st = encode_xmap(&plan->xmap, p, x);
+    if (st != CONV3D_OK) return st;
+    plan->xmap_src = x;
+  }
   if (launch_pack(p, s) != cudaSuccess) return CONV3D_ECUDA;
   if (plan->ev_begin && cudaEventRecord(plan->ev_begin, s) != cudaSuccess) return CONV3D_ECUDA;
   if (launch_conv(p, plan->wmap, plan->xmap, plan->info.row_chk != 0, plan->info.grid, s) !=
@@ -669,7 +713,7 @@ extern "C" conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int 
   st = noalloc_setup(dev, &base);
   if (st != CONV3D_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(base);
-  p.xp = ws + L.xp_off;
+  p.xp = L.xp_bytes ? ws + L.xp_off : nullptr;
   p.wp = ws + L.wp_off;
   p.partials = L.part_bytes ? reinterpret_cast<float*>(ws + L.part_off) : nullptr;
   p.status = reinterpret_cast<int*>(ws + L.status_off);

@@ -19,9 +19,9 @@ constexpr int kMaxStages = 8;
 enum : int {
   kRouteGather = 0,  // 16-byte cp.async gathers from a zero-padded channels-last copy of x
   kRouteIm2col = 1,  // TMA im2col loads from an unpadded channels-last copy (C % 32 == 0)
-  kRouteGrid = 2,    // stride 1: M indexes the zero-padded output grid, so every tap is a row
-                     // shift of one 2D view of the padded channels-last copy; one TMA tile of
-                     // 128 + S - 1 rows feeds the S taps along W (CTA pairs only)
+  kRouteGrid = 2,    // stride 1: M indexes the zero-padded grid of the input, so every tap is a
+                     // shift along that grid; one TMA load of 128 + S - 1 grid positions feeds
+                     // the S taps along W (CTA pairs only)
 };
 
 // Status-word bits recorded by kernels whose bounded waits ran out.
@@ -42,8 +42,12 @@ struct ConvParams {
   int a_cb;              // im2col route: channels per A sub-tile (32, 64 or 128 = its row bytes)
   int pk_pd, pk_ph, pk_pw;  // zero halo of the packed channels-last x (gather route only)
   int Dp, Hp, Wp;        // extents of the packed channels-last copy of x (halo included)
+  int Dg, Hg, Wg;        // padded-grid route: extents of the zero-padded grid, D + 2 pd, ...
+  int x_cl;              // the caller's x is channels-last (NDHWC): no transpose in the pack
+  int a_grid_im2col;     // padded-grid route: A by im2col loads from an unpadded channels-last x
+                         // (the caller's); otherwise by 2D tiles of the zero-padded copy
   int dhw;               // Do*Ho*Wo
-  int tiles_per_image;   // padded-grid route: M tiles per image (rows of d < Do planes only)
+  int tiles_per_image;   // padded-grid route: M tiles per image (grid rows of d < Do planes)
   int npq;               // N*dhw, the M of the GEMM view
   int taps;              // T*R*S
   int kg;                // taps*C, the K of the GEMM view
@@ -58,9 +62,10 @@ struct ConvParams {
   int tmem_cols;         // allocated TMEM columns (power of two)
   int acc_stride;        // TMEM column offset between the two accumulator buffers
   // tensors
-  const uint8_t* x;      // e4m3 NCDHW (caller's)
+  const uint8_t* x;      // e4m3 NCDHW, or NDHWC when x_cl (caller's)
   const uint8_t* w;      // e4m3 KCTRS (caller's)
-  uint8_t* xp;           // e4m3 [N][Dp][Hp][Wp][C], zero halo (workspace)
+  uint8_t* xp;           // e4m3 [N][Dp][Hp][Wp][C], zero halo (workspace; null when the TMA
+                         // routes read a channels-last x of the caller directly)
   uint8_t* wp;           // e4m3 [K][taps][C] (workspace)
   uint16_t* y;           // bf16 NCDHW (caller's)
   const float* scale_x;

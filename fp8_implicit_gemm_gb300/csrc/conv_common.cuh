@@ -73,7 +73,7 @@ __device__ __forceinline__ void sleep_ns_bounded(uint64_t ns) {
 // and the NCDHW offset of its channel-0 element (channel k adds k * dhw).
 //  - output-position routes: row m = m_tile * block_m + row_in_tile is output position m of the
 //    GEMM view; it is real iff m < npq (the row guard of the subject page);
-//  - padded-grid route: rows index the zero-padded output grid of one image, tile by tile
+//  - padded-grid route: rows index the zero-padded grid of one image, tile by tile
 //    (tiles_per_image tiles per image, none straddling two images); position (d, h, w) of that grid
 //    is real iff d < Do, h < Ho and w < Wo.
 struct RowDest {
@@ -85,11 +85,11 @@ __device__ __forceinline__ RowDest row_dest(const ConvParams& p, int m_tile, int
   if (p.route == kRouteGrid) {
     const int n = m_tile / p.tiles_per_image;
     const int mg = (m_tile - n * p.tiles_per_image) * p.block_m + row_in_tile;
-    const int hw = p.Hp * p.Wp;
+    const int hw = p.Hg * p.Wg;
     const int d = mg / hw;
     const int rem = mg - d * hw;
-    const int h = rem / p.Wp;
-    const int w = rem - h * p.Wp;
+    const int h = rem / p.Wg;
+    const int w = rem - h * p.Wg;
     r.valid = d < p.Do && h < p.Ho && w < p.Wo;
     r.y_off = r.valid ? (long long)n * p.K * p.dhw + ((long long)d * p.Ho + h) * p.Wo + w : 0;
   } else {

@@ -16,12 +16,14 @@
 // K block, so shared-memory traffic per MMA cycle drops from 192 to 128 bytes and more stages fit.
 //
 // kGrid (stride-1 convolutions): the rows of a unit are 256 consecutive positions of the
-// zero-padded output grid of one image, so the A rows of tap (t, r, s) are rows
-// (t*Hp + r)*Wp + s further down one 2D view [N*Dp*Hp*Wp][C] of the padded channels-last input.
-// A stage holds one (t, r, channel block): a single TMA tile of 128 + S - 1 rows serves the S taps
-// along W (their MMA descriptors start s rows into it; the 128-byte swizzle is a function of the
-// shared-memory address, so the shifted start reads the rows TMA wrote there), plus the S matching
-// B tiles. That cuts the bytes each SM's TMA unit must bring in per MMA by about a third, which is
+// zero-padded grid of one image (Dg x Hg x Wg, the input with its pads), so the A rows of tap
+// (t, r, s) are the grid positions (t*Hg + r)*Wg + s further on. A stage holds one
+// (t, r, channel block): a single TMA load of 128 + S - 1 consecutive grid positions serves the S
+// taps along W (their MMA descriptors start s rows into it; the 128-byte swizzle is a function of
+// the shared-memory address, so the shifted start reads the rows TMA wrote there), plus the S
+// matching B tiles. The load is a 2D tile of a zero-padded channels-last copy when the library
+// packs x itself, or an im2col load whose traversal covers the padded grid of the caller's
+// unpadded channels-last x (zeros outside the volume) when x comes channels-last. That cuts the bytes each SM's TMA unit must bring in per MMA by about a third, which is
 // what bounds the output-position route. Rows of the grid that are not outputs (h >= Ho, w >= Wo,
 // d >= Do) are computed and never stored.
 // Every wait is bounded; a wait that runs out records a status bit and both CTAs wind down.
@@ -134,10 +136,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         const Unit un = decode_unit(p, u);
         bool aborted = false;
         if (kGrid) {
-          // first padded-grid row of this CTA's 128 rows, as a row of the [N*Dp*Hp*Wp][C] view
+          // first padded-grid position of this CTA's 128 rows: as a row of the [N*Dg*Hg*Wg][C]
+          // view of the zero-padded copy (2D loads), or as the unpadded coordinates the im2col
+          // traversal starts from (rows past an image's grid continue into the next image, as
+          // the traversal does)
           const int n = un.m_tile / p.tiles_per_image;
-          const int xrow0 = n * p.Dp * p.Hp * p.Wp +
-                            (un.m_tile - n * p.tiles_per_image) * p.block_m + row_base;
+          const int g0 = (un.m_tile - n * p.tiles_per_image) * p.block_m + row_base;
+          const int xrow0 = n * p.Dg * p.Hg * p.Wg + g0;
+          const int plane = p.Hg * p.Wg;
+          int gd = g0 / plane;
+          const int grem = g0 - gd * plane;
+          const int gh = grem / p.Wg;
+          const int w0 = grem - gh * p.Wg - p.pw, h0 = gh - p.ph;
+          const int n0 = n + gd / p.Dg;
+          gd = gd % p.Dg;
+          const int d0 = gd - p.pd;
           const int ncb = p.C / p.a_cb;
           int tt, tr, cb;  // (t, r, channel block) of the unit's first group
           {
@@ -158,8 +171,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
               const uint32_t bar = leader_bars + (full(stage) - bars_u32);
               if (leader) mbar_arrive_expect_tx(full(stage), tx);
               const int c0 = cb * p.a_cb;
-              tma_load_2d_pair(sA_u32 + (uint32_t)stage * a_bytes, &xmap, bar, c0,
-                               xrow0 + (tt * p.Hp + tr) * p.Wp);
+              if (p.a_grid_im2col)
+                tma_load_im2col_5d_pair(sA_u32 + (uint32_t)stage * a_bytes, &xmap, bar, c0, w0,
+                                        h0, d0, n0, 0, (uint16_t)tr, (uint16_t)tt);
+              else
+                tma_load_2d_pair(sA_u32 + (uint32_t)stage * a_bytes, &xmap, bar, c0,
+                                 xrow0 + (tt * p.Hg + tr) * p.Wg);
               const int k_tap0 = ((tt * p.R + tr) * p.S) * p.C + c0;
               const uint32_t b_dst = sB_u32 + (uint32_t)stage * b_bytes;
               for (int ss = 0; ss < p.S; ++ss)

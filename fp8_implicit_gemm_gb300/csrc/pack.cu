@@ -17,7 +17,9 @@ namespace c3d {
 // Work of the pack kernel, as consecutive index ranges of one grid-stride loop:
 //   [0, x_items)          interior of x: with W % 4 == 0, one item = 16 channels x 4 pixels (16
 //                         aligned 4-byte loads, a byte transpose in registers, four 16-byte
-//                         stores); otherwise one item = 16 channels x 1 pixel (16 byte loads)
+//                         stores); otherwise one item = 16 channels x 1 pixel (16 byte loads);
+//                         from a channels-last x, one item = one 16-byte chunk copied into the
+//                         padded copy (no items when the TMA routes read that x directly)
 //   + halo_row_items      16-byte zero chunks of the padded rows (d or h in the halo)
 //   + halo_side_items     16-byte zero chunks of the W-halo pixels of interior rows
 //   + w_items             16 channels of one tap of one filter
@@ -26,13 +28,15 @@ namespace c3d {
 struct PackPlan {
   long long x_items, halo_row_items, halo_side_items, w_items;
   bool quad;  // W % 4 == 0: 4-pixel items
+  bool copy;  // x is channels-last already: 16-byte chunk copies
 };
 
 __host__ __device__ inline PackPlan pack_plan(const ConvParams& p) {
   PackPlan q;
   const long long cq = p.C / 16;
-  q.quad = (p.W % 4) == 0;
-  q.x_items = (long long)p.N * p.D * p.H * cq * (q.quad ? p.W / 4 : p.W);
+  q.copy = p.x_cl != 0;
+  q.quad = !q.copy && (p.W % 4) == 0;
+  q.x_items = p.xp == nullptr ? 0 : (long long)p.N * p.D * p.H * cq * (q.quad ? p.W / 4 : p.W);
   const long long halo_rows_per_image = (long long)p.Dp * p.Hp - (long long)p.D * p.H;
   q.halo_row_items = (long long)p.N * halo_rows_per_image * p.Wp * cq;
   q.halo_side_items = (long long)p.N * p.D * p.H * (p.Wp - p.W) * cq;
@@ -58,7 +62,20 @@ __global__ void __launch_bounds__(256) pack_kernel(ConvParams p, PackPlan q) {
   const long long plane = (long long)p.D * p.H * p.W;
   for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < total;
        g += (long long)gridDim.x * blockDim.x) {
-    if (g < e1) {
+    if (g < e1 && q.copy) {
+      // interior from a channels-last x: (chunk fastest, then pixel)
+      const long long pix = g / cq_n;  // ((n*D + d)*H + h)*W + w
+      const int cq = (int)(g - pix * cq_n);
+      const int w = (int)(pix % p.W);
+      const long long row = pix / p.W;
+      const int h = (int)(row % p.H);
+      const int d = (int)((row / p.H) % p.D);
+      const int n = (int)(row / ((long long)p.H * p.D));
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.x + pix * p.C + cq * 16));
+      *reinterpret_cast<uint4*>(
+          p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) * p.Wp + w + p.pk_pw) *
+                     p.C + cq * 16) = v;
+    } else if (g < e1) {
       // interior: (pixel or quad fastest, then channel chunk, then (n, d, h) row)
       const int per_row = q.quad ? p.W / 4 : p.W;
       const int wi = (int)(g % per_row);

@@ -61,11 +61,18 @@ typedef struct {
                             channels-last copy of x; 2: A by TMA im2col loads (EUNSUPPORTED
                             unless C % 32 == 0, strides <= 8 and -16 <= -pad, pad - (filter-1)
                             <= 15 on every axis); 3: padded-grid route, stride 1 and CTA pairs
-                            only: M runs over the zero-padded output grid and one TMA tile of
-                            128 + S - 1 rows feeds the S taps along W (EUNSUPPORTED unless every
-                            stride is 1 and C % 32 == 0) */
+                            only: M runs over the zero-padded grid of the input and one TMA
+                            im2col load of 128 + S - 1 grid positions feeds the S taps along W
+                            (EUNSUPPORTED unless every stride is 1, C % 32 == 0, S <= 129 and
+                            every pad <= 15) */
     int cta_pair;        /* 0: the library chooses; 1: one CTA per 128-row tile; 2: CTA pairs on
                             256-row tiles (tcgen05 cta_group::2; not on the gather route) */
+    int input_layout;    /* 0: x is NCDHW (the library transposes it to channels-last every
+                            run); 1: x is NDHWC, channels-last, the layout the TMA im2col unit
+                            reads: the im2col and padded-grid routes then read the caller's x
+                            directly and the run packs only the weights (the gather route still
+                            copies x into a zero-padded buffer). With 1 the padded-grid route
+                            also needs every pad <= 15. y stays NCDHW either way. */
 } conv3d_fp8_options;
 
 /* What a plan (or a would-be plan) decided. */
@@ -112,7 +119,9 @@ conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t *plan, int N, int C, int D, i
 
 /*
  * Run the planned convolution, asynchronously on `stream`.
- *   x_ncdhw: N*C*D*H*W e4m3 bytes, contiguous, 16-byte aligned.
+ *   x_ncdhw: N*C*D*H*W e4m3 bytes, contiguous, 16-byte aligned; NDHWC (channels-last) instead
+ *            when the plan was made with input_layout = 1 (the A tensor map then points at x:
+ *            it is re-encoded on the host whenever x differs from the previous run's).
  *   w_kctrs: K*C*T*R*S e4m3 bytes, contiguous, 16-byte aligned.
  *   scale_x, scale_w: device pointers to one fp32 each (read on the device, so a run can be
  *                     captured in a CUDA graph and the scales may change between replays).

@@ -29,7 +29,10 @@ class GpuConv:
         self.plan = capi.conv3d_fp8_plan(s.N, s.C, s.D, s.H, s.W, s.K, s.T, s.R, s.S, s.stride,
                                          s.pad, torch.cuda.current_device(), **options)
         self.info = capi.conv3d_fp8_get_info(self.plan)
-        self.x = inp["x"].cuda()
+        x = inp["x"]
+        if options.get("input_layout") == 1:  # the same bytes, channels-last
+            x = x.permute(0, 2, 3, 4, 1).contiguous()
+        self.x = x.cuda()
         self.w = inp["w"].cuda()
         self.sx = torch.tensor([inp["sx"]], dtype=torch.float32, device="cuda")
         self.sw = torch.tensor([inp["sw"]], dtype=torch.float32, device="cuda")

@@ -95,7 +95,7 @@ def test_describe_routes(lib):
     big_pad = synth.ConvShape(1, 32, 4, 4, 4, 16, pad=17)       # corner beyond [-16, 15]
     assert _describe(big_pad, cta_pair=1)["route"] == 1          # im2col impossible -> gather
     assert _describe(big_pad)["route"] == 3                      # the padded grid takes any pad
-    # the gather and grid routes' packed copy carries the zero halo, the im2col one does not
+    # the gather and padded-grid routes' packed copy carries the zero halo, the im2col one not
     s = synth.CONFIGS[2]
     ws = {r: _describe(s, route=r, splits=1)["workspace_bytes"] for r in (1, 2, 3)}
     assert ws[1] > ws[2] and ws[3] == ws[1]
@@ -131,6 +131,28 @@ def test_describe_tail_split(lib):
     assert _describe(synth.CONFIGS[4], splits=1)["full_tiles"] == 990
     i = _describe(synth.CONFIGS[4], splits=3)
     assert i["full_tiles"] == 0 and i["splits"] == 3
+
+
+def test_describe_channels_last_input(lib):
+    # the TMA routes read the caller's NDHWC x: no copy of x in the workspace; the gather route
+    # still keeps its zero-padded copy
+    for cfg in (2, 4):
+        s = synth.CONFIGS[cfg]
+        for r in (2, 3):
+            a = _describe(s, route=r, splits=1)
+            b = _describe(s, route=r, splits=1, input_layout=1)
+            assert a["workspace_bytes"] - b["workspace_bytes"] >= s.N * s.C * s.D * s.H * s.W
+        g = _describe(s, route=1, splits=1, cta_pair=1)
+        assert _describe(s, route=1, splits=1, cta_pair=1, input_layout=1)["workspace_bytes"] == \
+            g["workspace_bytes"]
+    # reading a channels-last x, the padded-grid route walks an im2col box: pads up to 15 only
+    assert _describe(synth.ConvShape(1, 32, 4, 4, 4, 16, pad=16), input_layout=1)["route"] == 2
+    assert _describe(synth.ConvShape(1, 32, 4, 4, 4, 16, pad=17), input_layout=1)["route"] == 1
+    assert capi.conv3d_fp8_describe_status(1, 32, 4, 4, 4, 16, 3, 3, 3, 1, 16, 152, route=3,
+                                           input_layout=1) == capi.CONV3D_EUNSUPPORTED
+    assert _describe(synth.ConvShape(1, 32, 4, 4, 4, 16, pad=16))["route"] == 3
+    assert capi.conv3d_fp8_describe_status(1, 32, 4, 4, 4, 16, 3, 3, 3, 1, 1, 152,
+                                           input_layout=2) == capi.CONV3D_EINVAL
 
 
 def test_describe_forced_options(lib):

@@ -148,6 +148,48 @@ def test_tail_tiles_split_along_k(kernel):
     assert 0 < info["full_tiles"] < tiles and info["splits"] > 1, info
 
 
+# Channels-last input (input_layout = 1): the TMA routes read the caller's NDHWC x directly (the
+# padded-grid route through an im2col traversal of its zero-padded grid), the gather route copies
+# it into its zero-padded buffer.
+@pytest.mark.parametrize("kernel", list(KERNELS))
+@pytest.mark.parametrize("cfg", [0, 1, 3])
+def test_channels_last_input_full_output(cfg, kernel):
+    if kernel == "grid-pair" and cfg == 3:
+        pytest.skip("the padded-grid route needs stride 1")
+    res, info = _full_case(synth.CONFIGS[cfg], synth.config_seed(cfg), input_layout=1,
+                           **KERNELS[kernel])
+    assert info["route"] == KERNELS[kernel]["route"]
+
+
+@pytest.mark.parametrize("cfg", [2, 4])
+def test_channels_last_input_sampled_outputs(cfg):
+    shape = synth.CONFIGS[cfg]
+    inp = synth.make_config_inputs(cfg)
+    g = GpuConv(shape, inp, input_layout=1)
+    try:
+        y = g.run()
+        assert not torch.isnan(y).any().item(), "some outputs never written"
+        idx = sample_indices(g.out_shape, 60000, seed=50 + cfg)
+        y64, yb = oracle.conv3d_fp8_points(inp["x"].numpy(), inp["w"].numpy(), inp["sx"],
+                                           inp["sw"], idx, shape.stride, shape.pad)
+        print(cfg, check_against(bits(y).ravel()[idx], y64, yb, shape.name))
+    finally:
+        g.close()
+
+
+@pytest.mark.parametrize("i", range(len(ODD)))
+def test_channels_last_input_odd_shapes(i):
+    res, info = _full_case(ODD[i], 77 + i, input_layout=1)
+    print(ODD[i], res, info["route"])
+
+
+@pytest.mark.parametrize("i", [i for i, s in enumerate(ODD)
+                               if s.C % 32 == 0 and s.stride == (1, 1, 1)])
+def test_channels_last_input_odd_shapes_grid_route(i):
+    res, info = _full_case(ODD[i], 77 + i, input_layout=1, route=3)
+    assert info["route"] == 3
+
+
 def test_split_k_is_reproducible_and_close_across_split_counts():
     shape = synth.CONFIGS[3]
     inp = synth.make_config_inputs(3)
