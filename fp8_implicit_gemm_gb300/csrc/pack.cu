@@ -209,8 +209,17 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(ConvParams p) {
     const RowDest dst = row_dest(p, m_tile, row);
     if (kRowChk && !dst.valid) continue;
     const float* src = p.partials + ((t * p.splits) * p.block_n + col_l) * p.block_m + row;
+    // eight loads in flight at a time; the additions stay in ascending split order
     float acc = 0.0f;
-    for (int s = 0; s < p.splits; ++s) acc += __ldcg(src + (long long)s * per_tile);
+    int s = 0;
+    for (; s + 8 <= p.splits; s += 8) {
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + (long long)(s + j) * per_tile);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc += v[j];
+    }
+    for (; s < p.splits; ++s) acc += __ldcg(src + (long long)s * per_tile);
     const __nv_bfloat16 b = __float2bfloat16_rn(acc * scale);
     p.y[dst.y_off + (long long)col * p.dhw] = *reinterpret_cast<const uint16_t*>(&b);
   }

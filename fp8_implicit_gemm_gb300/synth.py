@@ -105,3 +105,26 @@ def make_inputs(shape: ConvShape, seed: int) -> dict:
 
 def make_config_inputs(index: int) -> dict:
     return make_inputs(CONFIGS[index], config_seed(index))
+
+
+def make_inputs_bf16(shape: ConvShape, seed: int) -> dict:
+    """Seeded inputs of the BF16-input twin on the CPU: dict(x=bfloat16 NCDHW, w=bfloat16 KCTRS),
+    x ~ N(0, 1) and w ~ N(0, 1/(C*T*R*S)) drawn in fp32 (x first) and rounded to bfloat16."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    x = torch.randn((shape.N, shape.C, shape.D, shape.H, shape.W), generator=g,
+                    dtype=torch.float32).to(torch.bfloat16)
+    taps = shape.C * shape.T * shape.R * shape.S
+    w = (torch.randn((shape.K, shape.C, shape.T, shape.R, shape.S), generator=g,
+                     dtype=torch.float32) * (1.0 / taps) ** 0.5).to(torch.bfloat16)
+    return {"x": x.contiguous(), "w": w.contiguous()}
+
+
+def make_config_inputs_bf16(index: int) -> dict:
+    return make_inputs_bf16(CONFIGS[index], config_seed(index))
+
+
+def bf16_bits(t: torch.Tensor):
+    """The bit patterns of a bfloat16 CPU tensor as a numpy uint16 array."""
+    import numpy as np
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)

@@ -1,4 +1,4 @@
-"""CPU oracle for the FP8 (e4m3) 3D convolution with a BF16 NCDHW output.
+"""CPU oracle for the FP8 (e4m3) 3D convolution with a BF16 NCDHW output, and its BF16-input twin.
 
 TEST INFRASTRUCTURE. Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
 ``--impl reference`` legs of ``bench.py`` may import this package. It imports nothing from the
@@ -72,6 +72,13 @@ def _load() -> ctypes.CDLL:
             lib.o_conv3d_fp8_points.restype = ci
             lib.o_conv3d_fp8_points.argtypes = ([u8p, u8p, ctypes.c_float, ctypes.c_float] + shape
                                                 + [i64p, ctypes.c_longlong, dp, dp, u16p])
+            lib.o_bf16_decode.restype = ctypes.c_double
+            lib.o_bf16_decode.argtypes = [ctypes.c_ushort]
+            lib.o_conv3d_bf16.restype = ci
+            lib.o_conv3d_bf16.argtypes = [u16p, u16p] + shape + [dp, u16p]
+            lib.o_conv3d_bf16_points.restype = ci
+            lib.o_conv3d_bf16_points.argtypes = ([u16p, u16p] + shape
+                                                 + [i64p, ctypes.c_longlong, dp, u16p])
             _lib = lib
     return _lib
 
@@ -111,6 +118,14 @@ def bf16_rne(v) -> np.ndarray:
     return out.reshape(v.shape)
 
 
+def bf16_decode(bits) -> np.ndarray:
+    """Exact fp64 value of each bfloat16 bit pattern, decoded from the format definition."""
+    lib = _load()
+    bits = np.asarray(bits, dtype=np.uint16)
+    out = np.array([lib.o_bf16_decode(int(v)) for v in bits.ravel()], dtype=np.float64)
+    return out.reshape(bits.shape)
+
+
 def bf16_bits_to_f64(bits) -> np.ndarray:
     """Value of bfloat16 bit patterns (shift into the top half of an fp32)."""
     bits = np.asarray(bits, dtype=np.uint16)
@@ -137,7 +152,7 @@ def _check(rc: int):
     if rc == -1:
         raise ValueError("oracle: invalid shape, stride or padding")
     if rc == -2:
-        raise ValueError("oracle: e4m3 NaN byte (0x7F/0xFF) in an input")
+        raise ValueError("oracle: NaN (or, for bfloat16, infinite) value in an input")
     if rc == -3:
         raise IndexError("oracle: output index out of range")
     if rc != 0:
@@ -190,3 +205,46 @@ def conv3d_fp8_points(x: np.ndarray, w: np.ndarray, sx: float, sw: float, idx, s
                                  _ptr(yb, ctypes.c_ushort))
     _check(rc)
     return (ysum, y64, yb) if want_sum else (y64, yb)
+
+
+def _u16(a) -> np.ndarray:
+    """bfloat16 bit patterns as a contiguous uint16 array (accepts uint16/int16 arrays)."""
+    a = np.asarray(a)
+    if a.dtype == np.int16:
+        a = a.view(np.uint16)
+    return np.ascontiguousarray(a, dtype=np.uint16)
+
+
+def conv3d_bf16(x, w, stride=1, pad=1):
+    """Full convolution of the BF16-input twin. x: uint16 [N,C,D,H,W] bfloat16 bit patterns;
+    w: uint16 [K,C,T,R,S]. No scales. Returns (y64, ybf16), each [N,K,Do,Ho,Wo]."""
+    lib = _load()
+    x, w = _u16(x), _u16(w)
+    args = _shape_args(x, w, stride, pad)
+    N, _, D, H, W_, K, T, R, S, sd, sh, sww, pd, ph, pw = args
+    Do, Ho, Wo = out_dims(D, H, W_, T, R, S, (sd, sh, sww), (pd, ph, pw))
+    if min(Do, Ho, Wo) <= 0:
+        raise ValueError("oracle: empty output")
+    shape = (N, K, Do, Ho, Wo)
+    y64 = np.empty(shape, np.float64)
+    yb = np.empty(shape, np.uint16)
+    rc = lib.o_conv3d_bf16(_ptr(x, ctypes.c_ushort), _ptr(w, ctypes.c_ushort), *args,
+                           _ptr(y64, ctypes.c_double), _ptr(yb, ctypes.c_ushort))
+    _check(rc)
+    return y64, yb
+
+
+def conv3d_bf16_points(x, w, idx, stride=1, pad=1):
+    """Selected outputs of the BF16-input twin (flat NCDHW indices). Returns (y64, ybf16)."""
+    lib = _load()
+    x, w = _u16(x), _u16(w)
+    idx = np.ascontiguousarray(idx, dtype=np.int64)
+    args = _shape_args(x, w, stride, pad)
+    n = idx.size
+    y64 = np.empty(n, np.float64)
+    yb = np.empty(n, np.uint16)
+    rc = lib.o_conv3d_bf16_points(_ptr(x, ctypes.c_ushort), _ptr(w, ctypes.c_ushort), *args,
+                                  _ptr(idx, ctypes.c_longlong), n, _ptr(y64, ctypes.c_double),
+                                  _ptr(yb, ctypes.c_ushort))
+    _check(rc)
+    return y64, yb

@@ -30,6 +30,13 @@
  * The only rounding before the final BF16 rounding is the one fp64 multiply by sx*sw (the fp32 x
  * fp32 product itself is exact in fp64).
  *
+ * The BF16-input twin (the same page, "Notes": the BF16 implicit-GEMM conv3d kernel that
+ * already guards its padded rows) computes the same sum with X and Wt bfloat16 values and no
+ * scales: y64 = S, ybf16 = round-to-nearest-even of S. Its products are exact in fp64 (two 8-bit
+ * significands); the fp64 sum in the loop order below differs from the exact sum by at most
+ * (n - 1) * 2^-53 * sum|terms| (recursive summation, n terms), far below one BF16 ulp for the
+ * workloads here.
+ *
  * Build: gcc -O2 -fopenmp -shared -fPIC (OpenMP optional; without it the loops run serially).
  */
 #include <math.h>
@@ -56,6 +63,25 @@ double o_e4m3_decode(unsigned char b)
         mag = ldexp((double)m, -9);
     else
         mag = ldexp((double)(8 + m), e - 10);
+    return sign ? -mag : mag;
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * bfloat16: 1 sign bit, 8 exponent bits with bias 127, 7 mantissa bits. Exponent field 0 is
+ * subnormal: m * 2^-133; field 255 is infinity (m == 0) or NaN. Normal: (128 + m) * 2^(e-134).
+ * ------------------------------------------------------------------------------------------- */
+double o_bf16_decode(unsigned short b)
+{
+    int sign = (b >> 15) & 1;
+    int e = (b >> 7) & 0xFF;
+    int m = b & 0x7F;
+    double mag;
+    if (e == 0xFF)
+        return m ? NAN : (sign ? -INFINITY : INFINITY);
+    if (e == 0)
+        mag = ldexp((double)m, -133);
+    else
+        mag = ldexp((double)(128 + m), e - 134);
     return sign ? -mag : mag;
 }
 
@@ -266,6 +292,125 @@ int o_conv3d_fp8_points(const unsigned char *x, const unsigned char *w, float sx
         double v = scale * sum;
         if (ysum)
             ysum[j] = sum;
+        if (y64)
+            y64[j] = v;
+        if (ybf16)
+            ybf16[j] = o_bf16_rne(v);
+    }
+    return 0;
+}
+
+/* ============================================================================================
+ * BF16-input twin: x and w are bfloat16 bit patterns, no scales.
+ * ========================================================================================== */
+
+/* The sum S for one output element, straight from the definition (bfloat16 inputs). */
+static double o_point_sum_bf16(const o_shape *p, const unsigned short *x, const unsigned short *w,
+                               int n, int k, int od, int oh, int ow)
+{
+    double acc = 0.0;
+    int c, t, r, s;
+    for (c = 0; c < p->C; ++c) {
+        for (t = 0; t < p->T; ++t) {
+            int id = od * p->sd + t - p->pd;
+            if (id < 0 || id >= p->D)
+                continue;
+            for (r = 0; r < p->R; ++r) {
+                int ih = oh * p->sh + r - p->ph;
+                if (ih < 0 || ih >= p->H)
+                    continue;
+                for (s = 0; s < p->S; ++s) {
+                    int iw = ow * p->sw + s - p->pw;
+                    size_t xi, wi;
+                    if (iw < 0 || iw >= p->W)
+                        continue;
+                    xi = ((((size_t)n * p->C + c) * p->D + id) * p->H + ih) * p->W + iw;
+                    wi = ((((size_t)k * p->C + c) * p->T + t) * p->R + r) * p->S + s;
+                    acc += o_bf16_decode(x[xi]) * o_bf16_decode(w[wi]);
+                }
+            }
+        }
+    }
+    return acc;
+}
+
+static int o_check_bf16(const unsigned short *b, size_t n)
+{
+    size_t i;
+    for (i = 0; i < n; ++i)
+        if ((b[i] & 0x7F80) == 0x7F80)
+            return -2; /* infinity or NaN: not a valid input for the oracle */
+    return 0;
+}
+
+/*
+ * Full output of the BF16 twin. x: N*C*D*H*W bfloat16 (NCDHW), w: K*C*T*R*S bfloat16 (KCTRS).
+ * Outputs (each may be NULL): y64 = fp64 sums, ybf16 = their BF16 rounding, N*K*Do*Ho*Wo NCDHW.
+ * Returns 0, -1 on a bad shape, -2 on an infinite or NaN input.
+ */
+int o_conv3d_bf16(const unsigned short *x, const unsigned short *w,
+                  int N, int C, int D, int H, int W, int K, int T, int R, int S,
+                  int sd, int sh, int sww, int pd, int ph, int pw,
+                  double *y64, unsigned short *ybf16)
+{
+    o_shape p;
+    long long nk;
+
+    if (o_make_shape(&p, N, C, D, H, W, K, T, R, S, sd, sh, sww, pd, ph, pw) != 0)
+        return -1;
+    if (o_check_bf16(x, (size_t)N * C * D * H * W) != 0 ||
+        o_check_bf16(w, (size_t)K * C * T * R * S) != 0)
+        return -2;
+    nk = (long long)N * K;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long long job = 0; job < nk; ++job) {
+        int n = (int)(job / K), k = (int)(job % K);
+        int od, oh, ow;
+        for (od = 0; od < p.Do; ++od)
+            for (oh = 0; oh < p.Ho; ++oh)
+                for (ow = 0; ow < p.Wo; ++ow) {
+                    size_t yi = ((((size_t)n * K + k) * p.Do + od) * p.Ho + oh) * p.Wo + ow;
+                    double v = o_point_sum_bf16(&p, x, w, n, k, od, oh, ow);
+                    if (y64)
+                        y64[yi] = v;
+                    if (ybf16)
+                        ybf16[yi] = o_bf16_rne(v);
+                }
+    }
+    return 0;
+}
+
+/* Selected outputs of the BF16 twin; idx[i] is a flat NCDHW output index. -3: index out of range. */
+int o_conv3d_bf16_points(const unsigned short *x, const unsigned short *w,
+                         int N, int C, int D, int H, int W, int K, int T, int R, int S,
+                         int sd, int sh, int sww, int pd, int ph, int pw,
+                         const long long *idx, long long npts,
+                         double *y64, unsigned short *ybf16)
+{
+    o_shape p;
+    long long total;
+    int bad = 0;
+
+    if (o_make_shape(&p, N, C, D, H, W, K, T, R, S, sd, sh, sww, pd, ph, pw) != 0)
+        return -1;
+    if (o_check_bf16(x, (size_t)N * C * D * H * W) != 0 ||
+        o_check_bf16(w, (size_t)K * C * T * R * S) != 0)
+        return -2;
+    total = (long long)N * K * p.Do * p.Ho * p.Wo;
+    for (long long j = 0; j < npts; ++j)
+        if (idx[j] < 0 || idx[j] >= total)
+            bad = 1;
+    if (bad)
+        return -3;
+#pragma omp parallel for schedule(dynamic, 64)
+    for (long long j = 0; j < npts; ++j) {
+        long long f = idx[j];
+        int ow = (int)(f % p.Wo);
+        int oh = (int)((f / p.Wo) % p.Ho);
+        int od = (int)((f / ((long long)p.Wo * p.Ho)) % p.Do);
+        int k = (int)((f / ((long long)p.Wo * p.Ho * p.Do)) % K);
+        int n = (int)(f / ((long long)p.Wo * p.Ho * p.Do * K));
+        double v = o_point_sum_bf16(&p, x, w, n, k, od, oh, ow);
         if (y64)
             y64[j] = v;
         if (ybf16)
