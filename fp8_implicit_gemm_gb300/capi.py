@@ -85,6 +85,16 @@ def load() -> ctypes.CDLL:
             lib.conv3d_fp8_describe.restype = ci
             lib.conv3d_fp8_describe.argtypes = ([ci] * 9 + [i3, i3, ci, ctypes.POINTER(Options),
                                                             ctypes.POINTER(PlanInfo)])
+            lib.conv3d_bf16_plan.restype = ci
+            lib.conv3d_bf16_plan.argtypes = [ctypes.POINTER(vp)] + [ci] * 9 + [i3, i3, ci]
+            lib.conv3d_bf16_plan_ex.restype = ci
+            lib.conv3d_bf16_plan_ex.argtypes = ([ctypes.POINTER(vp)] + [ci] * 9 + [i3, i3, ci]
+                                                + [ctypes.POINTER(Options)])
+            lib.conv3d_bf16_run.restype = ci
+            lib.conv3d_bf16_run.argtypes = [vp, vp, vp, vp, i3, i3, vp]
+            lib.conv3d_bf16_describe.restype = ci
+            lib.conv3d_bf16_describe.argtypes = ([ci] * 9 + [i3, i3, ci, ctypes.POINTER(Options),
+                                                             ctypes.POINTER(PlanInfo)])
             lib.conv3d_fp8_workspace_size.restype = ctypes.c_size_t
             lib.conv3d_fp8_workspace_size.argtypes = [vp]
             lib.conv3d_fp8_out_dims.restype = ci
@@ -249,3 +259,48 @@ def conv3d_fp8_out_dims(plan) -> tuple[int, int, int]:
 def conv3d_fp8_destroy(plan) -> None:
     if plan:
         load().conv3d_fp8_destroy(plan)
+
+
+# ------------------------------------------------------------------------- BF16-input twin
+def conv3d_bf16_plan(N, C, D, H, W, K, T, R, S, stride, pad, device=0, **options) -> int:
+    """Create a plan of the BF16-input twin (same options as conv3d_fp8_plan)."""
+    lib = load()
+    h = ctypes.c_void_p()
+    o = _options(**options)
+    if o is None:
+        st = lib.conv3d_bf16_plan(ctypes.byref(h), N, C, D, H, W, K, T, R, S, _int3(stride),
+                                  _int3(pad), device)
+    else:
+        st = lib.conv3d_bf16_plan_ex(ctypes.byref(h), N, C, D, H, W, K, T, R, S, _int3(stride),
+                                     _int3(pad), device, ctypes.byref(o))
+    _raise(st, "conv3d_bf16_plan")
+    return h.value
+
+
+def conv3d_bf16_run_status(plan, x, w, y, stride, pad, stream=None) -> int:
+    return load().conv3d_bf16_run(plan, _ptr(x), _ptr(w), _ptr(y), _int3(stride), _int3(pad),
+                                  _stream(stream))
+
+
+def conv3d_bf16_run(plan, x, w, y, stride, pad, stream=None) -> None:
+    _raise(conv3d_bf16_run_status(plan, x, w, y, stride, pad, stream), "conv3d_bf16_run")
+
+
+def conv3d_bf16_describe_status(N, C, D, H, W, K, T, R, S, stride, pad, sm_count,
+                                **options) -> int:
+    info = PlanInfo()
+    o = _options(**options)
+    return load().conv3d_bf16_describe(N, C, D, H, W, K, T, R, S, _int3(stride), _int3(pad),
+                                       sm_count, ctypes.byref(o) if o is not None else None,
+                                       ctypes.byref(info))
+
+
+def conv3d_bf16_describe(N, C, D, H, W, K, T, R, S, stride, pad, sm_count, **options) -> dict:
+    """Host-only planning decision of the BF16-input twin (no device access)."""
+    info = PlanInfo()
+    o = _options(**options)
+    st = load().conv3d_bf16_describe(N, C, D, H, W, K, T, R, S, _int3(stride), _int3(pad),
+                                     sm_count, ctypes.byref(o) if o is not None else None,
+                                     ctypes.byref(info))
+    _raise(st, "conv3d_bf16_describe")
+    return info.as_dict()

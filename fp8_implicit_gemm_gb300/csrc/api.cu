@@ -21,6 +21,8 @@ struct conv3d_fp8_plan_s {
   CUtensorMap wmap{};
   CUtensorMap xmap{};  // A tensor map (TMA routes)
   const void* xmap_src = nullptr;  // caller's x the A map was last encoded for (channels-last x)
+  int elem_bytes = 1;              // 1: e4m3 plan (conv3d_fp8_*), 2: bfloat16 plan (conv3d_bf16_*)
+  const float* ones = nullptr;     // device fp32 {1, 1}: the scales of a bfloat16 plan's runs
   conv3d_fp8_plan_info info{};
   void* workspace = nullptr;
   cudaEvent_t ev_begin = nullptr;  // measurement hook, caller-owned
@@ -57,7 +59,7 @@ struct Layout {
 
 // Validation and every tiling decision, with no device access. `pair_slots` > 0 caps the number
 // of CTA pairs that can be resident at once (the device's cluster occupancy), when known.
-conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int S,
+conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, int T, int R, int S,
                      const int stride[3], const int pad[3], int sm_count,
                      const conv3d_fp8_options* opts, conv3d_fp8_plan_info* info, ConvParams* pp,
                      Layout* lay, int pair_slots = 0) {
@@ -71,6 +73,12 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   const int Ho = out_dim(H, R, stride[1], pad[1]);
   const int Wo = out_dim(W, S, stride[2], pad[2]);
   if (Do <= 0 || Ho <= 0 || Wo <= 0) return CONV3D_EINVAL;
+  if (elem_bytes != 1 && elem_bytes != 2) return CONV3D_EINVAL;
+  if (C >= (1 << 28)) return CONV3D_EUNSUPPORTED;
+  // From here on C counts the BYTES of one pixel's channels: every tile, stage, descriptor and
+  // tensor map below is laid out in bytes, the same for e4m3 and bfloat16 inputs.
+  const int C_el = C;
+  C *= elem_bytes;
   if (C % 16 != 0) return CONV3D_EUNSUPPORTED;
 
   const long long dhw = (long long)Do * Ho * Wo;
@@ -211,7 +219,7 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
   info->Ho = Ho;
   info->Wo = Wo;
   info->npq = npq;
-  info->k_gemm = (int)kg;
+  info->k_gemm = (int)(taps * C_el);
   info->block_m = block_m;
   info->block_n = block_n;
   info->m_tiles = (int)m_tiles;
@@ -232,6 +240,7 @@ conv3d_status decide(int N, int C, int D, int H, int W, int K, int T, int R, int
     ConvParams& p = *pp;
     std::memset(&p, 0, sizeof(p));
     p.N = N; p.C = C; p.D = D; p.H = H; p.W = W; p.K = K; p.T = T; p.R = R; p.S = S;
+    p.elem_bytes = elem_bytes;
     p.sd = stride[0]; p.sh = stride[1]; p.sw = stride[2];
     p.pd = pad[0]; p.ph = pad[1]; p.pw = pad[2];
     p.Do = Do; p.Ho = Ho; p.Wo = Wo;
@@ -416,17 +425,23 @@ extern "C" {
 conv3d_status conv3d_fp8_describe(int N, int C, int D, int H, int W, int K, int T, int R, int S,
                                   const int stride[3], const int pad[3], int sm_count,
                                   const conv3d_fp8_options* opts, conv3d_fp8_plan_info* info) {
-  return decide(N, C, D, H, W, K, T, R, S, stride, pad, sm_count, opts, info, nullptr, nullptr);
+  return decide(1, N, C, D, H, W, K, T, R, S, stride, pad, sm_count, opts, info, nullptr, nullptr);
 }
 
-conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t* out, int N, int C, int D, int H, int W, int K,
-                                 int T, int R, int S, const int stride[3], const int pad[3],
-                                 int device, const conv3d_fp8_options* opts) {
+}  // extern "C"
+
+namespace {
+
+// Plans of both input types: e4m3 (elem_bytes 1) and bfloat16 (elem_bytes 2).
+conv3d_status plan_impl(int elem_bytes, conv3d_fp8_plan_t* out, int N, int C, int D, int H, int W,
+                        int K, int T, int R, int S, const int stride[3], const int pad[3],
+                        int device, const conv3d_fp8_options* opts) {
   if (!out) return CONV3D_EINVAL;
   *out = nullptr;
   // Shape errors first, without touching any device.
   conv3d_fp8_plan_info probe{};
-  conv3d_status st = decide(N, C, D, H, W, K, T, R, S, stride, pad, 1, opts, &probe, nullptr, nullptr);
+  conv3d_status st = decide(elem_bytes, N, C, D, H, W, K, T, R, S, stride, pad, 1, opts, &probe,
+                            nullptr, nullptr);
   if (st != CONV3D_OK) return st;
 
   int ndev = 0;
@@ -444,8 +459,8 @@ conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t* out, int N, int C, int D, in
   conv3d_fp8_plan_s* plan = new (std::nothrow) conv3d_fp8_plan_s();
   if (!plan) return CONV3D_ENOMEM;
   Layout L{};
-  st = decide(N, C, D, H, W, K, T, R, S, stride, pad, prop.multiProcessorCount, opts, &plan->info,
-              &plan->p, &L);
+  st = decide(elem_bytes, N, C, D, H, W, K, T, R, S, stride, pad, prop.multiProcessorCount, opts,
+              &plan->info, &plan->p, &L);
   if (st != CONV3D_OK) {
     delete plan;
     return st;
@@ -453,8 +468,8 @@ conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t* out, int N, int C, int D, in
   if (plan->p.pair) {  // plan for the CTA pairs the device can actually hold at once
     const int clusters = conv_pair_max_active_clusters(plan->p);
     if (clusters > 0 && clusters < prop.multiProcessorCount / 2) {
-      st = decide(N, C, D, H, W, K, T, R, S, stride, pad, prop.multiProcessorCount, opts,
-                  &plan->info, &plan->p, &L, clusters);
+      st = decide(elem_bytes, N, C, D, H, W, K, T, R, S, stride, pad, prop.multiProcessorCount,
+                  opts, &plan->info, &plan->p, &L, clusters);
       if (st != CONV3D_OK) {
         delete plan;
         return st;
@@ -488,11 +503,18 @@ conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t* out, int N, int C, int D, in
   plan->p.wp = ws + L.wp_off;
   plan->p.partials = L.part_bytes ? reinterpret_cast<float*>(ws + L.part_off) : nullptr;
   plan->p.status = reinterpret_cast<int*>(ws + L.status_off);
-  if (cudaMemset(plan->p.status, 0, 256) != cudaSuccess) {
+  // The status word at offset 0 of its 256-byte slot; a bfloat16 plan keeps two fp32 ones at
+  // offset 128, the scales its runs pass to the kernels (its inputs carry no scale).
+  const float ones[2] = {1.0f, 1.0f};
+  if (cudaMemset(plan->p.status, 0, 256) != cudaSuccess ||
+      (elem_bytes == 2 && cudaMemcpy(ws + L.status_off + 128, ones, sizeof ones,
+                                     cudaMemcpyHostToDevice) != cudaSuccess)) {
     cudaFree(plan->workspace);
     delete plan;
     return CONV3D_ECUDA;
   }
+  plan->elem_bytes = elem_bytes;
+  plan->ones = reinterpret_cast<const float*>(ws + L.status_off + 128);
   if (plan->p.pair) {  // never more clusters than can be resident at once
     const int clusters = conv_pair_max_active_clusters(plan->p);
     if (clusters > 0 && plan->info.grid > 2 * clusters) plan->info.grid = 2 * clusters;
@@ -507,15 +529,10 @@ conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t* out, int N, int C, int D, in
   return CONV3D_OK;
 }
 
-conv3d_status conv3d_fp8_plan(conv3d_fp8_plan_t* out, int N, int C, int D, int H, int W, int K,
-                              int T, int R, int S, const int stride[3], const int pad[3],
-                              int device) {
-  return conv3d_fp8_plan_ex(out, N, C, D, H, W, K, T, R, S, stride, pad, device, nullptr);
-}
-
-conv3d_status conv3d_fp8_run(conv3d_fp8_plan_t plan, const void* x, const void* w,
-                             const float* scale_x, const float* scale_w, void* y,
-                             const int stride[3], const int pad[3], void* stream) {
+// Runs of both input types; the bfloat16 entry passes the plan's fp32 ones as the scales.
+conv3d_status run_impl(conv3d_fp8_plan_t plan, const void* x, const void* w,
+                       const float* scale_x, const float* scale_w, void* y,
+                       const int stride[3], const int pad[3], void* stream) {
   if (!plan || !x || !w || !scale_x || !scale_w || !y || !stride || !pad) return CONV3D_EINVAL;
   if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(scale_x, 4) ||
       !aligned(scale_w, 4))
@@ -547,6 +564,53 @@ conv3d_status conv3d_fp8_run(conv3d_fp8_plan_t plan, const void* x, const void* 
     return CONV3D_ECUDA;
   if (plan->ev_end && cudaEventRecord(plan->ev_end, s) != cudaSuccess) return CONV3D_ECUDA;
   return CONV3D_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t* out, int N, int C, int D, int H, int W, int K,
+                                 int T, int R, int S, const int stride[3], const int pad[3],
+                                 int device, const conv3d_fp8_options* opts) {
+  return plan_impl(1, out, N, C, D, H, W, K, T, R, S, stride, pad, device, opts);
+}
+
+conv3d_status conv3d_fp8_plan(conv3d_fp8_plan_t* out, int N, int C, int D, int H, int W, int K,
+                              int T, int R, int S, const int stride[3], const int pad[3],
+                              int device) {
+  return plan_impl(1, out, N, C, D, H, W, K, T, R, S, stride, pad, device, nullptr);
+}
+
+conv3d_status conv3d_fp8_run(conv3d_fp8_plan_t plan, const void* x, const void* w,
+                             const float* scale_x, const float* scale_w, void* y,
+                             const int stride[3], const int pad[3], void* stream) {
+  if (plan && plan->elem_bytes != 1) return CONV3D_EINVAL;
+  return run_impl(plan, x, w, scale_x, scale_w, y, stride, pad, stream);
+}
+
+conv3d_status conv3d_bf16_plan_ex(conv3d_fp8_plan_t* out, int N, int C, int D, int H, int W, int K,
+                                  int T, int R, int S, const int stride[3], const int pad[3],
+                                  int device, const conv3d_fp8_options* opts) {
+  return plan_impl(2, out, N, C, D, H, W, K, T, R, S, stride, pad, device, opts);
+}
+
+conv3d_status conv3d_bf16_plan(conv3d_fp8_plan_t* out, int N, int C, int D, int H, int W, int K,
+                               int T, int R, int S, const int stride[3], const int pad[3],
+                               int device) {
+  return plan_impl(2, out, N, C, D, H, W, K, T, R, S, stride, pad, device, nullptr);
+}
+
+conv3d_status conv3d_bf16_run(conv3d_fp8_plan_t plan, const void* x, const void* w, void* y,
+                              const int stride[3], const int pad[3], void* stream) {
+  if (!plan || plan->elem_bytes != 2) return CONV3D_EINVAL;
+  return run_impl(plan, x, w, plan->ones, plan->ones + 1, y, stride, pad, stream);
+}
+
+conv3d_status conv3d_bf16_describe(int N, int C, int D, int H, int W, int K, int T, int R, int S,
+                                   const int stride[3], const int pad[3], int sm_count,
+                                   const conv3d_fp8_options* opts, conv3d_fp8_plan_info* info) {
+  return decide(2, N, C, D, H, W, K, T, R, S, stride, pad, sm_count, opts, info, nullptr, nullptr);
 }
 
 conv3d_status conv3d_fp8_set_timing_events(conv3d_fp8_plan_t plan, void* ev_begin, void* ev_end) {
@@ -681,7 +745,7 @@ extern "C" conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int 
   // Shape errors first, without touching the device.
   conv3d_fp8_plan_info info{};
   conv3d_status st =
-      decide(N, C, D, H, W, K, T, R, S, stride, pad, 1, nullptr, &info, nullptr, nullptr);
+      decide(1, N, C, D, H, W, K, T, R, S, stride, pad, 1, nullptr, &info, nullptr, nullptr);
   if (st != CONV3D_OK) return st;
 
   int dev = -1, major = 0, minor = 0, sms = 0;
@@ -698,12 +762,13 @@ extern "C" conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int 
 
   ConvParams p{};
   Layout L{};
-  st = decide(N, C, D, H, W, K, T, R, S, stride, pad, sms, nullptr, &info, &p, &L);
+  st = decide(1, N, C, D, H, W, K, T, R, S, stride, pad, sms, nullptr, &info, &p, &L);
   if (st != CONV3D_OK) return st;
   if (p.pair) {  // plan for the CTA pairs the device can actually hold at once
     const int clusters = conv_pair_max_active_clusters(p);
     if (clusters > 0 && clusters < sms / 2) {
-      st = decide(N, C, D, H, W, K, T, R, S, stride, pad, sms, nullptr, &info, &p, &L, clusters);
+      st = decide(1, N, C, D, H, W, K, T, R, S, stride, pad, sms, nullptr, &info, &p, &L,
+                  clusters);
       if (st != CONV3D_OK) return st;
     }
   }

@@ -35,7 +35,8 @@ enum : int {
 
 struct ConvParams {
   // problem
-  int N, C, D, H, W, K, T, R, S;
+  int N, C, D, H, W, K, T, R, S;  // C: bytes of one pixel's channels (channels * elem_bytes)
+  int elem_bytes;        // 1: e4m3 inputs (kind::f8f6f4); 2: bfloat16 inputs (kind::f16)
   int sd, sh, sw, pd, ph, pw;
   int Do, Ho, Wo;
   int route;             // kRouteGather or kRouteIm2col (how A reaches shared memory)

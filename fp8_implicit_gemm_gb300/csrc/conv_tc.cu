@@ -4,7 +4,8 @@
 // GEMM view (the subject page, "Root cause"): row = output position (npq = N*Do*Ho*Wo rows),
 // col = output channel (K columns), reduction over K_gemm = (tap, channel) of T*R*S*C.
 //
-// One persistent CTA per SM walks a static list of work units (m-tile, n-tile, K-split). Warp roles:
+// One persistent CTA per SM walks a static list of work units (m-tile, n-tile, K-split).
+// Warp roles:
 //   warps 0-3  epilogue: TMEM -> registers, scale, bf16, stores masked on row < npq and col < K
 //              (warp w owns TMEM lanes 32w..32w+31, i.e. rows 32w..32w+31 of the tile)
 //   warp 8     TMA loader: per stage one 2D tile of the packed weights (B) and, on the im2col
@@ -14,7 +15,9 @@
 //   warps 4-7  gather route only (C % 32 != 0 or paddings beyond the im2col corner range): A by
 //              16-byte cp.async gathers from the zero-padded channels-last input into the
 //              128-byte-swizzled stage; rows at or past npq are zero-filled
-//   warp 9     MMA issuer: 4 x tcgen05.mma (M=128, N=block_n, K=32) per 128-byte K block
+//   warp 9     MMA issuer: 4 x tcgen05.mma (M=128, N=block_n, K=32 bytes) per 128-byte K block;
+//              kind::f8f6f4 on e4m3 bytes, or kind::f16 on bfloat16 pairs (kBf16): the tiles,
+//              stages and descriptors are the same in bytes
 // Stages are handed over with mbarriers: TMA-full (transaction bytes of A and/or B), A-full (128
 // gather arrivals, gather route), stage-empty (tcgen05.commit). Two TMEM accumulators let the
 // epilogue of one tile overlap the main loop of the next. Every wait is bounded; a wait that runs
@@ -27,7 +30,7 @@ namespace c3d {
 
 constexpr int kLoaderLag = 2;  // cp.async groups kept in flight before a stage is signalled full
 
-template <bool kRowChk>
+template <bool kRowChk, bool kBf16>
 __global__ void __launch_bounds__(kNumThreads, 1)
     conv3d_fp8_tc_kernel(const __grid_constant__ CUtensorMap wmap,
                          const __grid_constant__ CUtensorMap xmap, const ConvParams p) {
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   } else {
     // ------------------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = make_idesc_e4m3_f32(kBlockM, (uint32_t)p.block_n);
+      const uint32_t idesc = make_idesc<kBf16>(kBlockM, (uint32_t)p.block_n);
       // A rows are 128 bytes (SW128) on the gather route, a_cb bytes on the im2col route. K step
       // j covers bytes [32j, 32j+32) of the 128-byte K block: in A it lies in sub-tile 32j / a_cb
       // at byte 32j % a_cb of each row, in B at byte 32j of each 128-byte row. Everything that
@@ -263,16 +266,16 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const uint32_t acc0 = kb > un.kb0 ? 1u : 0u;
           const int rem = p.kg - kb * kBlockK;
           if (rem >= kBlockK) {
-            mma_f8f6f4(d_tmem, adesc + a_step[0], bdesc, idesc, acc0);
-            mma_f8f6f4(d_tmem, adesc + a_step[1], bdesc + 2u, idesc, 1u);
-            mma_f8f6f4(d_tmem, adesc + a_step[2], bdesc + 4u, idesc, 1u);
-            mma_f8f6f4(d_tmem, adesc + a_step[3], bdesc + 6u, idesc, 1u);
+            mma_cta<kBf16>(d_tmem, adesc + a_step[0], bdesc, idesc, acc0);
+            mma_cta<kBf16>(d_tmem, adesc + a_step[1], bdesc + 2u, idesc, 1u);
+            mma_cta<kBf16>(d_tmem, adesc + a_step[2], bdesc + 4u, idesc, 1u);
+            mma_cta<kBf16>(d_tmem, adesc + a_step[3], bdesc + 6u, idesc, 1u);
           } else {
             const int nsteps = (rem + kMmaK - 1) / kMmaK;
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               if (j < nsteps)
-                mma_f8f6f4(d_tmem, adesc + a_step[j], bdesc + 2u * j, idesc, j > 0 ? 1u : acc0);
+                mma_cta<kBf16>(d_tmem, adesc + a_step[j], bdesc + 2u * j, idesc, j > 0 ? 1u : acc0);
           }
           mma_commit(empty(stage));
           ring.next(S);
@@ -299,11 +302,15 @@ size_t conv_smem_bytes(int block_n, int stages) {
 }
 
 cudaError_t conv_set_smem_attr(size_t smem_bytes) {
-  cudaError_t e = cudaFuncSetAttribute(conv3d_fp8_tc_kernel<true>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(conv3d_fp8_tc_kernel<false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_bytes);
+  const int v = (int)smem_bytes;
+  cudaError_t e = cudaSuccess;
+  const void* kernels[] = {(const void*)conv3d_fp8_tc_kernel<true, false>,
+                           (const void*)conv3d_fp8_tc_kernel<false, false>,
+                           (const void*)conv3d_fp8_tc_kernel<true, true>,
+                           (const void*)conv3d_fp8_tc_kernel<false, true>};
+  for (const void* k : kernels)
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, v);
   if (e == cudaSuccess) e = conv_pair_set_smem_attr(smem_bytes);
   return e;
 }
@@ -312,10 +319,15 @@ cudaError_t launch_conv(const ConvParams& p, const CUtensorMap& wmap, const CUte
                         bool row_chk, int grid, cudaStream_t stream) {
   if (p.pair) return launch_conv_pair(p, wmap, xmap, row_chk, grid, stream);
   const size_t smem = conv_smem_bytes(p.block_n, p.stages);
-  if (row_chk)
-    conv3d_fp8_tc_kernel<true><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
+  const bool bf16 = p.elem_bytes == 2;
+  if (row_chk && bf16)
+    conv3d_fp8_tc_kernel<true, true><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
+  else if (row_chk)
+    conv3d_fp8_tc_kernel<true, false><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
+  else if (bf16)
+    conv3d_fp8_tc_kernel<false, true><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
   else
-    conv3d_fp8_tc_kernel<false><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
+    conv3d_fp8_tc_kernel<false, false><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
   return cudaGetLastError();
 }
 

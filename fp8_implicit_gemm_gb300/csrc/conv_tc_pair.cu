@@ -23,9 +23,12 @@
 // the shared-memory address, so the shifted start reads the rows TMA wrote there), plus the S
 // matching B tiles. The load is a 2D tile of a zero-padded channels-last copy when the library
 // packs x itself, or an im2col load whose traversal covers the padded grid of the caller's
-// unpadded channels-last x (zeros outside the volume) when x comes channels-last. That cuts the bytes each SM's TMA unit must bring in per MMA by about a third, which is
-// what bounds the output-position route. Rows of the grid that are not outputs (h >= Ho, w >= Wo,
-// d >= Do) are computed and never stored.
+// unpadded channels-last x (zeros outside the volume) when x comes channels-last. That cuts the
+// bytes each SM's TMA unit must bring in per MMA by about a third, which is what bounds the
+// output-position route. Rows of the grid that are not outputs (h >= Ho, w >= Wo, d >= Do) are
+// computed and never stored.
+// kBf16: bfloat16 inputs (tcgen05.mma kind::f16, K = 16 elements) instead of e4m3 (kind::f8f6f4,
+// K = 32 elements); every tile, stage and descriptor is the same in bytes.
 // Every wait is bounded; a wait that runs out records a status bit and both CTAs wind down.
 #include <cuda_runtime.h>
 
@@ -49,7 +52,7 @@ __host__ __device__ inline void pair_stage_bytes(const ConvParams& p, bool grid,
   }
 }
 
-template <bool kRowChk, bool kGrid>
+template <bool kRowChk, bool kGrid, bool kBf16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     conv3d_fp8_tc_pair_kernel(const __grid_constant__ CUtensorMap wmap,
                               const __grid_constant__ CUtensorMap xmap, const ConvParams p) {
@@ -235,7 +238,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
-      const uint32_t idesc = make_idesc_e4m3_f32(2 * kBlockM, (uint32_t)p.block_n);
+      const uint32_t idesc = make_idesc<kBf16>(2 * kBlockM, (uint32_t)p.block_n);
       const uint32_t a_cb = (uint32_t)p.a_cb;
       const uint32_t a_layout =
           a_cb == 128 ? kLayoutSw128 : (a_cb == 64 ? kLayoutSw64 : kLayoutSw32);
@@ -280,15 +283,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             uint32_t acc = acc0;
             for (int ss = 0; ss < p.S; ++ss) {
               if (steps_cb == 4) {
-                mma_f8f6f4_pair(d_tmem, a_tap, b_tap, idesc, acc);
-                mma_f8f6f4_pair(d_tmem, a_tap + 2u, b_tap + 2u, idesc, 1u);
-                mma_f8f6f4_pair(d_tmem, a_tap + 4u, b_tap + 4u, idesc, 1u);
-                mma_f8f6f4_pair(d_tmem, a_tap + 6u, b_tap + 6u, idesc, 1u);
+                mma_pair<kBf16>(d_tmem, a_tap, b_tap, idesc, acc);
+                mma_pair<kBf16>(d_tmem, a_tap + 2u, b_tap + 2u, idesc, 1u);
+                mma_pair<kBf16>(d_tmem, a_tap + 4u, b_tap + 4u, idesc, 1u);
+                mma_pair<kBf16>(d_tmem, a_tap + 6u, b_tap + 6u, idesc, 1u);
               } else if (steps_cb == 2) {
-                mma_f8f6f4_pair(d_tmem, a_tap, b_tap, idesc, acc);
-                mma_f8f6f4_pair(d_tmem, a_tap + 2u, b_tap + 2u, idesc, 1u);
+                mma_pair<kBf16>(d_tmem, a_tap, b_tap, idesc, acc);
+                mma_pair<kBf16>(d_tmem, a_tap + 2u, b_tap + 2u, idesc, 1u);
               } else {
-                mma_f8f6f4_pair(d_tmem, a_tap, b_tap, idesc, acc);
+                mma_pair<kBf16>(d_tmem, a_tap, b_tap, idesc, acc);
               }
               acc = 1u;
               a_tap += a_row16;
@@ -298,16 +301,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
             const uint64_t bdesc = bdesc0 + (uint64_t)((uint32_t)stage * b_stage16);
             const int rem = p.kg - kb * kBlockK;
             if (rem >= kBlockK) {
-              mma_f8f6f4_pair(d_tmem, adesc + a_step[0], bdesc, idesc, acc0);
-              mma_f8f6f4_pair(d_tmem, adesc + a_step[1], bdesc + 2u, idesc, 1u);
-              mma_f8f6f4_pair(d_tmem, adesc + a_step[2], bdesc + 4u, idesc, 1u);
-              mma_f8f6f4_pair(d_tmem, adesc + a_step[3], bdesc + 6u, idesc, 1u);
+              mma_pair<kBf16>(d_tmem, adesc + a_step[0], bdesc, idesc, acc0);
+              mma_pair<kBf16>(d_tmem, adesc + a_step[1], bdesc + 2u, idesc, 1u);
+              mma_pair<kBf16>(d_tmem, adesc + a_step[2], bdesc + 4u, idesc, 1u);
+              mma_pair<kBf16>(d_tmem, adesc + a_step[3], bdesc + 6u, idesc, 1u);
             } else {
               const int nsteps = (rem + kMmaK - 1) / kMmaK;
 #pragma unroll
               for (int j = 0; j < 4; ++j)
                 if (j < nsteps)
-                  mma_f8f6f4_pair(d_tmem, adesc + a_step[j], bdesc + 2u * j, idesc,
+                  mma_pair<kBf16>(d_tmem, adesc + a_step[j], bdesc + 2u * j, idesc,
                                   j > 0 ? 1u : acc0);
             }
           }
@@ -340,26 +343,38 @@ size_t conv_pair_smem_bytes(const ConvParams& p) {
 
 cudaError_t conv_pair_set_smem_attr(size_t smem_bytes) {
   const int v = (int)smem_bytes;
-  cudaError_t e = cudaFuncSetAttribute(conv3d_fp8_tc_pair_kernel<true, false>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, v);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(conv3d_fp8_tc_pair_kernel<false, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, v);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(conv3d_fp8_tc_pair_kernel<true, true>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, v);
+  cudaError_t e = cudaSuccess;
+  const void* kernels[] = {(const void*)conv3d_fp8_tc_pair_kernel<true, false, false>,
+                           (const void*)conv3d_fp8_tc_pair_kernel<false, false, false>,
+                           (const void*)conv3d_fp8_tc_pair_kernel<true, true, false>,
+                           (const void*)conv3d_fp8_tc_pair_kernel<true, false, true>,
+                           (const void*)conv3d_fp8_tc_pair_kernel<false, false, true>,
+                           (const void*)conv3d_fp8_tc_pair_kernel<true, true, true>};
+  for (const void* k : kernels)
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, v);
   return e;
+}
+
+template <bool kBf16>
+void launch_pair_typed(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
+                       bool row_chk, int grid, size_t smem, cudaStream_t stream) {
+  const dim3 g(grid), b(kNumThreads);
+  if (p.route == kRouteGrid)  // grid rows that are not outputs always need the row test
+    conv3d_fp8_tc_pair_kernel<true, true, kBf16><<<g, b, smem, stream>>>(wmap, xmap, p);
+  else if (row_chk)
+    conv3d_fp8_tc_pair_kernel<true, false, kBf16><<<g, b, smem, stream>>>(wmap, xmap, p);
+  else
+    conv3d_fp8_tc_pair_kernel<false, false, kBf16><<<g, b, smem, stream>>>(wmap, xmap, p);
 }
 
 cudaError_t launch_conv_pair(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
                              bool row_chk, int grid, cudaStream_t stream) {
   const size_t smem = conv_pair_smem_bytes(p);
-  if (p.route == kRouteGrid)  // grid rows that are not outputs always need the row test
-    conv3d_fp8_tc_pair_kernel<true, true><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
-  else if (row_chk)
-    conv3d_fp8_tc_pair_kernel<true, false><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
+  if (p.elem_bytes == 2)
+    launch_pair_typed<true>(p, wmap, xmap, row_chk, grid, smem, stream);
   else
-    conv3d_fp8_tc_pair_kernel<false, false><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
+    launch_pair_typed<false>(p, wmap, xmap, row_chk, grid, smem, stream);
   return cudaGetLastError();
 }
 
@@ -376,7 +391,7 @@ int conv_pair_max_active_clusters(const ConvParams& p) {
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, conv3d_fp8_tc_pair_kernel<true, false>, &cfg) !=
+  if (cudaOccupancyMaxActiveClusters(&n, conv3d_fp8_tc_pair_kernel<true, false, false>, &cfg) !=
       cudaSuccess) {
     cudaGetLastError();
     return 0;

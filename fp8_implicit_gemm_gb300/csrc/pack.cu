@@ -27,7 +27,8 @@ namespace c3d {
 // along W of the NCDHW input.
 struct PackPlan {
   long long x_items, halo_row_items, halo_side_items, w_items;
-  bool quad;  // W % 4 == 0: 4-pixel items
+  bool quad;  // e4m3 and W % 4 == 0: 4-pixel items
+  bool two;   // bfloat16 and W % 2 == 0: 2-pixel items
   bool copy;  // x is channels-last already: 16-byte chunk copies
 };
 
@@ -35,8 +36,10 @@ __host__ __device__ inline PackPlan pack_plan(const ConvParams& p) {
   PackPlan q;
   const long long cq = p.C / 16;
   q.copy = p.x_cl != 0;
-  q.quad = !q.copy && (p.W % 4) == 0;
-  q.x_items = p.xp == nullptr ? 0 : (long long)p.N * p.D * p.H * cq * (q.quad ? p.W / 4 : p.W);
+  q.quad = !q.copy && p.elem_bytes == 1 && (p.W % 4) == 0;
+  q.two = !q.copy && p.elem_bytes == 2 && (p.W % 2) == 0;
+  const int per_row = q.quad ? p.W / 4 : (q.two ? p.W / 2 : p.W);
+  q.x_items = p.xp == nullptr ? 0 : (long long)p.N * p.D * p.H * cq * per_row;
   const long long halo_rows_per_image = (long long)p.Dp * p.Hp - (long long)p.D * p.H;
   q.halo_row_items = (long long)p.N * halo_rows_per_image * p.Wp * cq;
   q.halo_side_items = (long long)p.N * p.D * p.H * (p.Wp - p.W) * cq;
@@ -75,6 +78,45 @@ __global__ void __launch_bounds__(256) pack_kernel(ConvParams p, PackPlan q) {
       *reinterpret_cast<uint4*>(
           p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) * p.Wp + w + p.pk_pw) *
                      p.C + cq * 16) = v;
+    } else if (g < e1 && p.elem_bytes == 2) {
+      // interior, bfloat16: one item = 8 channels (one 16-byte chunk) x 2 pixels (or 1 when W is
+      // odd); pixels fastest, then chunk, then (n, d, h) row
+      const int per_row = q.two ? p.W / 2 : p.W;
+      const int wi = (int)(g % per_row);
+      const long long rest = g / per_row;
+      const int cq = (int)(rest % cq_n);
+      const long long row = rest / cq_n;  // n*D*H + d*H + h
+      const int h = (int)(row % p.H);
+      const int d = (int)((row / p.H) % p.D);
+      const int n = (int)(row / ((long long)p.H * p.D));
+      const int c_el = p.C >> 1;
+      const uint16_t* src = reinterpret_cast<const uint16_t*>(p.x) +
+                            ((long long)n * c_el + cq * 8) * plane + ((long long)d * p.H + h) * p.W;
+      uint8_t* dst_row = p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) *
+                                     p.Wp + p.pk_pw) * p.C + cq * 16;
+      if (q.two) {
+        uint32_t v[8];  // v[c]: pixels 2wi (low half) and 2wi+1 (high half) of channel c
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          v[j] = __ldg(reinterpret_cast<const uint32_t*>(src + j * plane) + wi);
+        uint32_t lo[4], hi[4];  // channel pairs (2k, 2k+1) of pixel 2wi and of pixel 2wi+1
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          lo[k] = __byte_perm(v[2 * k], v[2 * k + 1], 0x5410);
+          hi[k] = __byte_perm(v[2 * k], v[2 * k + 1], 0x7632);
+        }
+        *reinterpret_cast<uint4*>(dst_row + (long long)(2 * wi) * p.C) =
+            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(dst_row + (long long)(2 * wi + 1) * p.C) =
+            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      } else {
+        uint32_t v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          v[k] = (uint32_t)__ldg(src + (2 * k) * plane + wi) |
+                 ((uint32_t)__ldg(src + (2 * k + 1) * plane + wi) << 16);
+        *reinterpret_cast<uint4*>(dst_row + (long long)wi * p.C) = make_uint4(v[0], v[1], v[2], v[3]);
+      }
     } else if (g < e1) {
       // interior: (pixel or quad fastest, then channel chunk, then (n, d, h) row)
       const int per_row = q.quad ? p.W / 4 : p.W;
@@ -157,15 +199,24 @@ __global__ void __launch_bounds__(256) pack_kernel(ConvParams p, PackPlan q) {
           p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) * p.Wp + wp) * p.C +
           cq * 16) = make_uint4(0u, 0u, 0u, 0u);
     } else {
+      // weights: one item = one 16-byte chunk (16 e4m3 or 8 bfloat16 channels) of one tap
       const long long gw = g - e3;
       const int tap = (int)(gw % p.taps);
       const long long rest = gw / p.taps;
       const int cq = (int)(rest % cq_n);
       const int k = (int)(rest / cq_n);
-      const uint8_t* src = p.w + ((long long)k * p.C + cq * 16) * p.taps + tap;
       uint32_t v[4] = {0u, 0u, 0u, 0u};
+      if (p.elem_bytes == 2) {
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(p.w) +
+                              ((long long)k * (p.C >> 1) + cq * 8) * p.taps + tap;
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j >> 2] |= (uint32_t)__ldg(src + j * p.taps) << ((j & 3) * 8);
+        for (int j = 0; j < 8; ++j) v[j >> 1] |= (uint32_t)__ldg(src + j * p.taps) << ((j & 1) * 16);
+      } else {
+        const uint8_t* src = p.w + ((long long)k * p.C + cq * 16) * p.taps + tap;
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          v[j >> 2] |= (uint32_t)__ldg(src + j * p.taps) << ((j & 3) * 8);
+      }
       uint4* dst =
           reinterpret_cast<uint4*>(p.wp + ((long long)k * p.taps + tap) * p.C + cq * 16);
       *dst = make_uint4(v[0], v[1], v[2], v[3]);

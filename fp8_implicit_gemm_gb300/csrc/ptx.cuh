@@ -239,6 +239,27 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uin
       : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 x bf16 -> fp32, one CTA (K = 16 elements = 32 bytes).
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// The CTA-pair form of mma_bf16 (M = 256 over the pair, as mma_f8f6f4_pair).
+__device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -289,6 +310,35 @@ __device__ __forceinline__ uint64_t make_sw128_kmajor_desc(uint32_t smem_addr) {
 // M >> 4 at bits 24-28.
 __host__ __device__ constexpr uint32_t make_idesc_e4m3_f32(uint32_t m, uint32_t n) {
   return (1u << 4) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16 with bfloat16 A and B: D fp32 (bits 4-5 = 1),
+// A and B bf16 (bits 7-9 and 10-12 = 1), both K-major, N >> 3 at bits 17-22, M >> 4 at 24-28.
+__host__ __device__ constexpr uint32_t make_idesc_bf16_f32(uint32_t m, uint32_t n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
+}
+
+// One MMA of the element type the kernel was compiled for: e4m3 (kind::f8f6f4) or bf16
+// (kind::f16). Both consume 32 bytes of K per row of A and B.
+template <bool kBf16>
+__device__ __forceinline__ uint32_t make_idesc(uint32_t m, uint32_t n) {
+  return kBf16 ? make_idesc_bf16_f32(m, n) : make_idesc_e4m3_f32(m, n);
+}
+template <bool kBf16>
+__device__ __forceinline__ void mma_cta(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  if constexpr (kBf16)
+    mma_bf16(d_tmem, a_desc, b_desc, idesc, accumulate);
+  else
+    mma_f8f6f4(d_tmem, a_desc, b_desc, idesc, accumulate);
+}
+template <bool kBf16>
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+  if constexpr (kBf16)
+    mma_bf16_pair(d_tmem, a_desc, b_desc, idesc, accumulate);
+  else
+    mma_f8f6f4_pair(d_tmem, a_desc, b_desc, idesc, accumulate);
 }
 
 }  // namespace c3d

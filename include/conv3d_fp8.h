@@ -198,6 +198,34 @@ void conv3d_fp8_destroy(conv3d_fp8_plan_t plan);
 /* Static description of a status code. */
 const char *conv3d_fp8_strerror(conv3d_status status);
 
+/*
+ * BF16-input twin ("Notes" of the subject page: the BF16 implicit-GEMM conv3d kernel, which guards
+ * its padded rows the same way). The same convolution with bfloat16 x and w and no scales:
+ *   y = bf16(sum over c, t, r, s of x * w), fp32 accumulation on the tensor cores
+ *   (tcgen05.mma kind::f16), BF16 NCDHW output with the same row and column guards, the same
+ *   routes, tiles (in bytes), split-K path and scheduler as the e4m3 path.
+ * Plans are conv3d_fp8_plan_t values: conv3d_fp8_destroy, _check, _get_info, _out_dims,
+ * _workspace_size and _set_timing_events apply to them too; conv3d_fp8_run rejects a bfloat16
+ * plan and conv3d_bf16_run an e4m3 one (EINVAL). C must be a multiple of 8 (16 bytes); the im2col
+ * and padded-grid routes need C % 16 == 0. k_gemm in the plan info counts elements.
+ *   x_ncdhw: N*C*D*H*W bfloat16, contiguous, 16-byte aligned (NDHWC with input_layout = 1).
+ *   w_kctrs: K*C*T*R*S bfloat16, contiguous, 16-byte aligned.
+ *   y_ncdhw: N*K*Do*Ho*Wo bfloat16, as for conv3d_fp8_run.
+ * Errors as for the e4m3 calls.
+ */
+conv3d_status conv3d_bf16_plan(conv3d_fp8_plan_t *plan, int N, int C, int D, int H, int W, int K,
+                               int T, int R, int S, const int stride[3], const int pad[3],
+                               int device);
+conv3d_status conv3d_bf16_plan_ex(conv3d_fp8_plan_t *plan, int N, int C, int D, int H, int W,
+                                  int K, int T, int R, int S, const int stride[3],
+                                  const int pad[3], int device, const conv3d_fp8_options *opts);
+conv3d_status conv3d_bf16_run(conv3d_fp8_plan_t plan, const void *x_ncdhw, const void *w_kctrs,
+                              void *y_ncdhw, const int stride[3], const int pad[3], void *stream);
+/* Host-only planning of the BF16 twin, as conv3d_fp8_describe. */
+conv3d_status conv3d_bf16_describe(int N, int C, int D, int H, int W, int K, int T, int R, int S,
+                                   const int stride[3], const int pad[3], int sm_count,
+                                   const conv3d_fp8_options *opts, conv3d_fp8_plan_info *info);
+
 #ifdef __cplusplus
 }
 #endif

@@ -155,6 +155,27 @@ def test_describe_channels_last_input(lib):
                                            input_layout=2) == capi.CONV3D_EINVAL
 
 
+def test_describe_bf16_twin(lib):
+    d = lambda s, **kw: capi.conv3d_bf16_describe(s.N, s.C, s.D, s.H, s.W, s.K, s.T, s.R, s.S,
+                                                  s.stride, s.pad, 152, **kw)
+    for cfg, s in enumerate(synth.CONFIGS):
+        a, b = _describe(s), d(s)
+        assert b["k_gemm"] == a["k_gemm"] == s.C * s.T * s.R * s.S   # elements
+        assert b["route"] == a["route"] and b["cta_pair"] == a["cta_pair"]
+        # K blocks are 128 bytes of K_gemm (or, on the padded-grid route, one channel block of a
+        # (t, r) pair): the same bytes hold half as many bfloat16 channels
+        if b["route"] == 3:
+            assert b["k_blocks"] == s.T * s.R * (2 * s.C) // min(128, 2 * s.C)
+        else:
+            assert b["k_blocks"] == -(-2 * b["k_gemm"] // 128)
+    # C in 16-byte units: 8 bfloat16 channels suffice (gather route), 4 do not
+    assert d(synth.ConvShape(1, 8, 4, 4, 4, 16))["route"] == 1
+    assert capi.conv3d_bf16_describe_status(1, 4, 4, 4, 4, 16, 3, 3, 3, 1, 1,
+                                            152) == capi.CONV3D_EUNSUPPORTED
+    # 16 channels = 32 bytes: the TMA routes apply
+    assert d(synth.ConvShape(1, 16, 4, 8, 8, 16))["route"] in (2, 3)
+
+
 def test_describe_forced_options(lib):
     s = synth.CONFIGS[1]
     i = _describe(s, splits=4, block_n=64, max_ctas=10, cta_pair=1)
