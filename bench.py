@@ -39,6 +39,10 @@ if ROOT not in sys.path:
 DEFAULT_CONFIG = 4
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+METRIC = "conv3d fp8 TFLOP/s and % of FP8/HBM roofline at 1 GB300"
+METRIC_BF16 = "conv3d BF16-input twin TFLOP/s and % of BF16/HBM roofline at 1 GB300"
+DATA = "synthetic (seeded N(0,1) inputs quantised to e4m3 per tensor)"
+DATA_BF16 = "synthetic (seeded N(0,1) inputs rounded to bfloat16)"
 MAIN_KERNEL_SOURCES = ["conv_tc.cu", "conv_tc_pair.cu", "conv_common.cuh", "ptx.cuh",
                        "conv3d_fp8_internal.h"]
 
@@ -48,15 +52,15 @@ def log(*a):
 
 
 # ----------------------------------------------------------------------------------- problem math
-def problem_figures(shape):
+def problem_figures(shape, elem_bytes: int = 1):
     Do = (shape.D + 2 * shape.pad[0] - shape.T) // shape.stride[0] + 1
     Ho = (shape.H + 2 * shape.pad[1] - shape.R) // shape.stride[1] + 1
     Wo = (shape.W + 2 * shape.pad[2] - shape.S) // shape.stride[2] + 1
     npq = shape.N * Do * Ho * Wo
     kg = shape.C * shape.T * shape.R * shape.S
     flop = 2.0 * npq * shape.K * kg
-    x_bytes = shape.N * shape.C * shape.D * shape.H * shape.W
-    w_bytes = shape.K * kg
+    x_bytes = elem_bytes * shape.N * shape.C * shape.D * shape.H * shape.W
+    w_bytes = elem_bytes * shape.K * kg
     y_bytes = 2 * npq * shape.K
     return {"Do": Do, "Ho": Ho, "Wo": Wo, "npq": npq, "k_gemm": kg, "flop": flop,
             "x_bytes": x_bytes, "w_bytes": w_bytes, "y_bytes": y_bytes,
@@ -223,20 +227,33 @@ class Dist:
 
 
 # ------------------------------------------------------------------------------- CPU baseline
-def cpu_oracle_sample(inp, shape, target_s: float, seed: int, min_points: int = 256):
+def oracle_points_fn(inp, shape, bf16: bool):
+    """The oracle's sampled-points call on this input set (e4m3 with scales, or the BF16 twin)."""
+    import oracle
+    from fp8_implicit_gemm_gb300 import synth
+    if bf16:
+        x, w = synth.bf16_bits(inp["x"]), synth.bf16_bits(inp["w"])
+        return lambda idx: oracle.conv3d_bf16_points(x, w, idx, shape.stride, shape.pad)
+    x, w = inp["x"].numpy(), inp["w"].numpy()
+    return lambda idx: oracle.conv3d_fp8_points(x, w, inp["sx"], inp["sw"], idx, shape.stride,
+                                                shape.pad)
+
+
+def cpu_oracle_sample(inp, shape, target_s: float, seed: int, min_points: int = 256,
+                      bf16: bool = False):
     """Time the oracle on a random sample of outputs sized to about target_s seconds."""
     import numpy as np
     import oracle
     fig = problem_figures(shape)
     total = shape.K * fig["npq"]
-    x, w = inp["x"].numpy(), inp["w"].numpy()
+    points = oracle_points_fn(inp, shape, bf16)
     rng = np.random.default_rng(seed)
     n = min_points
     t = 0.0
     while True:
         idx = rng.integers(0, total, n)
         t0 = time.perf_counter()
-        oracle.conv3d_fp8_points(x, w, inp["sx"], inp["sw"], idx, shape.stride, shape.pad)
+        points(idx)
         t = time.perf_counter() - t0
         if t >= target_s * 0.5 or n >= total:
             break
@@ -258,21 +275,22 @@ def run_ours(args):
     dev = torch.cuda.current_device()
     build.build()
     shape = synth.CONFIGS[args.config]
-    fig = problem_figures(shape)
-    inp = synth.make_config_inputs(args.config)
+    bf16 = args.dtype == "bf16"  # the BF16-input twin instead of the e4m3 path
+    fig = problem_figures(shape, 2 if bf16 else 1)
+    inp = synth.make_config_inputs_bf16(args.config) if bf16 else synth.make_config_inputs(args.config)
     channels_last = args.input_layout == "ndhwc"
     # the library's x: the same bytes, laid out NDHWC when asked (the oracle keeps NCDHW)
     x_lib = inp["x"].permute(0, 2, 3, 4, 1).contiguous() if channels_last else inp["x"]
 
-    plan = capi.conv3d_fp8_plan(shape.N, shape.C, shape.D, shape.H, shape.W, shape.K, shape.T,
-                                shape.R, shape.S, shape.stride, shape.pad, dev,
-                                input_layout=1 if channels_last else 0)
+    make_plan = capi.conv3d_bf16_plan if bf16 else capi.conv3d_fp8_plan
+    plan = make_plan(shape.N, shape.C, shape.D, shape.H, shape.W, shape.K, shape.T, shape.R,
+                     shape.S, shape.stride, shape.pad, dev, input_layout=1 if channels_last else 0)
     info = capi.conv3d_fp8_get_info(plan)
     stream = torch.cuda.current_stream()
     x = x_lib.to(dev)
     w = inp["w"].to(dev)
-    sx = torch.tensor([inp["sx"]], dtype=torch.float32, device=dev)
-    sw = torch.tensor([inp["sw"]], dtype=torch.float32, device=dev)
+    sx = torch.tensor([inp.get("sx", 1.0)], dtype=torch.float32, device=dev)
+    sw = torch.tensor([inp.get("sw", 1.0)], dtype=torch.float32, device=dev)
     y = torch.full((shape.N, shape.K, fig["Do"], fig["Ho"], fig["Wo"]), float("nan"),
                    dtype=torch.bfloat16, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -280,8 +298,14 @@ def run_ours(args):
     # pack, main kernel, and the reduction when some tiles are split along K
     launches_per_step = 2 + (1 if info["full_tiles"] < info["m_tiles"] * info["n_tiles"] else 0)
 
+    def run(scale_x, scale_w):
+        if bf16:
+            capi.conv3d_bf16_run(plan, x, w, y, shape.stride, shape.pad, stream)
+        else:
+            capi.conv3d_fp8_run(plan, x, w, scale_x, scale_w, y, shape.stride, shape.pad, stream)
+
     def step():
-        capi.conv3d_fp8_run(plan, x, w, sx, sw, y, shape.stride, shape.pad, stream)
+        run(sx, sw)
 
     for _ in range(args.warmup):
         flush.fill_(1)
@@ -330,7 +354,8 @@ def run_ours(args):
     # ---- end to end through the public C-ABI call with host buffers
     x_h = x_lib.pin_memory()
     w_h = inp["w"].pin_memory()
-    s_h = torch.tensor([inp["sx"], inp["sw"]], dtype=torch.float32).pin_memory()
+    # host scales of the e4m3 path (the BF16 twin has none)
+    s_h = torch.tensor([inp["sx"], inp["sw"]] if not bf16 else [], dtype=torch.float32).pin_memory()
     s_d = torch.empty(2, dtype=torch.float32, device=dev)
     y_h = torch.empty(y.shape, dtype=torch.bfloat16).pin_memory()
     e2e_steps = max(3, min(K, 200))
@@ -344,8 +369,9 @@ def run_ours(args):
     for i in range(e2e_steps):
         x.copy_(x_h, non_blocking=True)
         w.copy_(w_h, non_blocking=True)
-        s_d.copy_(s_h, non_blocking=True)
-        capi.conv3d_fp8_run(plan, x, w, s_d[0:1], s_d[1:2], y, shape.stride, shape.pad, stream)
+        if not bf16:
+            s_d.copy_(s_h, non_blocking=True)
+        run(s_d[0:1], s_d[1:2])
         y_h.copy_(y, non_blocking=True)
     e_stop.record(stream)
     torch.cuda.synchronize()
@@ -355,22 +381,25 @@ def run_ours(args):
         raise RuntimeError("e2e result has unwritten outputs")
     e2e = {"value": fig["flop"] * dist.world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
            "ms_per_step": round(e2e_ms, 4),
-           "h2d_bytes_per_step": int(x_h.numel() + w_h.numel() + 4 * s_h.numel()),
+           "h2d_bytes_per_step": int(x_h.numel() * x_h.element_size() +
+                                     w_h.numel() * w_h.element_size() + 4 * s_h.numel()),
            "d2h_bytes_per_step": int(2 * y_h.numel())}
 
     # ---- roofline of the dominant kernel (the implicit-GEMM kernel)
     peaks, peaks_kind = load_peaks()
-    fp8_peak = FP8_PER_BF16 * float(peaks["bf16_tflops"])
+    # the contraction's own dtype: e4m3 = the measured bf16 peak x the nominal fp8/bf16 ratio
+    fp8_peak = (1.0 if bf16 else FP8_PER_BF16) * float(peaks["bf16_tflops"])
     hbm_peak = float(peaks["hbm_gbs"])
     t_flop = fig["flop"] / (fp8_peak * 1e12)
     t_hbm = fig["alg_bytes"] / (hbm_peak * 1e9)
-    workload = shape.name
+    workload = shape.name + (" [bf16 inputs]" if bf16 else "")
     traffic = committed_traffic(workload)
     if t_flop >= t_hbm:
         achieved = fig["flop"] / (mean_kern_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak, 1),
                 "unit": "TFLOP/s", "frac": round(achieved / fp8_peak, 4),
-                "peak_source": f"{peaks_kind} bf16 burst x {FP8_PER_BF16:g} (nominal fp8/bf16)"}
+                "peak_source": (f"{peaks_kind} bf16 burst" if bf16 else
+                                f"{peaks_kind} bf16 burst x {FP8_PER_BF16:g} (nominal fp8/bf16)")}
     else:
         achieved = fig["alg_bytes"] / (mean_kern_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": round(hbm_peak, 1),
@@ -389,12 +418,12 @@ def run_ours(args):
 
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_oracle_sample(inp, shape, args.cpu_seconds, seed=7)
+        cpu = cpu_oracle_sample(inp, shape, args.cpu_seconds, seed=7, bf16=bf16)
 
     clocks = sampler.summary()
     capi.conv3d_fp8_destroy(plan)
     out = {
-        "metric": "conv3d fp8 TFLOP/s and % of FP8/HBM roofline at 1 GB300",
+        "metric": METRIC_BF16 if bf16 else METRIC,
         "value": round(value, 2),
         "unit": "TFLOP/s",
         "n_gpus": dist.world,
@@ -404,8 +433,8 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3",
-        "data": "synthetic (seeded N(0,1) inputs quantised to e4m3 per tensor)",
+        "dtype": "bf16" if bf16 else "e4m3",
+        "data": DATA_BF16 if bf16 else DATA,
         "config": {"workload": workload, "N": shape.N, "C": shape.C, "D": shape.D, "H": shape.H,
                    "W": shape.W, "K": shape.K, "filter": [shape.T, shape.R, shape.S],
                    "stride": list(shape.stride), "pad": list(shape.pad), "npq": fig["npq"],
@@ -440,26 +469,26 @@ def run_reference(args):
 
     oracle.build()
     shape = synth.CONFIGS[args.config]
-    fig = problem_figures(shape)
-    inp = synth.make_config_inputs(args.config)
-    x, w = inp["x"].numpy(), inp["w"].numpy()
+    bf16 = args.dtype == "bf16"
+    fig = problem_figures(shape, 2 if bf16 else 1)
+    inp = synth.make_config_inputs_bf16(args.config) if bf16 else synth.make_config_inputs(args.config)
+    points = oracle_points_fn(inp, shape, bf16)
     total = shape.K * fig["npq"]
     rng = np.random.default_rng(11)
     # size each step so that warm-up + timed steps take about args.ref_seconds in total
     probe = rng.integers(0, total, 512)
     t0 = time.perf_counter()
-    oracle.conv3d_fp8_points(x, w, inp["sx"], inp["sw"], probe, shape.stride, shape.pad)
+    points(probe)
     rate = 512 / max(time.perf_counter() - t0, 1e-6)
     per_step = max(32, int(rate * args.ref_seconds / max(1, args.steps + args.warmup)))
     per_step = min(per_step, total)
     for _ in range(args.warmup):
-        oracle.conv3d_fp8_points(x, w, inp["sx"], inp["sw"], rng.integers(0, total, per_step),
-                                 shape.stride, shape.pad)
+        points(rng.integers(0, total, per_step))
     times = []
     for _ in range(args.steps):
         idx = rng.integers(0, total, per_step)
         t0 = time.perf_counter()
-        oracle.conv3d_fp8_points(x, w, inp["sx"], inp["sw"], idx, shape.stride, shape.pad)
+        points(idx)
         times.append(time.perf_counter() - t0)
     flop = 2.0 * fig["k_gemm"] * per_step
     ms = 1e3 * statistics.mean(times)
@@ -467,7 +496,7 @@ def run_reference(args):
     sample = f"{per_step} random outputs of {total} per step (fp64 direct sum, one by one)"
     out = {
         "impl": "reference",
-        "metric": "conv3d fp8 TFLOP/s and % of FP8/HBM roofline at 1 GB300",
+        "metric": METRIC_BF16 if bf16 else METRIC,
         "value": value,
         "unit": "TFLOP/s",
         "n_gpus": world,
@@ -478,8 +507,8 @@ def run_reference(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f64",
-        "data": "synthetic (seeded N(0,1) inputs quantised to e4m3 per tensor)",
-        "config": {"workload": shape.name, "N": shape.N, "C": shape.C, "D": shape.D,
+        "data": DATA_BF16 if bf16 else DATA,
+        "config": {"workload": shape.name + (" [bf16 inputs]" if bf16 else ""), "N": shape.N, "C": shape.C, "D": shape.D,
                    "H": shape.H, "W": shape.W, "K": shape.K,
                    "filter": [shape.T, shape.R, shape.S], "stride": list(shape.stride),
                    "pad": list(shape.pad), "npq": fig["npq"],
@@ -502,6 +531,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--dtype", choices=["e4m3", "bf16"], default="e4m3",
+                    help="input type: the e4m3 path, or its BF16-input twin")
     ap.add_argument("--input-layout", choices=["ncdhw", "ndhwc"], default="ncdhw",
                     help="layout of x handed to the library (y is NCDHW either way)")
     args = ap.parse_args()
