@@ -7,7 +7,8 @@ CUDA package and the CUDA package imports nothing from it.
 The arithmetic lives in ``conv3d_fp8_oracle.c`` (plain C, fp64, OpenMP over output channels);
 this module only builds that file with gcc and marshals numpy arrays through ctypes.
 What it computes, and the passages it follows, are stated in the C file's header.
-``alias.py`` holds the padded-row alias predictor (a counting function, no convolution).
+``alias.py`` holds the padded-row alias predictor (a counting function, no convolution);
+``quantize.py`` the per-tensor e4m3 quantiser (numpy).
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against values fixed by the
 e4m3/bfloat16 formats, closed forms, special cases that reduce to library routines, brute force
