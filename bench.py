@@ -281,6 +281,13 @@ def run_ours(args):
     channels_last = args.input_layout == "ndhwc"
     # the library's x: the same bytes, laid out NDHWC when asked (the oracle keeps NCDHW)
     x_lib = inp["x"].permute(0, 2, 3, 4, 1).contiguous() if channels_last else inp["x"]
+    quant = args.quantize_x  # x handed over as fp32 / bf16 values, quantised on the device
+    if quant:
+        if bf16 or channels_last:
+            raise SystemExit("--quantize-x runs the e4m3 path on an NCDHW x")
+        g = torch.Generator().manual_seed(synth.config_seed(args.config))
+        x_lib = torch.randn((shape.N, shape.C, shape.D, shape.H, shape.W), generator=g).to(
+            torch.float32 if quant == "fp32" else torch.bfloat16)
 
     make_plan = capi.conv3d_bf16_plan if bf16 else capi.conv3d_fp8_plan
     plan = make_plan(shape.N, shape.C, shape.D, shape.H, shape.W, shape.K, shape.T, shape.R,
@@ -295,11 +302,16 @@ def run_ours(args):
                    dtype=torch.bfloat16, device=dev)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
-    # pack, main kernel, and the reduction when some tiles are split along K
+    # pack, main kernel, and the reduction when some tiles are split along K (+ the amax
+    # reduction and the scale finalisation when x is quantised on the device)
     launches_per_step = 2 + (1 if info["full_tiles"] < info["m_tiles"] * info["n_tiles"] else 0)
+    launches_per_step += 2 if quant else 0
 
     def run(scale_x, scale_w):
-        if bf16:
+        if quant:
+            capi.conv3d_fp8_run_quantize_x(plan, x, w, scale_w, y, shape.stride, shape.pad, None,
+                                           stream)
+        elif bf16:
             capi.conv3d_bf16_run(plan, x, w, y, shape.stride, shape.pad, stream)
         else:
             capi.conv3d_fp8_run(plan, x, w, scale_x, scale_w, y, shape.stride, shape.pad, stream)
@@ -416,6 +428,30 @@ def run_ours(args):
     roof["alg_bytes"] = fig["alg_bytes"]
     roof["step_roofline_frac"] = round(max(t_flop, t_hbm) / (mean_step_ms * 1e-3), 4)
 
+    # ---- the device quantiser alone (two passes over x: amax, then the cast), HBM-bound
+    quantiser = None
+    if quant:
+        n = x.numel()
+        qdst = torch.empty(n, dtype=torch.uint8, device=dev)
+        qscale = torch.empty(1, dtype=torch.float32, device=dev)
+        qms = []
+        for i in range(13):
+            flush.fill_(i & 255)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            capi.conv3d_fp8_quantize(x, qdst, qscale, stream)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                qms.append(e0.elapsed_time(e1))
+        qbytes = 2 * n * x.element_size() + n  # read x twice (amax, cast), write the codes
+        q_ms = statistics.median(qms)
+        quantiser = {"kernels": "amax_kernel + quant_cast_kernel + quant_finalize_kernel",
+                     "bound": "hbm", "ms": round(q_ms, 5), "alg_bytes": qbytes,
+                     "achieved": round(qbytes / (q_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                     "peak": round(hbm_peak, 1),
+                     "frac": round(qbytes / (q_ms * 1e-3) / 1e9 / hbm_peak, 4)}
+
     cpu = None
     if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
         cpu = cpu_oracle_sample(inp, shape, args.cpu_seconds, seed=7, bf16=bf16)
@@ -440,6 +476,8 @@ def run_ours(args):
                    "stride": list(shape.stride), "pad": list(shape.pad), "npq": fig["npq"],
                    "gflop_per_step": round(fig["flop"] / 1e9, 3),
                    "input_layout": "NDHWC" if channels_last else "NCDHW", "output_layout": "NCDHW",
+                   "x_source": (f"{quant} values, quantised to e4m3 on the device every step"
+                                if quant else "e4m3 bytes"),
                    "plan": {k: info[k] for k in ("route", "cta_pair", "block_m", "block_n",
                                                  "m_tiles", "n_tiles", "full_tiles", "splits",
                                                  "stages", "grid", "row_chk")},
@@ -447,6 +485,7 @@ def run_ours(args):
                          "per-step events)",
                    "parallelism": f"replicas x{dist.world}"},
         "roofline": roof,
+        "quantiser": quantiser,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K,
@@ -533,6 +572,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--dtype", choices=["e4m3", "bf16"], default="e4m3",
                     help="input type: the e4m3 path, or its BF16-input twin")
+    ap.add_argument("--quantize-x", choices=["fp32", "bf16"], default=None,
+                    help="hand x over as fp32 / bf16 values: each step quantises it on the device")
     ap.add_argument("--input-layout", choices=["ncdhw", "ndhwc"], default="ncdhw",
                     help="layout of x handed to the library (y is NCDHW either way)")
     args = ap.parse_args()

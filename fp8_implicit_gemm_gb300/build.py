@@ -22,7 +22,7 @@ INCLUDE = os.path.join(REPO_ROOT, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 LIB_NAME = "libconv3d_fp8.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
-SOURCES = ["api.cu", "pack.cu", "conv_tc.cu", "conv_tc_pair.cu"]
+SOURCES = ["api.cu", "pack.cu", "conv_tc.cu", "conv_tc_pair.cu", "quant.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                  "-I", INCLUDE, "-I", CSRC]

@@ -95,6 +95,10 @@ def load() -> ctypes.CDLL:
             lib.conv3d_bf16_describe.restype = ci
             lib.conv3d_bf16_describe.argtypes = ([ci] * 9 + [i3, i3, ci, ctypes.POINTER(Options),
                                                              ctypes.POINTER(PlanInfo)])
+            lib.conv3d_fp8_quantize.restype = ci
+            lib.conv3d_fp8_quantize.argtypes = [vp, ci, ctypes.c_longlong, vp, vp, vp]
+            lib.conv3d_fp8_run_quantize_x.restype = ci
+            lib.conv3d_fp8_run_quantize_x.argtypes = [vp, vp, ci, vp, vp, vp, i3, i3, vp, vp]
             lib.conv3d_fp8_workspace_size.restype = ctypes.c_size_t
             lib.conv3d_fp8_workspace_size.argtypes = [vp]
             lib.conv3d_fp8_out_dims.restype = ci
@@ -304,3 +308,40 @@ def conv3d_bf16_describe(N, C, D, H, W, K, T, R, S, stride, pad, sm_count, **opt
                                      ctypes.byref(info))
     _raise(st, "conv3d_bf16_describe")
     return info.as_dict()
+
+
+# ------------------------------------------------------------------------------- quantiser
+CONV3D_SRC_F32 = 1
+CONV3D_SRC_BF16 = 2
+
+
+def _src_type(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return CONV3D_SRC_F32
+    if t.dtype == torch.bfloat16:
+        return CONV3D_SRC_BF16
+    raise ValueError(f"the quantiser takes fp32 or bfloat16 values, not {t.dtype}")
+
+
+def conv3d_fp8_quantize_status(src, dst, scale_out, stream=None) -> int:
+    """Quantise a CUDA fp32/bfloat16 tensor into uint8 e4m3 codes (dst) and a device scale."""
+    return load().conv3d_fp8_quantize(_ptr(src), _src_type(src), src.numel(), _ptr(dst),
+                                      _ptr(scale_out), _stream(stream))
+
+
+def conv3d_fp8_quantize(src, dst, scale_out, stream=None) -> None:
+    _raise(conv3d_fp8_quantize_status(src, dst, scale_out, stream), "conv3d_fp8_quantize")
+
+
+def conv3d_fp8_run_quantize_x_status(plan, x_src, w, scale_w, y, stride, pad, scale_x_out=None,
+                                     stream=None) -> int:
+    return load().conv3d_fp8_run_quantize_x(plan, _ptr(x_src), _src_type(x_src), _ptr(w),
+                                            _ptr(scale_w), _ptr(y), _int3(stride), _int3(pad),
+                                            _ptr(scale_x_out), _stream(stream))
+
+
+def conv3d_fp8_run_quantize_x(plan, x_src, w, scale_w, y, stride, pad, scale_x_out=None,
+                              stream=None) -> None:
+    _raise(conv3d_fp8_run_quantize_x_status(plan, x_src, w, scale_w, y, stride, pad, scale_x_out,
+                                            stream), "conv3d_fp8_run_quantize_x")

@@ -532,7 +532,8 @@ conv3d_status plan_impl(int elem_bytes, conv3d_fp8_plan_t* out, int N, int C, in
 // Runs of both input types; the bfloat16 entry passes the plan's fp32 ones as the scales.
 conv3d_status run_impl(conv3d_fp8_plan_t plan, const void* x, const void* w,
                        const float* scale_x, const float* scale_w, void* y,
-                       const int stride[3], const int pad[3], void* stream) {
+                       const int stride[3], const int pad[3], void* stream,
+                       int x_src_type = kSrcE4m3) {
   if (!plan || !x || !w || !scale_x || !scale_w || !y || !stride || !pad) return CONV3D_EINVAL;
   if (!aligned(x, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(scale_x, 4) ||
       !aligned(scale_w, 4))
@@ -544,6 +545,7 @@ conv3d_status run_impl(conv3d_fp8_plan_t plan, const void* x, const void* w,
   if (cur != plan->device) return CONV3D_EINVAL;
 
   ConvParams p = plan->p;
+  p.x_src_type = x_src_type;
   p.x = static_cast<const uint8_t*>(x);
   p.w = static_cast<const uint8_t*>(w);
   p.y = static_cast<uint16_t*>(y);
@@ -605,6 +607,50 @@ conv3d_status conv3d_bf16_run(conv3d_fp8_plan_t plan, const void* x, const void*
                               const int stride[3], const int pad[3], void* stream) {
   if (!plan || plan->elem_bytes != 2) return CONV3D_EINVAL;
   return run_impl(plan, x, w, plan->ones, plan->ones + 1, y, stride, pad, stream);
+}
+
+conv3d_status conv3d_fp8_quantize(const void* src, int src_type, long long n, void* dst_e4m3,
+                                  float* scale_out, void* stream) {
+  if (!src || !dst_e4m3 || !scale_out || n <= 0) return CONV3D_EINVAL;
+  if (src_type != CONV3D_SRC_F32 && src_type != CONV3D_SRC_BF16) return CONV3D_EINVAL;
+  if (!aligned(src, 16) || !aligned(dst_e4m3, 16) || !aligned(scale_out, 4)) return CONV3D_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int type = src_type == CONV3D_SRC_F32 ? kSrcF32 : kSrcBf16;
+  // scale_out holds the amax bits until the finalisation turns them into the scale
+  unsigned* amax = reinterpret_cast<unsigned*>(scale_out);
+  if (launch_amax(src, type, n, amax, s) != cudaSuccess ||
+      launch_quant_cast(src, type, n, static_cast<uint8_t*>(dst_e4m3), amax, s) != cudaSuccess ||
+      launch_quant_finalize(amax, scale_out, nullptr, s) != cudaSuccess)
+    return CONV3D_ECUDA;
+  return CONV3D_OK;
+}
+
+conv3d_status conv3d_fp8_run_quantize_x(conv3d_fp8_plan_t plan, const void* x_src, int src_type,
+                                        const void* w, const float* scale_w, void* y,
+                                        const int stride[3], const int pad[3], float* scale_x_out,
+                                        void* stream) {
+  if (!plan || plan->elem_bytes != 1 || plan->p.x_cl) return CONV3D_EINVAL;
+  if (src_type != CONV3D_SRC_F32 && src_type != CONV3D_SRC_BF16) return CONV3D_EINVAL;
+  if (!x_src || !aligned(x_src, 16) || (scale_x_out && !aligned(scale_x_out, 4)))
+    return CONV3D_EINVAL;
+  if (!w || !scale_w || !y || !stride || !pad) return CONV3D_EINVAL;
+  for (int i = 0; i < 3; ++i)
+    if (stride[i] != plan->stride[i] || pad[i] != plan->pad[i]) return CONV3D_EINVAL;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return CONV3D_ECUDA;
+  if (cur != plan->device) return CONV3D_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int type = src_type == CONV3D_SRC_F32 ? kSrcF32 : kSrcBf16;
+  const ConvParams& q = plan->p;
+  const long long n = (long long)q.N * q.C * q.D * q.H * q.W;
+  // the plan's 256-byte status slot: status word at 0, amax bits at 64, the scale of x at 68
+  uint8_t* slot = reinterpret_cast<uint8_t*>(q.status);
+  unsigned* amax = reinterpret_cast<unsigned*>(slot + 64);
+  float* scale_x = reinterpret_cast<float*>(slot + 68);
+  if (launch_amax(x_src, type, n, amax, s) != cudaSuccess ||
+      launch_quant_finalize(amax, scale_x, scale_x_out, s) != cudaSuccess)
+    return CONV3D_ECUDA;
+  return run_impl(plan, x_src, w, scale_x, scale_w, y, stride, pad, stream, type);
 }
 
 conv3d_status conv3d_bf16_describe(int N, int C, int D, int H, int W, int K, int T, int R, int S,

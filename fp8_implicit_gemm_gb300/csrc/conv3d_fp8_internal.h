@@ -24,6 +24,9 @@ enum : int {
                      // the S taps along W (CTA pairs only)
 };
 
+// Source types of the quantiser (and of x when a run quantises it in the pack).
+enum : int { kSrcE4m3 = 0, kSrcF32 = 1, kSrcBf16 = 2 };
+
 // Status-word bits recorded by kernels whose bounded waits ran out.
 enum : int {
   kStatusWaitFull = 1 << 0,       // MMA warp waiting for operands
@@ -45,6 +48,8 @@ struct ConvParams {
   int Dp, Hp, Wp;        // extents of the packed channels-last copy of x (halo included)
   int Dg, Hg, Wg;        // padded-grid route: extents of the zero-padded grid, D + 2 pd, ...
   int x_cl;              // the caller's x is channels-last (NDHWC): no transpose in the pack
+  int x_src_type;        // kSrcE4m3: x is e4m3 bytes; kSrcF32 / kSrcBf16: the pack quantises x
+                         // (NCDHW values) with the device scale *scale_x
   int a_grid_im2col;     // padded-grid route: A by im2col loads from an unpadded channels-last x
                          // (the caller's); otherwise by 2D tiles of the zero-padded copy
   int dhw;               // Do*Ho*Wo
@@ -82,6 +87,14 @@ cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream);
 cudaError_t launch_conv(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
                         bool row_chk, int grid, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ConvParams& p, bool row_chk, cudaStream_t stream);
+// quantiser (quant.cu): amax of |src| into *amax_bits (zeroed first); e4m3 codes of src with the
+// scale of that amax; the scale itself into scale_out (and scale_copy when not null)
+cudaError_t launch_amax(const void* src, int type, long long n, unsigned* amax_bits,
+                        cudaStream_t stream);
+cudaError_t launch_quant_cast(const void* src, int type, long long n, uint8_t* dst,
+                              const unsigned* amax_bits, cudaStream_t stream);
+cudaError_t launch_quant_finalize(const unsigned* amax_bits, float* scale_out, float* scale_copy,
+                                  cudaStream_t stream);
 size_t conv_smem_bytes(int block_n, int stages);
 cudaError_t conv_set_smem_attr(size_t smem_bytes);  // both kernels
 cudaError_t launch_conv_pair(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,

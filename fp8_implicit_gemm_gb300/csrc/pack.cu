@@ -11,6 +11,7 @@
 #include <cuda_bf16.h>
 
 #include "conv_common.cuh"
+#include "quant.cuh"
 
 namespace c3d {
 
@@ -18,6 +19,8 @@ namespace c3d {
 //   [0, x_items)          interior of x: with W % 4 == 0, one item = 16 channels x 4 pixels (16
 //                         aligned 4-byte loads, a byte transpose in registers, four 16-byte
 //                         stores); otherwise one item = 16 channels x 1 pixel (16 byte loads);
+//                         an fp32 or bfloat16 x (x_src_type) is quantised to e4m3 on the way, with
+//                         the device scale *scale_x, in the same items;
 //                         from a channels-last x, one item = one 16-byte chunk copied into the
 //                         padded copy (no items when the TMA routes read that x directly)
 //   + halo_row_items      16-byte zero chunks of the padded rows (d or h in the halo)
@@ -63,6 +66,7 @@ __global__ void __launch_bounds__(256) pack_kernel(ConvParams p, PackPlan q) {
   const long long total = e3 + q.w_items;
   const int cq_n = p.C >> 4;
   const long long plane = (long long)p.D * p.H * p.W;
+  const float qs = p.x_src_type != kSrcE4m3 ? __ldg(p.scale_x) : 1.0f;
   for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < total;
        g += (long long)gridDim.x * blockDim.x) {
     if (g < e1 && q.copy) {
@@ -78,6 +82,59 @@ __global__ void __launch_bounds__(256) pack_kernel(ConvParams p, PackPlan q) {
       *reinterpret_cast<uint4*>(
           p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) * p.Wp + w + p.pk_pw) *
                      p.C + cq * 16) = v;
+    } else if (g < e1 && p.x_src_type != kSrcE4m3) {
+      // interior, quantised from fp32 / bfloat16 values: as the e4m3 items below, each channel's
+      // 4 (or 1) pixels quantised into one 32-bit word (or byte) before the byte transpose
+      const int per_row = q.quad ? p.W / 4 : p.W;
+      const int wi = (int)(g % per_row);
+      const long long rest = g / per_row;
+      const int cq = (int)(rest % cq_n);
+      const long long row = rest / cq_n;  // n*D*H + d*H + h
+      const int h = (int)(row % p.H);
+      const int d = (int)((row / p.H) % p.D);
+      const int n = (int)(row / ((long long)p.H * p.D));
+      const long long el0 = ((long long)n * p.C + cq * 16) * plane + ((long long)d * p.H + h) * p.W;
+      uint8_t* dst_row = p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) *
+                                     p.Wp + p.pk_pw) * p.C + cq * 16;
+      if (q.quad) {
+        uint32_t v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const long long e = el0 + j * plane + 4 * wi;
+          float a[4];
+          if (p.x_src_type == kSrcF32) {
+            const float4 f = __ldg(reinterpret_cast<const float4*>(p.x) + e / 4);
+            a[0] = f.x; a[1] = f.y; a[2] = f.z; a[3] = f.w;
+          } else {
+            const uint2 u = __ldg(reinterpret_cast<const uint2*>(p.x) + e / 4);
+            a[0] = __uint_as_float(u.x << 16);
+            a[1] = __uint_as_float(u.x & 0xFFFF0000u);
+            a[2] = __uint_as_float(u.y << 16);
+            a[3] = __uint_as_float(u.y & 0xFFFF0000u);
+          }
+          v[j] = quant4(a[0], a[1], a[2], a[3], qs);
+        }
+        uint32_t o[4][4];  // o[pixel][word of 4 channels]
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          uint32_t t[4];
+          transpose4x4(v + 4 * b, t);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) o[j][b] = t[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(dst_row + (long long)(4 * wi + j) * p.C) =
+              make_uint4(o[j][0], o[j][1], o[j][2], o[j][3]);
+      } else {
+        uint32_t v[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float a = src_value(p.x, p.x_src_type, el0 + j * plane + wi);
+          v[j >> 2] |= (quant4(a, 0.0f, 0.0f, 0.0f, qs) & 0xFFu) << ((j & 3) * 8);
+        }
+        *reinterpret_cast<uint4*>(dst_row + (long long)wi * p.C) = make_uint4(v[0], v[1], v[2], v[3]);
+      }
     } else if (g < e1 && p.elem_bytes == 2) {
       // interior, bfloat16: one item = 8 channels (one 16-byte chunk) x 2 pixels (or 1 when W is
       // odd); pixels fastest, then chunk, then (n, d, h) row

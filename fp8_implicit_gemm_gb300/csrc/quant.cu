@@ -1,0 +1,137 @@
+// quant.cu -- per-tensor e4m3 quantiser on the GPU: the producer of the e4m3 bytes and of the
+// per-tensor scale that the implicit GEMM consumes ("fp8cast" on the subject page, "[Fix] conv3d
+// fp8: guard padded M rows in the epilogue store", section "Problem").
+//
+//   amax = max |v|,  s = fp32(amax / 448) (1 when amax == 0),
+//   q = e4m3_rne(clamp(fp32(v / s), +-448))
+//
+// Three launches, no host synchronisation: an amax reduction into a device word (the bit pattern
+// of a non-negative float orders like the float, so an integer max is the float max), the cast
+// (IEEE fp32 division, then the hardware's satfinite round-to-nearest-even e4m3 conversion), and
+// a one-thread finalisation that turns the amax into the scale. The cast of x can instead be
+// fused into the pack of a run (pack.cu, x_src_type != 0), which reads the finalised scale.
+// NaN inputs are not supported (the reduction would carry them into the scale).
+#include <cuda_runtime.h>
+
+#include "conv3d_fp8_internal.h"
+#include "quant.cuh"
+
+namespace c3d {
+
+constexpr int kQuantThreads = 256;
+
+__global__ void __launch_bounds__(kQuantThreads) amax_kernel(const void* src, int type,
+                                                             long long n, unsigned* amax_bits) {
+  const int per_vec = type == kSrcF32 ? 4 : 8;  // elements in 16 bytes
+  const long long nvec = n / per_vec;
+  const uint8_t* base = static_cast<const uint8_t*>(src);
+  float m = 0.0f;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nvec; i += stride) {
+    if (type == kSrcF32) {
+      float v[4];
+      load16_f32(base + i * 16, v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) m = fmaxf(m, fabsf(v[j]));
+    } else {
+      float v[8];
+      load16_bf16(base + i * 16, v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+    }
+  }
+  for (long long i = nvec * per_vec + blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += stride)
+    m = fmaxf(m, fabsf(src_value(src, type, i)));
+  unsigned bits = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(m));
+  __shared__ unsigned warp_max[kQuantThreads / 32];
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = bits;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    bits = threadIdx.x < kQuantThreads / 32 ? warp_max[threadIdx.x] : 0u;
+    bits = __reduce_max_sync(0xFFFFFFFFu, bits);
+    if (threadIdx.x == 0) atomicMax(amax_bits, bits);
+  }
+}
+
+__global__ void __launch_bounds__(kQuantThreads) quant_cast_kernel(const void* src, int type,
+                                                                   long long n, uint8_t* dst,
+                                                                   const unsigned* amax_bits) {
+  const float s = scale_from_amax(*amax_bits);
+  const long long nchunk = n / 16;  // 16 elements -> one 16-byte store
+  const uint8_t* base = static_cast<const uint8_t*>(src);
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nchunk; i += stride) {
+    float v[16];
+    if (type == kSrcF32) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float t[4];
+        load16_f32(base + (i * 4 + k) * 16, t);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[4 * k + j] = t[j];
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        float t[8];
+        load16_bf16(base + (i * 2 + k) * 16, t);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[8 * k + j] = t[j];
+      }
+    }
+    uint4 o;
+    o.x = quant4(v[0], v[1], v[2], v[3], s);
+    o.y = quant4(v[4], v[5], v[6], v[7], s);
+    o.z = quant4(v[8], v[9], v[10], v[11], s);
+    o.w = quant4(v[12], v[13], v[14], v[15], s);
+    *reinterpret_cast<uint4*>(dst + i * 16) = o;
+  }
+  for (long long i = nchunk * 16 + blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n;
+       i += stride)
+    dst[i] = (uint8_t)(quant4(src_value(src, type, i), 0.0f, 0.0f, 0.0f, s) & 0xFFu);
+}
+
+// scale_out[0] (and scale_copy[0], if given) = the scale of the reduced amax
+__global__ void quant_finalize_kernel(const unsigned* amax_bits, float* scale_out,
+                                      float* scale_copy) {
+  const float s = scale_from_amax(*amax_bits);
+  *scale_out = s;
+  if (scale_copy) *scale_copy = s;
+}
+
+static int quant_blocks(long long work) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  long long b = (work + kQuantThreads - 1) / kQuantThreads;
+  const long long cap = (long long)(sms > 0 ? sms : 1) * 8;
+  if (b > cap) b = cap;
+  return b < 1 ? 1 : (int)b;
+}
+
+cudaError_t launch_amax(const void* src, int type, long long n, unsigned* amax_bits,
+                        cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(amax_bits, 0, sizeof(unsigned), stream);
+  if (e != cudaSuccess) return e;
+  const long long vecs = n / (type == kSrcF32 ? 4 : 8);
+  amax_kernel<<<quant_blocks(vecs > 0 ? vecs : 1), kQuantThreads, 0, stream>>>(src, type, n,
+                                                                               amax_bits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_cast(const void* src, int type, long long n, uint8_t* dst,
+                              const unsigned* amax_bits, cudaStream_t stream) {
+  const long long chunks = n / 16;
+  quant_cast_kernel<<<quant_blocks(chunks > 0 ? chunks : 1), kQuantThreads, 0, stream>>>(
+      src, type, n, dst, amax_bits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_finalize(const unsigned* amax_bits, float* scale_out, float* scale_copy,
+                                  cudaStream_t stream) {
+  quant_finalize_kernel<<<1, 1, 0, stream>>>(amax_bits, scale_out, scale_copy);
+  return cudaGetLastError();
+}
+
+}  // namespace c3d

@@ -199,6 +199,39 @@ void conv3d_fp8_destroy(conv3d_fp8_plan_t plan);
 const char *conv3d_fp8_strerror(conv3d_status status);
 
 /*
+ * Per-tensor e4m3 quantiser on the GPU: the producer of the e4m3 bytes and scale that
+ * conv3d_fp8_run consumes (the "fp8cast" of the subject page's section "Problem"), with no host
+ * synchronisation:
+ *   amax = max |v|,  s = fp32(amax / 448) (1 when amax == 0),
+ *   q = e4m3 round-to-nearest-even of clamp(fp32(v / s), -448, 448) (IEEE fp32 division).
+ * NaN inputs are not supported (their codes and the scale are then unspecified).
+ */
+typedef enum { CONV3D_SRC_F32 = 1, CONV3D_SRC_BF16 = 2 } conv3d_src_type;
+
+/*
+ * Quantise n values of src (fp32 or bfloat16, 16-byte aligned device pointer) into n e4m3 bytes
+ * at dst_e4m3 (16-byte aligned) and their scale into *scale_out (a device float, which also holds
+ * the running amax while the call's kernels execute). Asynchronous on `stream`. Errors: EINVAL
+ * (NULL or misaligned pointers, n <= 0, unknown src_type), ECUDA.
+ */
+conv3d_status conv3d_fp8_quantize(const void *src, int src_type, long long n, void *dst_e4m3,
+                                  float *scale_out, void *stream);
+
+/*
+ * A run of an e4m3 plan (made with input_layout = 0) from an fp32 or bfloat16 NCDHW x: the amax
+ * and the scale of x are computed on the device, the pack quantises x to e4m3 while it transposes
+ * it (no separate quantised copy), and the implicit GEMM reads the scale from the device.
+ *   x_src: N*C*D*H*W values of src_type, contiguous NCDHW, 16-byte aligned.
+ *   w_kctrs, scale_w, y_ncdhw, stride, pad: as for conv3d_fp8_run.
+ *   scale_x_out: if not NULL, a device float that receives the scale of x.
+ * Errors: EINVAL (as conv3d_fp8_run, a bfloat16 or channels-last plan, unknown src_type), ECUDA.
+ */
+conv3d_status conv3d_fp8_run_quantize_x(conv3d_fp8_plan_t plan, const void *x_src, int src_type,
+                                        const void *w_kctrs, const float *scale_w, void *y_ncdhw,
+                                        const int stride[3], const int pad[3], float *scale_x_out,
+                                        void *stream);
+
+/*
  * BF16-input twin ("Notes" of the subject page: the BF16 implicit-GEMM conv3d kernel, which guards
  * its padded rows the same way). The same convolution with bfloat16 x and w and no scales:
  *   y = bf16(sum over c, t, r, s of x * w), fp32 accumulation on the tensor cores
