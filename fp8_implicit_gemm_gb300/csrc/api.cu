@@ -21,6 +21,8 @@ struct conv3d_fp8_plan_s {
   CUtensorMap wmap{};
   CUtensorMap xmap{};  // A tensor map (TMA routes)
   const void* xmap_src = nullptr;  // caller's x the A map was last encoded for (channels-last x)
+  CUtensorMap ymap{};              // y as [N][K][dhw] bf16 (TMA-store epilogue)
+  const void* ymap_src = nullptr;  // caller's y the map was last encoded for
   int elem_bytes = 1;              // 1: e4m3 plan (conv3d_fp8_*), 2: bfloat16 plan (conv3d_bf16_*)
   const float* ones = nullptr;     // device fp32 {1, 1}: the scales of a bfloat16 plan's runs
   conv3d_fp8_plan_info info{};
@@ -88,7 +90,7 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
   conv3d_fp8_options o{};
   if (opts) o = *opts;
   if (o.route < 0 || o.route > 3 || o.cta_pair < 0 || o.cta_pair > 2 || o.input_layout < 0 ||
-      o.input_layout > 1)
+      o.input_layout > 1 || o.epilogue < 0 || o.epilogue > 2)
     return CONV3D_EINVAL;
   const bool x_cl = o.input_layout == 1;  // the caller's x is channels-last
   // The TMA im2col route needs C in whole 32-byte sub-tile rows and bounding-box corners
@@ -123,6 +125,12 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
   else
     route = im2col_ok ? kRouteIm2col : kRouteGather;
   const int a_cb = C % 128 == 0 ? 128 : (C % 64 == 0 ? 64 : 32);
+  // TMA-store epilogue: the output-position routes (a tile's rows are consecutive positions of
+  // one image's dhw run), with dhw a multiple of 8 (16-byte rows of the map of y and 16-byte
+  // aligned box starts). By default the explicit guarded stores.
+  const bool epi_ok = route != kRouteGrid && dhw % 8 == 0;
+  if (o.epilogue == 2 && !epi_ok) return CONV3D_EUNSUPPORTED;
+  const bool epi_tma = o.epilogue == 2;
   // A zero-padded channels-last copy of x for the gather route, and for the padded-grid route
   // when the library transposes x anyway; the TMA routes read a channels-last x of the caller
   // directly (no copy at all), and the im2col route's copy needs no halo.
@@ -228,6 +236,7 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
   info->splits = (int)splits;
   info->k_blocks_per_split = (int)kbps;
   info->full_tiles = (int)full_tiles;
+  info->epilogue = epi_tma ? 2 : 1;
   info->stages = stages;
   info->row_chk = route == kRouteGrid ? 1 : (npq % block_m) != 0;
   info->grid = (int)grid;
@@ -250,6 +259,7 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
     p.Dp = (int)Dp; p.Hp = (int)Hp; p.Wp = (int)Wp;
     p.Dg = (int)Dg; p.Hg = (int)Hg; p.Wg = (int)Wg;
     p.x_cl = x_cl ? 1 : 0;
+    p.epi_tma = epi_tma ? 1 : 0;
     p.a_grid_im2col = route == kRouteGrid && x_cl ? 1 : 0;
     p.dhw = (int)dhw;
     p.tiles_per_image = (int)tiles_per_image;
@@ -368,6 +378,21 @@ conv3d_status encode_im2col_map(CUtensorMap* map, void* xcl, const ConvParams& p
   return r == CUDA_SUCCESS ? CONV3D_OK : CONV3D_ECUDA;
 }
 
+// y as a bf16 tensor [N][K][dhw] (dhw innermost) for the TMA-store epilogue: a box is 128
+// positions of 32 channels of one image; stores outside the extents are dropped by the TMA unit.
+conv3d_status encode_ymap(CUtensorMap* map, const ConvParams& p, void* y) {
+  EncodeTiledFn enc = get_encode_tiled();
+  if (!enc) return CONV3D_ECUDA;
+  const cuuint64_t dims[3] = {(cuuint64_t)p.dhw, (cuuint64_t)p.K, (cuuint64_t)p.N};
+  const cuuint64_t strides[2] = {(cuuint64_t)p.dhw * 2, (cuuint64_t)p.K * p.dhw * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kBlockM, 32u, 1u};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, y, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? CONV3D_OK : CONV3D_ECUDA;
+}
+
 // Whether the A tensor map reads the caller's x (a channels-last x on a TMA route), so that it is
 // encoded per run rather than once per plan.
 bool xmap_reads_caller_x(const ConvParams& p) { return p.x_cl && p.route != kRouteGather; }
@@ -481,8 +506,9 @@ conv3d_status plan_impl(int elem_bytes, conv3d_fp8_plan_t* out, int N, int C, in
     plan->stride[i] = stride[i];
     plan->pad[i] = pad[i];
   }
-  const size_t smem = plan->p.pair ? conv_pair_smem_bytes(plan->p)
-                                    : conv_smem_bytes(plan->p.block_n, plan->p.stages);
+  const size_t smem = plan->p.pair
+                         ? conv_pair_smem_bytes(plan->p)
+                         : conv_smem_bytes(plan->p.block_n, plan->p.stages, plan->p.epi_tma != 0);
   if ((int)smem > prop.sharedMemPerBlockOptin) {
     delete plan;
     return CONV3D_EUNSUPPORTED;
@@ -557,10 +583,15 @@ conv3d_status run_impl(conv3d_fp8_plan_t plan, const void* x, const void* w,
     if (st != CONV3D_OK) return st;
     plan->xmap_src = x;
   }
+  if (p.epi_tma && plan->ymap_src != y) {
+    const conv3d_status st = encode_ymap(&plan->ymap, p, y);
+    if (st != CONV3D_OK) return st;
+    plan->ymap_src = y;
+  }
   if (launch_pack(p, s) != cudaSuccess) return CONV3D_ECUDA;
   if (plan->ev_begin && cudaEventRecord(plan->ev_begin, s) != cudaSuccess) return CONV3D_ECUDA;
-  if (launch_conv(p, plan->wmap, plan->xmap, plan->info.row_chk != 0, plan->info.grid, s) !=
-      cudaSuccess)
+  if (launch_conv(p, plan->wmap, plan->xmap, plan->ymap, plan->info.row_chk != 0,
+                  plan->info.grid, s) != cudaSuccess)
     return CONV3D_ECUDA;
   if (has_split_tiles(p) && launch_splitk_reduce(p, plan->info.row_chk != 0, s) != cudaSuccess)
     return CONV3D_ECUDA;
@@ -844,7 +875,8 @@ extern "C" conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(p.status, 0, sizeof(int), s) != cudaSuccess) return CONV3D_ECUDA;
   if (launch_pack(p, s) != cudaSuccess) return CONV3D_ECUDA;
-  if (launch_conv(p, wmap, xmap, info.row_chk != 0, info.grid, s) != cudaSuccess)
+  const CUtensorMap ymap{};  // explicit guarded stores here (no TMA-store epilogue)
+  if (launch_conv(p, wmap, xmap, ymap, info.row_chk != 0, info.grid, s) != cudaSuccess)
     return CONV3D_ECUDA;
   if (has_split_tiles(p) && launch_splitk_reduce(p, info.row_chk != 0, s) != cudaSuccess)
     return CONV3D_ECUDA;

@@ -14,6 +14,7 @@ constexpr int kATileBytes = kBlockM * kBlockK;  // 16 KB
 constexpr int kNumThreads = 320;    // 4 epilogue warps, 4 A-loader warps, 1 TMA warp, 1 MMA warp
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kMaxStages = 8;
+constexpr int kEpiStageBytes = 2 * 32 * kBlockM * 2;  // two bf16 boxes [32 columns][128 rows]
 
 // How the A operand (im2col rows of x) reaches shared memory.
 enum : int {
@@ -48,6 +49,8 @@ struct ConvParams {
   int Dp, Hp, Wp;        // extents of the packed channels-last copy of x (halo included)
   int Dg, Hg, Wg;        // padded-grid route: extents of the zero-padded grid, D + 2 pd, ...
   int x_cl;              // the caller's x is channels-last (NDHWC): no transpose in the pack
+  int epi_tma;           // whole tiles leave through TMA stores bounded by the map of y (output-
+                         // position routes); otherwise explicit guarded stores
   int x_src_type;        // kSrcE4m3: x is e4m3 bytes; kSrcF32 / kSrcBf16: the pack quantises x
                          // (NCDHW values) with the device scale *scale_x
   int a_grid_im2col;     // padded-grid route: A by im2col loads from an unpadded channels-last x
@@ -85,7 +88,7 @@ struct ConvParams {
 // Launchers (defined in the .cu files). Each returns the CUDA error of its launch.
 cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream);
 cudaError_t launch_conv(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
-                        bool row_chk, int grid, cudaStream_t stream);
+                        const CUtensorMap& ymap, bool row_chk, int grid, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ConvParams& p, bool row_chk, cudaStream_t stream);
 // quantiser (quant.cu): amax of |src| into *amax_bits (zeroed first); e4m3 codes of src with the
 // scale of that amax; the scale itself into scale_out (and scale_copy when not null)
@@ -95,10 +98,10 @@ cudaError_t launch_quant_cast(const void* src, int type, long long n, uint8_t* d
                               const unsigned* amax_bits, cudaStream_t stream);
 cudaError_t launch_quant_finalize(const unsigned* amax_bits, float* scale_out, float* scale_copy,
                                   cudaStream_t stream);
-size_t conv_smem_bytes(int block_n, int stages);
+size_t conv_smem_bytes(int block_n, int stages, bool epi_tma);
 cudaError_t conv_set_smem_attr(size_t smem_bytes);  // both kernels
 cudaError_t launch_conv_pair(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
-                             bool row_chk, int grid, cudaStream_t stream);
+                             const CUtensorMap& ymap, bool row_chk, int grid, cudaStream_t stream);
 size_t conv_pair_smem_bytes(const ConvParams& p);
 cudaError_t conv_pair_set_smem_attr(size_t smem_bytes);
 int conv_pair_max_active_clusters(const ConvParams& p);  // 0 if the query fails

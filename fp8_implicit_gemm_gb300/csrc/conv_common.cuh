@@ -143,6 +143,58 @@ __device__ __forceinline__ void epilogue_row(const ConvParams& p, const Unit& un
   }
 }
 
+// Hardware-bounded epilogue of a whole tile (output-position routes, no split): the 128 epilogue
+// threads of the CTA stage 32 columns at a time as bf16 [32 columns][128 rows] in shared memory
+// and one thread stores the box with TMA through the tensor map of y viewed as [N][K][dhw]. The
+// map's extents bound the store in hardware: rows past the end of image n0 (pix >= dhw), among
+// them the padded rows of the last tile, and columns >= K are not written, the TMA counterpart of
+// the buffer-descriptor bound of the subject page ("Root cause"). Rows that spill into a later
+// image take the explicit guarded stores. Two 8 KB buffers alternate; `chunk` counts the boxes
+// this CTA has staged (the same in all 128 threads) and picks the buffer. `m0` = GEMM row of the
+// CTA's first row, `row` = this thread's row (0..127). Uses named barrier 1.
+__device__ __forceinline__ void epilogue_tile_tma(const ConvParams& p, const Unit& un,
+                                                  const CUtensorMap* ymap, uint32_t trow, int m0,
+                                                  int row, float scale, uint16_t* stage,
+                                                  uint32_t& chunk) {
+  const bool any = m0 < p.npq;  // a CTA whose rows are all padding stores nothing
+  const int n0 = any ? m0 / p.dhw : 0;
+  const int pix0 = m0 - n0 * p.dhw;
+  const int r1 = p.dhw - pix0;  // rows [0, r1) lie in image n0
+  const int m = m0 + row;
+  const bool spill = row >= r1 && m < p.npq;
+  long long y_off = 0;
+  if (spill) {
+    const int n = m / p.dhw;
+    y_off = (long long)n * p.K * p.dhw + (m - n * p.dhw);
+  }
+  const int col0 = un.n_tile * p.block_n;
+  for (int cc = 0; cc < p.block_n; cc += 32) {
+    if (col0 + cc >= p.K) break;  // uniform across the 128 threads
+    uint32_t r[32];
+    tmem_ld_32x32b_x32(trow + cc, r);
+    tmem_ld_wait();
+    uint16_t* buf = stage + (chunk & 1u) * (32 * kBlockM);
+    if (chunk >= 2) {  // the box stored from this buffer two chunks ago must have been read
+      if (threadIdx.x == 0) bulk_wait_group_read<1>();
+      named_barrier_sync(1, 128);
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(r[j]) * scale);
+      const uint16_t v = *reinterpret_cast<const uint16_t*>(&b);
+      buf[j * kBlockM + row] = v;
+      if (spill && col0 + cc + j < p.K) p.y[y_off + (long long)(col0 + cc + j) * p.dhw] = v;
+    }
+    fence_proxy_async_smem();  // the staged values, visible to the TMA unit
+    named_barrier_sync(1, 128);
+    if (threadIdx.x == 0 && any) {
+      tma_store_3d(ymap, smem_u32(buf), pix0, col0 + cc, n0);
+      bulk_commit_group();
+    }
+    ++chunk;
+  }
+}
+
 // The (tap, channel) walk of the im2col loads, in K_gemm order: channel fastest by a_cb, then
 // s, r, t.
 struct TapWalk {

@@ -33,7 +33,8 @@ constexpr int kLoaderLag = 2;  // cp.async groups kept in flight before a stage 
 template <bool kRowChk, bool kBf16>
 __global__ void __launch_bounds__(kNumThreads, 1)
     conv3d_fp8_tc_kernel(const __grid_constant__ CUtensorMap wmap,
-                         const __grid_constant__ CUtensorMap xmap, const ConvParams p) {
+                         const __grid_constant__ CUtensorMap xmap,
+                         const __grid_constant__ CUtensorMap ymap, const ConvParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);  // 1024-aligned stages
@@ -42,7 +43,10 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   const uint32_t b_bytes = (uint32_t)p.block_n * kBlockK;
   uint8_t* sA = smem;
   uint8_t* sB = smem + (size_t)S * kATileBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)S * b_bytes);
+  // bf16 staging of the TMA-store epilogue (1024-aligned, after the stages), then the barriers
+  uint16_t* sEpi = reinterpret_cast<uint16_t*>(sB + (size_t)S * b_bytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)S * b_bytes +
+                                               (p.epi_tma ? (size_t)kEpiStageBytes : 0));
   // bars: fullA[S], fullB[S], empty[S], accFull[2], accEmpty[2], drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -78,6 +82,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (lane == 0) {
       prefetch_tensormap(&wmap);
       if (p.route == kRouteIm2col) prefetch_tensormap(&xmap);
+      if (p.epi_tma) prefetch_tensormap(&ymap);
     }
   }
   tc_fence_before();
@@ -90,18 +95,26 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   if (warp < 4) {
     // ------------------------------------------------------------------------------ epilogue
     const float scale = __ldg(p.scale_x) * __ldg(p.scale_w);
-    uint32_t tc = 0;
+    uint32_t tc = 0, chunk = 0;
     for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++tc) {
       const Unit un = decode_unit(p, u);
       const int buf = tc & 1;
-      if (!wait_bounded(accFull(buf), (tc >> 1) & 1, ab, kStatusWaitAccFull)) break;
+      bool ok = wait_bounded(accFull(buf), (tc >> 1) & 1, ab, kStatusWaitAccFull);
+      // the TMA-store epilogue synchronises its 128 threads: they go on or stop together
+      if (p.epi_tma) ok = named_barrier_and(1, 128, ok);
+      if (!ok) break;
       tc_fence_after();
       const uint32_t trow =
           tmem_base + (uint32_t)buf * p.acc_stride + ((uint32_t)(warp * 32) << 16);
-      epilogue_row<kRowChk>(p, un, trow, threadIdx.x, scale);
+      if (p.epi_tma && un.part < 0)
+        epilogue_tile_tma(p, un, &ymap, trow, un.m_tile * p.block_m, threadIdx.x, scale, sEpi,
+                          chunk);
+      else
+        epilogue_row<kRowChk>(p, un, trow, threadIdx.x, scale);
       tc_fence_before();
       mbar_arrive(accEmpty(buf));
     }
+    if (p.epi_tma && threadIdx.x == 0) bulk_wait_group_all();  // stores done before exit
   } else if (warp < 8) {
     // ------------------------------------------------------------------------------ A gather
     if (!im2col) {
@@ -296,8 +309,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   if (warp == 8) tmem_dealloc(tmem_base, (uint32_t)p.tmem_cols);
 }
 
-size_t conv_smem_bytes(int block_n, int stages) {
+size_t conv_smem_bytes(int block_n, int stages, bool epi_tma) {
   return 1024 + (size_t)stages * (kATileBytes + (size_t)block_n * kBlockK) +
+         (epi_tma ? (size_t)kEpiStageBytes : 0) +
          (size_t)(3 * stages + 5) * 8 + 16;
 }
 
@@ -316,18 +330,18 @@ cudaError_t conv_set_smem_attr(size_t smem_bytes) {
 }
 
 cudaError_t launch_conv(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
-                        bool row_chk, int grid, cudaStream_t stream) {
-  if (p.pair) return launch_conv_pair(p, wmap, xmap, row_chk, grid, stream);
-  const size_t smem = conv_smem_bytes(p.block_n, p.stages);
+                        const CUtensorMap& ymap, bool row_chk, int grid, cudaStream_t stream) {
+  if (p.pair) return launch_conv_pair(p, wmap, xmap, ymap, row_chk, grid, stream);
+  const size_t smem = conv_smem_bytes(p.block_n, p.stages, p.epi_tma != 0);
   const bool bf16 = p.elem_bytes == 2;
   if (row_chk && bf16)
-    conv3d_fp8_tc_kernel<true, true><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
+    conv3d_fp8_tc_kernel<true, true><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, ymap, p);
   else if (row_chk)
-    conv3d_fp8_tc_kernel<true, false><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
+    conv3d_fp8_tc_kernel<true, false><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, ymap, p);
   else if (bf16)
-    conv3d_fp8_tc_kernel<false, true><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
+    conv3d_fp8_tc_kernel<false, true><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, ymap, p);
   else
-    conv3d_fp8_tc_kernel<false, false><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, p);
+    conv3d_fp8_tc_kernel<false, false><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, ymap, p);
   return cudaGetLastError();
 }
 

@@ -55,7 +55,8 @@ __host__ __device__ inline void pair_stage_bytes(const ConvParams& p, bool grid,
 template <bool kRowChk, bool kGrid, bool kBf16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     conv3d_fp8_tc_pair_kernel(const __grid_constant__ CUtensorMap wmap,
-                              const __grid_constant__ CUtensorMap xmap, const ConvParams p) {
+                              const __grid_constant__ CUtensorMap xmap,
+                              const __grid_constant__ CUtensorMap ymap, const ConvParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_u32 = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_u32 & 1023u)) & 1023u);  // 1024-aligned stages
@@ -66,7 +67,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
   pair_stage_bytes(p, kGrid, &a_bytes, &b_bytes);
   uint8_t* sA = smem;
   uint8_t* sB = smem + (size_t)S * a_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)S * b_bytes);
+  // bf16 staging of the TMA-store epilogue (1024-aligned, after the stages), then the barriers
+  uint16_t* sEpi = reinterpret_cast<uint16_t*>(sB + (size_t)S * b_bytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sB + (size_t)S * b_bytes +
+                                               (p.epi_tma ? (size_t)kEpiStageBytes : 0));
   // bars: full[S] (leader's is used), empty[S], accFull[2], accEmpty[2] (leader's), drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
@@ -103,6 +107,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     if (lane == 0) {
       prefetch_tensormap(&wmap);
       prefetch_tensormap(&xmap);
+      if (p.epi_tma) prefetch_tensormap(&ymap);
     }
   }
   tc_fence_before();
@@ -117,18 +122,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
   if (warp < 4) {
     // ------------------------------------------------------------------------------ epilogue
     const float scale = __ldg(p.scale_x) * __ldg(p.scale_w);
-    uint32_t tc = 0;
+    uint32_t tc = 0, chunk = 0;
     for (int u = cluster_id; u < p.num_units; u += num_clusters, ++tc) {
       const Unit un = decode_unit(p, u);
       const int buf = tc & 1;
-      if (!wait_bounded<true>(accFull(buf), (tc >> 1) & 1, ab, kStatusWaitAccFull)) break;
+      bool ok = wait_bounded<true>(accFull(buf), (tc >> 1) & 1, ab, kStatusWaitAccFull);
+      // the TMA-store epilogue synchronises its 128 threads: they go on or stop together
+      if (p.epi_tma) ok = named_barrier_and(1, 128, ok);
+      if (!ok) break;
       tc_fence_after();
       const uint32_t trow =
           tmem_base + (uint32_t)buf * p.acc_stride + ((uint32_t)(warp * 32) << 16);
-      epilogue_row<kRowChk>(p, un, trow, row_base + threadIdx.x, scale);
+      if (!kGrid && p.epi_tma && un.part < 0)
+        epilogue_tile_tma(p, un, &ymap, trow, un.m_tile * p.block_m + row_base, threadIdx.x,
+                          scale, sEpi, chunk);
+      else
+        epilogue_row<kRowChk>(p, un, trow, row_base + threadIdx.x, scale);
       tc_fence_before();
       mbar_arrive_cluster(leader_bars + (accEmpty(buf) - bars_u32));
     }
+    if (p.epi_tma && threadIdx.x == 0) bulk_wait_group_all();  // stores done before exit
   } else if (warp == 8) {
     // ------------------------------------------------------------------------------ TMA loader
     if (lane == 0) {
@@ -338,7 +351,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
 size_t conv_pair_smem_bytes(const ConvParams& p) {
   uint32_t a_bytes, b_bytes;
   pair_stage_bytes(p, p.route == kRouteGrid, &a_bytes, &b_bytes);
-  return 1024 + (size_t)p.stages * (a_bytes + b_bytes) + (size_t)(2 * p.stages + 5) * 8 + 16;
+  return 1024 + (size_t)p.stages * (a_bytes + b_bytes) + (p.epi_tma ? (size_t)kEpiStageBytes : 0) +
+         (size_t)(2 * p.stages + 5) * 8 + 16;
 }
 
 cudaError_t conv_pair_set_smem_attr(size_t smem_bytes) {
@@ -358,23 +372,25 @@ cudaError_t conv_pair_set_smem_attr(size_t smem_bytes) {
 
 template <bool kBf16>
 void launch_pair_typed(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
-                       bool row_chk, int grid, size_t smem, cudaStream_t stream) {
+                       const CUtensorMap& ymap, bool row_chk, int grid, size_t smem,
+                       cudaStream_t stream) {
   const dim3 g(grid), b(kNumThreads);
   if (p.route == kRouteGrid)  // grid rows that are not outputs always need the row test
-    conv3d_fp8_tc_pair_kernel<true, true, kBf16><<<g, b, smem, stream>>>(wmap, xmap, p);
+    conv3d_fp8_tc_pair_kernel<true, true, kBf16><<<g, b, smem, stream>>>(wmap, xmap, ymap, p);
   else if (row_chk)
-    conv3d_fp8_tc_pair_kernel<true, false, kBf16><<<g, b, smem, stream>>>(wmap, xmap, p);
+    conv3d_fp8_tc_pair_kernel<true, false, kBf16><<<g, b, smem, stream>>>(wmap, xmap, ymap, p);
   else
-    conv3d_fp8_tc_pair_kernel<false, false, kBf16><<<g, b, smem, stream>>>(wmap, xmap, p);
+    conv3d_fp8_tc_pair_kernel<false, false, kBf16><<<g, b, smem, stream>>>(wmap, xmap, ymap, p);
 }
 
 cudaError_t launch_conv_pair(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
-                             bool row_chk, int grid, cudaStream_t stream) {
+                             const CUtensorMap& ymap, bool row_chk, int grid,
+                             cudaStream_t stream) {
   const size_t smem = conv_pair_smem_bytes(p);
   if (p.elem_bytes == 2)
-    launch_pair_typed<true>(p, wmap, xmap, row_chk, grid, smem, stream);
+    launch_pair_typed<true>(p, wmap, xmap, ymap, row_chk, grid, smem, stream);
   else
-    launch_pair_typed<false>(p, wmap, xmap, row_chk, grid, smem, stream);
+    launch_pair_typed<false>(p, wmap, xmap, ymap, row_chk, grid, smem, stream);
   return cudaGetLastError();
 }
 

@@ -73,6 +73,13 @@ typedef struct {
                             directly and the run packs only the weights (the gather route still
                             copies x into a zero-padded buffer). With 1 the padded-grid route
                             also needs every pad <= 15. y stays NCDHW either way. */
+    int epilogue;        /* 0: the library chooses (explicit stores); 1: explicit stores masked
+                            on row < npq and col < K; 2: TMA stores through a tensor map of y
+                            as [N][K][dhw], whose extents drop what lies past the end of an image
+                            or past K in hardware (rows spilling into a later image still take
+                            guarded stores). 2 needs an output-position route (not the padded
+                            grid) and dhw % 8 == 0 (EUNSUPPORTED otherwise); the map of y is
+                            re-encoded on the host whenever y differs from the previous run's */
 } conv3d_fp8_options;
 
 /* What a plan (or a would-be plan) decided. */
@@ -98,6 +105,7 @@ typedef struct {
                                  are split `splits` ways. With splits == 1 every tile is whole;
                                  a split count in the options splits every tile; by default
                                  only the tiles of a mostly idle last wave are split */
+    int epilogue;             /* 1: explicit guarded stores, 2: TMA stores (as in options) */
 } conv3d_fp8_plan_info;
 
 /*

@@ -176,6 +176,19 @@ def test_describe_bf16_twin(lib):
     assert d(synth.ConvShape(1, 16, 4, 8, 8, 16))["route"] in (2, 3)
 
 
+def test_describe_tma_epilogue(lib):
+    s0 = synth.CONFIGS[0]
+    assert _describe(s0)["epilogue"] == 1                            # default: explicit stores
+    assert _describe(s0, epilogue=2, route=2)["epilogue"] == 2
+    # not on the padded-grid route, not with dhw % 8 != 0 (3*5*7 = 105)
+    assert capi.conv3d_fp8_describe_status(1, 32, 8, 8, 8, 32, 3, 3, 3, 1, 1, 152, route=3,
+                                           epilogue=2) == capi.CONV3D_EUNSUPPORTED
+    assert capi.conv3d_fp8_describe_status(1, 32, 3, 5, 7, 32, 3, 3, 3, 1, 1, 152, route=2,
+                                           epilogue=2) == capi.CONV3D_EUNSUPPORTED
+    assert capi.conv3d_fp8_describe_status(1, 32, 3, 5, 7, 32, 3, 3, 3, 1, 1, 152,
+                                           epilogue=3) == capi.CONV3D_EINVAL
+
+
 def test_describe_forced_options(lib):
     s = synth.CONFIGS[1]
     i = _describe(s, splits=4, block_n=64, max_ctas=10, cta_pair=1)
