@@ -260,6 +260,7 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
     p.Dg = (int)Dg; p.Hg = (int)Hg; p.Wg = (int)Wg;
     p.x_cl = x_cl ? 1 : 0;
     p.epi_tma = epi_tma ? 1 : 0;
+    p.halo_once = 1;  // a plan zeroes its padded copy once (the allocation-free entry does not)
     p.a_grid_im2col = route == kRouteGrid && x_cl ? 1 : 0;
     p.dhw = (int)dhw;
     p.tiles_per_image = (int)tiles_per_image;
@@ -529,6 +530,12 @@ conv3d_status plan_impl(int elem_bytes, conv3d_fp8_plan_t* out, int N, int C, in
   plan->p.wp = ws + L.wp_off;
   plan->p.partials = L.part_bytes ? reinterpret_cast<float*>(ws + L.part_off) : nullptr;
   plan->p.status = reinterpret_cast<int*>(ws + L.status_off);
+  // the zero halo of the padded copy, once: no run writes it again
+  if (L.xp_bytes && cudaMemset(plan->p.xp, 0, L.xp_bytes) != cudaSuccess) {
+    cudaFree(plan->workspace);
+    delete plan;
+    return CONV3D_ECUDA;
+  }
   // The status word at offset 0 of its 256-byte slot; a bfloat16 plan keeps two fp32 ones at
   // offset 128, the scales its runs pass to the kernels (its inputs carry no scale).
   const float ones[2] = {1.0f, 1.0f};
@@ -859,6 +866,8 @@ extern "C" conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int 
   p.wp = ws + L.wp_off;
   p.partials = L.part_bytes ? reinterpret_cast<float*>(ws + L.part_off) : nullptr;
   p.status = reinterpret_cast<int*>(ws + L.status_off);
+  // the shared scratch holds other problems between calls: the pack writes the halo every run
+  p.halo_once = 0;
   p.x = static_cast<const uint8_t*>(x);
   p.w = static_cast<const uint8_t*>(w);
   p.y = static_cast<uint16_t*>(y);

@@ -51,6 +51,7 @@ struct ConvParams {
   int x_cl;              // the caller's x is channels-last (NDHWC): no transpose in the pack
   int epi_tma;           // whole tiles leave through TMA stores bounded by the map of y (output-
                          // position routes); otherwise explicit guarded stores
+  int halo_once;         // the plan zeroed its padded copy at creation: the pack skips the halo
   int x_src_type;        // kSrcE4m3: x is e4m3 bytes; kSrcF32 / kSrcBf16: the pack quantises x
                          // (NCDHW values) with the device scale *scale_x
   int a_grid_im2col;     // padded-grid route: A by im2col loads from an unpadded channels-last x

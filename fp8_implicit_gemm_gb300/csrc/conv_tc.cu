@@ -334,14 +334,11 @@ cudaError_t launch_conv(const ConvParams& p, const CUtensorMap& wmap, const CUte
   if (p.pair) return launch_conv_pair(p, wmap, xmap, ymap, row_chk, grid, stream);
   const size_t smem = conv_smem_bytes(p.block_n, p.stages, p.epi_tma != 0);
   const bool bf16 = p.elem_bytes == 2;
-  if (row_chk && bf16)
-    conv3d_fp8_tc_kernel<true, true><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, ymap, p);
-  else if (row_chk)
-    conv3d_fp8_tc_kernel<true, false><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, ymap, p);
-  else if (bf16)
-    conv3d_fp8_tc_kernel<false, true><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, ymap, p);
-  else
-    conv3d_fp8_tc_kernel<false, false><<<grid, kNumThreads, smem, stream>>>(wmap, xmap, ymap, p);
+  auto kernel = row_chk ? (bf16 ? conv3d_fp8_tc_kernel<true, true>
+                               : conv3d_fp8_tc_kernel<true, false>)
+                        : (bf16 ? conv3d_fp8_tc_kernel<false, true>
+                               : conv3d_fp8_tc_kernel<false, false>);
+  kernel<<<grid, kNumThreads, smem, stream>>>(wmap, xmap, ymap, p);
   return cudaGetLastError();
 }
 

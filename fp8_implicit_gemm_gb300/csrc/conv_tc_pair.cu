@@ -371,16 +371,15 @@ cudaError_t conv_pair_set_smem_attr(size_t smem_bytes) {
 }
 
 template <bool kBf16>
-void launch_pair_typed(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
-                       const CUtensorMap& ymap, bool row_chk, int grid, size_t smem,
-                       cudaStream_t stream) {
-  const dim3 g(grid), b(kNumThreads);
-  if (p.route == kRouteGrid)  // grid rows that are not outputs always need the row test
-    conv3d_fp8_tc_pair_kernel<true, true, kBf16><<<g, b, smem, stream>>>(wmap, xmap, ymap, p);
-  else if (row_chk)
-    conv3d_fp8_tc_pair_kernel<true, false, kBf16><<<g, b, smem, stream>>>(wmap, xmap, ymap, p);
-  else
-    conv3d_fp8_tc_pair_kernel<false, false, kBf16><<<g, b, smem, stream>>>(wmap, xmap, ymap, p);
+cudaError_t launch_pair_typed(const ConvParams& p, const CUtensorMap& wmap,
+                              const CUtensorMap& xmap, const CUtensorMap& ymap, bool row_chk,
+                              int grid, size_t smem, cudaStream_t stream) {
+  auto kernel = p.route == kRouteGrid  // grid rows that are not outputs always need the row test
+                    ? conv3d_fp8_tc_pair_kernel<true, true, kBf16>
+                    : (row_chk ? conv3d_fp8_tc_pair_kernel<true, false, kBf16>
+                               : conv3d_fp8_tc_pair_kernel<false, false, kBf16>);
+  kernel<<<grid, kNumThreads, smem, stream>>>(wmap, xmap, ymap, p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_conv_pair(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
@@ -388,10 +387,8 @@ cudaError_t launch_conv_pair(const ConvParams& p, const CUtensorMap& wmap, const
                              cudaStream_t stream) {
   const size_t smem = conv_pair_smem_bytes(p);
   if (p.elem_bytes == 2)
-    launch_pair_typed<true>(p, wmap, xmap, ymap, row_chk, grid, smem, stream);
-  else
-    launch_pair_typed<false>(p, wmap, xmap, ymap, row_chk, grid, smem, stream);
-  return cudaGetLastError();
+    return launch_pair_typed<true>(p, wmap, xmap, ymap, row_chk, grid, smem, stream);
+  return launch_pair_typed<false>(p, wmap, xmap, ymap, row_chk, grid, smem, stream);
 }
 
 int conv_pair_max_active_clusters(const ConvParams& p) {

@@ -1,0 +1,327 @@
+// pack_items.cuh -- the items of the operand pack (x NCDHW -> channels-last copy, w KCTRS ->
+// K x taps x C): PackPlan (the index ranges of the work) and pack_item (one item).
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "conv_common.cuh"
+#include "quant.cuh"
+
+namespace c3d {
+
+// Work of the pack kernel, as consecutive index ranges of one grid-stride loop:
+//   [0, x_items)          interior of x: with W % 4 == 0, one item = 16 channels x 4 pixels (16
+//                         aligned 4-byte loads, a byte transpose in registers, four 16-byte
+//                         stores); otherwise one item = 16 channels x 1 pixel (16 byte loads);
+//                         an fp32 or bfloat16 x (x_src_type) is quantised to e4m3 on the way, with
+//                         the device scale *scale_x, in the same items;
+//                         from a channels-last x, one item = one 16-byte chunk copied into the
+//                         padded copy (no items when the TMA routes read that x directly)
+//   + halo_row_items      16-byte zero chunks of the padded rows (d or h in the halo)
+//   + halo_side_items     16-byte zero chunks of the W-halo pixels of interior rows
+//   + w_items             16 channels of one tap of one filter
+// Pixels (or pixel quads) run fastest across threads, so each load of a warp is a contiguous run
+// along W of the NCDHW input.
+struct PackPlan {
+  long long x_items, halo_row_items, halo_side_items, w_items;
+  bool hex;   // e4m3 bytes and W % 16 == 0: 16-pixel items (16-byte loads)
+  bool quad;  // e4m3 and W % 4 == 0: 4-pixel items
+  bool two;   // bfloat16 and W % 2 == 0: 2-pixel items
+  bool copy;  // x is channels-last already: 16-byte chunk copies
+};
+
+__host__ __device__ inline PackPlan pack_plan(const ConvParams& p) {
+  PackPlan q;
+  const long long cq = p.C / 16;
+  q.copy = p.x_cl != 0;
+  q.quad = !q.copy && p.elem_bytes == 1 && (p.W % 4) == 0;
+  q.hex = q.quad && p.x_src_type == kSrcE4m3 && (p.W % 16) == 0;
+  q.two = !q.copy && p.elem_bytes == 2 && (p.W % 2) == 0;
+  const int per_row = q.hex ? p.W / 16 : q.quad ? p.W / 4 : (q.two ? p.W / 2 : p.W);
+  q.x_items = p.xp == nullptr ? 0 : (long long)p.N * p.D * p.H * cq * per_row;
+  const long long halo_rows_per_image = (long long)p.Dp * p.Hp - (long long)p.D * p.H;
+  q.halo_row_items = (long long)p.N * halo_rows_per_image * p.Wp * cq;
+  q.halo_side_items = (long long)p.N * p.D * p.H * (p.Wp - p.W) * cq;
+  q.w_items = (long long)p.K * p.taps * cq;
+  if (p.halo_once) {  // the plan zeroed its padded copy once: the halo is never written again
+    q.halo_row_items = 0;
+    q.halo_side_items = 0;
+  }
+  return q;
+}
+
+// Byte transpose of a 4x4 block: v[c] holds pixels 0..3 of channel c; o[j] gets channels 0..3 of
+// pixel j.
+__device__ __forceinline__ void transpose4x4(const uint32_t v[4], uint32_t o[4]) {
+  const uint32_t t0 = __byte_perm(v[0], v[1], 0x5140), t1 = __byte_perm(v[2], v[3], 0x5140);
+  const uint32_t t2 = __byte_perm(v[0], v[1], 0x7362), t3 = __byte_perm(v[2], v[3], 0x7362);
+  o[0] = __byte_perm(t0, t1, 0x5410);
+  o[1] = __byte_perm(t0, t1, 0x7632);
+  o[2] = __byte_perm(t2, t3, 0x5410);
+  o[3] = __byte_perm(t2, t3, 0x7632);
+}
+
+// Per-thread constants of the item loop.
+struct PackCtx {
+  long long e1, e2, e3;  // ends of the interior, halo-row and halo-side ranges
+  int cq_n;              // 16-byte chunks per pixel
+  long long plane;       // D * H * W
+  float qs;              // scale that quantises an fp32 / bfloat16 x (1 otherwise)
+};
+
+__device__ __forceinline__ PackCtx pack_ctx(const ConvParams& p, const PackPlan& q) {
+  PackCtx c;
+  c.e1 = q.x_items;
+  c.e2 = c.e1 + q.halo_row_items;
+  c.e3 = c.e2 + q.halo_side_items;
+  c.cq_n = p.C >> 4;
+  c.plane = (long long)p.D * p.H * p.W;
+  c.qs = p.x_src_type != kSrcE4m3 ? __ldg(p.scale_x) : 1.0f;
+  return c;
+}
+
+// Item g of the pack (g < e3 + w_items).
+__device__ __forceinline__ void pack_item(const ConvParams& p, const PackPlan& q,
+                                          const PackCtx& c, long long g) {
+  const long long e1 = c.e1, e2 = c.e2, e3 = c.e3;
+  const int cq_n = c.cq_n;
+  const long long plane = c.plane;
+  const float qs = c.qs;
+  if (g < e1 && q.copy) {
+    // interior from a channels-last x: (chunk fastest, then pixel)
+    const long long pix = g / cq_n;  // ((n*D + d)*H + h)*W + w
+    const int cq = (int)(g - pix * cq_n);
+    const int w = (int)(pix % p.W);
+    const long long row = pix / p.W;
+    const int h = (int)(row % p.H);
+    const int d = (int)((row / p.H) % p.D);
+    const int n = (int)(row / ((long long)p.H * p.D));
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(p.x + pix * p.C + cq * 16));
+    *reinterpret_cast<uint4*>(
+        p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) * p.Wp + w + p.pk_pw) *
+                   p.C + cq * 16) = v;
+  } else if (g < e1 && p.x_src_type != kSrcE4m3) {
+    // interior, quantised from fp32 / bfloat16 values: as the e4m3 items below, each channel's
+    // 4 (or 1) pixels quantised into one 32-bit word (or byte) before the byte transpose
+    const int per_row = q.quad ? p.W / 4 : p.W;
+    const int wi = (int)(g % per_row);
+    const long long rest = g / per_row;
+    const int cq = (int)(rest % cq_n);
+    const long long row = rest / cq_n;  // n*D*H + d*H + h
+    const int h = (int)(row % p.H);
+    const int d = (int)((row / p.H) % p.D);
+    const int n = (int)(row / ((long long)p.H * p.D));
+    const long long el0 = ((long long)n * p.C + cq * 16) * plane + ((long long)d * p.H + h) * p.W;
+    uint8_t* dst_row = p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) *
+                                   p.Wp + p.pk_pw) * p.C + cq * 16;
+    if (q.quad) {
+      uint32_t v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const long long e = el0 + j * plane + 4 * wi;
+        float a[4];
+        if (p.x_src_type == kSrcF32) {
+          const float4 f = __ldg(reinterpret_cast<const float4*>(p.x) + e / 4);
+          a[0] = f.x; a[1] = f.y; a[2] = f.z; a[3] = f.w;
+        } else {
+          const uint2 u = __ldg(reinterpret_cast<const uint2*>(p.x) + e / 4);
+          a[0] = __uint_as_float(u.x << 16);
+          a[1] = __uint_as_float(u.x & 0xFFFF0000u);
+          a[2] = __uint_as_float(u.y << 16);
+          a[3] = __uint_as_float(u.y & 0xFFFF0000u);
+        }
+        v[j] = quant4(a[0], a[1], a[2], a[3], qs);
+      }
+      uint32_t o[4][4];  // o[pixel][word of 4 channels]
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        uint32_t t[4];
+        transpose4x4(v + 4 * b, t);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j][b] = t[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(dst_row + (long long)(4 * wi + j) * p.C) =
+            make_uint4(o[j][0], o[j][1], o[j][2], o[j][3]);
+    } else {
+      uint32_t v[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float a = src_value(p.x, p.x_src_type, el0 + j * plane + wi);
+        v[j >> 2] |= (quant4(a, 0.0f, 0.0f, 0.0f, qs) & 0xFFu) << ((j & 3) * 8);
+      }
+      *reinterpret_cast<uint4*>(dst_row + (long long)wi * p.C) = make_uint4(v[0], v[1], v[2], v[3]);
+    }
+  } else if (g < e1 && p.elem_bytes == 2) {
+    // interior, bfloat16: one item = 8 channels (one 16-byte chunk) x 2 pixels (or 1 when W is
+    // odd); pixels fastest, then chunk, then (n, d, h) row
+    const int per_row = q.two ? p.W / 2 : p.W;
+    const int wi = (int)(g % per_row);
+    const long long rest = g / per_row;
+    const int cq = (int)(rest % cq_n);
+    const long long row = rest / cq_n;  // n*D*H + d*H + h
+    const int h = (int)(row % p.H);
+    const int d = (int)((row / p.H) % p.D);
+    const int n = (int)(row / ((long long)p.H * p.D));
+    const int c_el = p.C >> 1;
+    const uint16_t* src = reinterpret_cast<const uint16_t*>(p.x) +
+                          ((long long)n * c_el + cq * 8) * plane + ((long long)d * p.H + h) * p.W;
+    uint8_t* dst_row = p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) *
+                                   p.Wp + p.pk_pw) * p.C + cq * 16;
+    if (q.two) {
+      uint32_t v[8];  // v[c]: pixels 2wi (low half) and 2wi+1 (high half) of channel c
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        v[j] = __ldg(reinterpret_cast<const uint32_t*>(src + j * plane) + wi);
+      uint32_t lo[4], hi[4];  // channel pairs (2k, 2k+1) of pixel 2wi and of pixel 2wi+1
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        lo[k] = __byte_perm(v[2 * k], v[2 * k + 1], 0x5410);
+        hi[k] = __byte_perm(v[2 * k], v[2 * k + 1], 0x7632);
+      }
+      *reinterpret_cast<uint4*>(dst_row + (long long)(2 * wi) * p.C) =
+          make_uint4(lo[0], lo[1], lo[2], lo[3]);
+      *reinterpret_cast<uint4*>(dst_row + (long long)(2 * wi + 1) * p.C) =
+          make_uint4(hi[0], hi[1], hi[2], hi[3]);
+    } else {
+      uint32_t v[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        v[k] = (uint32_t)__ldg(src + (2 * k) * plane + wi) |
+               ((uint32_t)__ldg(src + (2 * k + 1) * plane + wi) << 16);
+      *reinterpret_cast<uint4*>(dst_row + (long long)wi * p.C) = make_uint4(v[0], v[1], v[2], v[3]);
+    }
+  } else if (g < e1) {
+    // interior: (pixel group fastest, then channel chunk, then (n, d, h) row)
+    const int per_row = q.hex ? p.W / 16 : q.quad ? p.W / 4 : p.W;
+    const int wi = (int)(g % per_row);
+    const long long rest = g / per_row;
+    const int cq = (int)(rest % cq_n);
+    const long long row = rest / cq_n;  // n*D*H + d*H + h
+    const int h = (int)(row % p.H);
+    const int d = (int)((row / p.H) % p.D);
+    const int n = (int)(row / ((long long)p.H * p.D));
+    const uint8_t* src = p.x + ((long long)n * p.C + cq * 16) * plane +
+                         ((long long)d * p.H + h) * p.W;
+    uint8_t* dst_row = p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) *
+                                   p.Wp + p.pk_pw) * p.C + cq * 16;
+    if (q.hex) {
+      // 16 channels x 16 pixels: one 16-byte load per channel, then four 4-pixel groups through
+      // the same 4x4 byte transposes as the quad items
+      uint4 u[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        u[j] = __ldg(reinterpret_cast<const uint4*>(src + j * plane) + wi);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          v[j] = k == 0 ? u[j].x : k == 1 ? u[j].y : k == 2 ? u[j].z : u[j].w;
+        uint32_t o[4][4];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          uint32_t t[4];
+          transpose4x4(v + 4 * b, t);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) o[j][b] = t[j];
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(dst_row + (long long)(16 * wi + 4 * k + j) * p.C) =
+              make_uint4(o[j][0], o[j][1], o[j][2], o[j][3]);
+      }
+    } else if (q.quad) {
+      uint32_t v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        v[j] = __ldg(reinterpret_cast<const uint32_t*>(src + j * plane) + wi);
+      uint32_t o[4][4];  // o[pixel][word of 4 channels]
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        uint32_t t[4];
+        transpose4x4(v + 4 * b, t);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j][b] = t[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4*>(dst_row + (long long)(4 * wi + j) * p.C) =
+            make_uint4(o[j][0], o[j][1], o[j][2], o[j][3]);
+    } else {
+      uint32_t v[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        v[j >> 2] |= (uint32_t)__ldg(src + j * plane + wi) << ((j & 3) * 8);
+      *reinterpret_cast<uint4*>(dst_row + (long long)wi * p.C) = make_uint4(v[0], v[1], v[2], v[3]);
+    }
+  } else if (g < e2) {
+    // zero chunks of a halo row: halo planes first, then the halo rows of interior planes
+    const long long gi = g - e1;
+    const long long per_row = (long long)p.Wp * cq_n;
+    const long long r = (gi / per_row);
+    const long long chunk = gi - r * per_row;
+    const long long halo_rows_per_image = (long long)p.Dp * p.Hp - (long long)p.D * p.H;
+    const int n = (int)(r / halo_rows_per_image);
+    long long rr = r - (long long)n * halo_rows_per_image;
+    const long long front = (long long)p.pk_pd * p.Hp;
+    int dp, hp;
+    if (rr < front) {
+      dp = (int)(rr / p.Hp);
+      hp = (int)(rr % p.Hp);
+    } else if (rr < 2 * front) {
+      rr -= front;
+      dp = p.pk_pd + p.D + (int)(rr / p.Hp);
+      hp = (int)(rr % p.Hp);
+    } else {
+      rr -= 2 * front;
+      const int side = 2 * p.pk_ph;
+      const int kk = (int)(rr % side);
+      dp = p.pk_pd + (int)(rr / side);
+      hp = kk < p.pk_ph ? kk : p.H + kk;
+    }
+    *reinterpret_cast<uint4*>(p.xp + (((long long)n * p.Dp + dp) * p.Hp + hp) * p.Wp * p.C +
+                              chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
+  } else if (g < e3) {
+    // zero chunks of the W-halo pixels of interior rows
+    const long long gi = g - e2;
+    const int side = p.Wp - p.W;
+    const long long per_row = (long long)side * cq_n;
+    const long long row = gi / per_row;  // n*D*H + d*H + h
+    const long long rem = gi - row * per_row;
+    const int kk = (int)(rem / cq_n);
+    const int cq = (int)(rem - (long long)kk * cq_n);
+    const int wp = kk < p.pk_pw ? kk : p.W + kk;
+    const int h = (int)(row % p.H);
+    const int d = (int)((row / p.H) % p.D);
+    const int n = (int)(row / ((long long)p.H * p.D));
+    *reinterpret_cast<uint4*>(
+        p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) * p.Wp + wp) * p.C +
+        cq * 16) = make_uint4(0u, 0u, 0u, 0u);
+  } else {
+    // weights: one item = one 16-byte chunk (16 e4m3 or 8 bfloat16 channels) of one tap
+    const long long gw = g - e3;
+    const int tap = (int)(gw % p.taps);
+    const long long rest = gw / p.taps;
+    const int cq = (int)(rest % cq_n);
+    const int k = (int)(rest / cq_n);
+    uint32_t v[4] = {0u, 0u, 0u, 0u};
+    if (p.elem_bytes == 2) {
+      const uint16_t* src = reinterpret_cast<const uint16_t*>(p.w) +
+                            ((long long)k * (p.C >> 1) + cq * 8) * p.taps + tap;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j >> 1] |= (uint32_t)__ldg(src + j * p.taps) << ((j & 1) * 16);
+    } else {
+      const uint8_t* src = p.w + ((long long)k * p.C + cq * 16) * p.taps + tap;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        v[j >> 2] |= (uint32_t)__ldg(src + j * p.taps) << ((j & 3) * 8);
+    }
+    uint4* dst =
+        reinterpret_cast<uint4*>(p.wp + ((long long)k * p.taps + tap) * p.C + cq * 16);
+    *dst = make_uint4(v[0], v[1], v[2], v[3]);
+  }
+}
+
+}  // namespace c3d
