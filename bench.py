@@ -341,23 +341,32 @@ def run_ours(args):
     time.sleep(0.3)
     dist.barrier()
     torch.cuda.synchronize()
+    # The steps are timed as a user runs them: CUDA events on the stream around each step only. The
+    # library's own events around the implicit GEMM (the roofline's kernel time) sit between its
+    # kernels and hold back their programmatic dependent launches, so they are recorded in a
+    # second timed pass of the same steps.
     t_wall0 = time.perf_counter()
     for i in range(K):
         flush.fill_(i & 0xFF)
-        s0, s1, k0, k1 = ev[i]
-        capi.conv3d_fp8_set_timing_events(plan, k0, k1)
+        s0, s1, _, _ = ev[i]
         s0.record(stream)
         step()
         s1.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
     t_wall = time.perf_counter() - t_wall0
+    K2 = min(K, 500)  # kernel-time pass
+    for i in range(K2):
+        flush.fill_(i & 0xFF)
+        capi.conv3d_fp8_set_timing_events(plan, ev[i][2], ev[i][3])
+        step()
+    torch.cuda.synchronize()
     sampler.stop()
     capi.conv3d_fp8_set_timing_events(plan, None, None)
     if capi.conv3d_fp8_check(plan) != capi.CONV3D_OK:
         raise RuntimeError("a kernel reported a timed-out wait")
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    kern_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    kern_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K2)]
     total_ms = dist.max(sum(step_ms), dev)
     mean_step_ms = total_ms / K
     mean_kern_ms = statistics.mean(kern_ms)
@@ -424,6 +433,8 @@ def run_ours(args):
         # the timed window then also holds the reduction of the tiles split along K
         roof["kernel"] += " + splitk_reduce_kernel"
     roof["kernel_ms"] = round(mean_kern_ms, 5)
+    roof["kernel_timing"] = (f"library events around the GEMM (+ reduce) on the launching stream, "
+                             f"{K2} steps after the {K} timed ones")
     roof["alg_flop"] = fig["flop"]
     roof["alg_bytes"] = fig["alg_bytes"]
     roof["step_roofline_frac"] = round(max(t_flop, t_hbm) / (mean_step_ms * 1e-3), 4)

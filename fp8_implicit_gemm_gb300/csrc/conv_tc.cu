@@ -89,6 +89,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait_primary();        // the pack's output (launched dependent on it), complete and visible
+  pdl_launch_dependents();   // the reduction of split tiles may be scheduled
   const AbortState ab{abort_flag, p.status, p.timeout_ns};
   const bool im2col = p.route == kRouteIm2col;
 
@@ -338,8 +340,18 @@ cudaError_t launch_conv(const ConvParams& p, const CUtensorMap& wmap, const CUte
                                : conv3d_fp8_tc_kernel<true, false>)
                         : (bf16 ? conv3d_fp8_tc_kernel<false, true>
                                : conv3d_fp8_tc_kernel<false, false>);
-  kernel<<<grid, kNumThreads, smem, stream>>>(wmap, xmap, ymap, p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the prologue overlaps the tail of the pack kernel before it
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kNumThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, wmap, xmap, ymap, p);
 }
 
 }  // namespace c3d

@@ -115,6 +115,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
   cluster_sync();  // both CTAs' barriers exist before anyone signals across the pair
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait_primary();        // the pack's output (launched dependent on it), complete and visible
+  pdl_launch_dependents();   // the reduction of split tiles may be scheduled
   const AbortState ab{abort_flag, p.status, p.timeout_ns};
   const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
   const int row_base = (int)rank * kBlockM;  // this CTA's rows within the 256-row unit
@@ -378,8 +380,18 @@ cudaError_t launch_pair_typed(const ConvParams& p, const CUtensorMap& wmap,
                     ? conv3d_fp8_tc_pair_kernel<true, true, kBf16>
                     : (row_chk ? conv3d_fp8_tc_pair_kernel<true, false, kBf16>
                                : conv3d_fp8_tc_pair_kernel<false, false, kBf16>);
-  kernel<<<grid, kNumThreads, smem, stream>>>(wmap, xmap, ymap, p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the prologue overlaps the tail of the pack kernel before it
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kNumThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, wmap, xmap, ymap, p);
 }
 
 cudaError_t launch_conv_pair(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,

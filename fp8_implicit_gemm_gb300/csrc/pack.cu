@@ -15,6 +15,7 @@
 namespace c3d {
 
 __global__ void __launch_bounds__(256) pack_kernel(ConvParams p, PackPlan q) {
+  pdl_launch_dependents();  // the implicit GEMM may start its prologue while the pack runs
   const PackCtx c = pack_ctx(p, q);
   const long long total = c.e3 + q.w_items;
   for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < total;
@@ -44,6 +45,7 @@ template <bool kRowChk>
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(ConvParams p) {
   const long long per_tile = (long long)p.block_n * p.block_m;
   const long long total = ((long long)p.m_tiles * p.n_tiles - p.full_tiles) * per_tile;
+  pdl_wait_primary();  // the partials of the implicit GEMM, complete and visible
   const float scale = __ldg(p.scale_x) * __ldg(p.scale_w);
   for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < total;
        g += (long long)gridDim.x * blockDim.x) {
@@ -84,11 +86,17 @@ cudaError_t launch_splitk_reduce(const ConvParams& p, bool row_chk, cudaStream_t
   long long blocks = (total + 255) / 256;
   const long long cap = (long long)sms * 16;
   if (blocks > cap) blocks = cap;
-  if (row_chk)
-    splitk_reduce_kernel<true><<<(unsigned)blocks, 256, 0, stream>>>(p);
-  else
-    splitk_reduce_kernel<false><<<(unsigned)blocks, 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return row_chk ? cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<true>, p)
+                 : cudaLaunchKernelEx(&cfg, splitk_reduce_kernel<false>, p);
 }
 
 }  // namespace c3d

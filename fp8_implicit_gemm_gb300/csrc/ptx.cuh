@@ -163,6 +163,17 @@ __device__ __forceinline__ void bulk_wait_group_read() {
 __device__ __forceinline__ void bulk_wait_group_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Programmatic dependent launch: the next kernel of the stream (launched with programmatic
+// stream serialisation) may be scheduled once every CTA of this grid has signalled; it runs up to
+// its griddepcontrol.wait, which returns when this grid has completed and its memory is visible.
+// Both are no-ops for kernels launched without the attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_primary() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Named barrier `id` over `count` threads (a multiple of 32).
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
