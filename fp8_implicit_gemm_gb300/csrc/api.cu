@@ -178,14 +178,15 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
   const long long tiles = m_tiles * n_tiles;
   long long splits = o.splits;
   if (splits < 0) return CONV3D_EINVAL;
-  // Tiles 0..full_tiles-1 are computed whole; the rest are split along K. By default: with fewer
-  // than half as many tiles as slots, every tile is split to fill the machine; with more tiles
+  // Tiles 0..full_tiles-1 are computed whole; the rest are split along K. By default: with at most
+  // a quarter as many tiles as slots, every tile is split to fill the machine (with more tiles
+  // the reduction of the partials costs more than the shorter K loops save); with more tiles
   // than slots, only the tiles of a last, mostly idle wave are split, over the slots that wave
   // would leave idle. A split count in the options splits every tile that many ways.
   long long full_tiles = 0;
   if (splits == 0) {
     splits = 1;
-    if (tiles * 2 <= slots && k_blocks >= 8) {
+    if (tiles * 4 <= slots && k_blocks >= 8) {
       splits = std::max<long long>(1, std::min<long long>(slots / tiles, k_blocks / 4));
     } else if (tiles > slots && k_blocks >= 4) {
       const long long tail = tiles % slots;
