@@ -204,6 +204,12 @@ def test_describe_forced_options(lib):
     ((1, 16, 4, 4, 4, 16, 3, 3, 3, 0, 1), capi.CONV3D_EINVAL),    # stride 0
     ((1, 16, 4, 4, 4, 16, 3, 3, 3, 1, -1), capi.CONV3D_EINVAL),   # negative pad
     ((1, 24, 4, 4, 4, 16, 3, 3, 3, 1, 1), capi.CONV3D_EUNSUPPORTED),  # C % 16 != 0
+    ((1, 16, 4, 4, 4, 0, 3, 3, 3, 1, 1), capi.CONV3D_EINVAL),     # K = 0
+    ((1, 16, 4, 4, 4, 16, 0, 3, 3, 1, 1), capi.CONV3D_EINVAL),    # empty filter
+    # index ranges beyond 32 bits: npq = 2^31 rows, and 2^40 bytes of y
+    ((2048, 16, 1024, 1024, 1, 16, 1, 1, 1, 1, 0), capi.CONV3D_EUNSUPPORTED),
+    ((1, 16, 1024, 1024, 1024, 1 << 20, 1, 1, 1, 1, 0), capi.CONV3D_EUNSUPPORTED),
+    ((1, 1 << 28, 1, 1, 1, 16, 1, 1, 1, 1, 0), capi.CONV3D_EUNSUPPORTED),  # C * elem overflow guard
 ])
 def test_describe_validation(lib, args, code):
     N, C, D, H, W, K, T, R, S, st, pd = args
