@@ -241,7 +241,9 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs the loop and waits on the barriers; one elected lane issues the MMAs of
+    // a stage together with the commits that track them.
+    {
       const uint32_t idesc = make_idesc<kBf16>(kBlockM, (uint32_t)p.block_n);
       // A rows are 128 bytes (SW128) on the gather route, a_cb bytes on the im2col route. K step
       // j covers bytes [32j, 32j+32) of the 128-byte K block: in A it lies in sub-tile 32j / a_cb
@@ -264,42 +266,49 @@ __global__ void __launch_bounds__(kNumThreads, 1)
       for (int u = blockIdx.x; u < p.num_units && !aborted; u += gridDim.x, ++tc) {
         const Unit un = decode_unit(p, u);
         const int buf = tc & 1;
-        if (!wait_bounded(accEmpty(buf), ((tc >> 1) & 1) ^ 1, ab, kStatusWaitAccEmpty)) break;
+        if (!wait_bounded_warp(accEmpty(buf), ((tc >> 1) & 1) ^ 1, ab, kStatusWaitAccEmpty))
+          break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)buf * p.acc_stride;
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
           const int stage = ring.stage;
           const uint32_t ph = ring.phase;
-          if ((!im2col && !wait_bounded(fullA(stage), ph, ab, kStatusWaitFull)) ||
-              !wait_bounded(fullB(stage), ph, ab, kStatusWaitFull)) {
+          if ((!im2col && !wait_bounded_warp(fullA(stage), ph, ab, kStatusWaitFull)) ||
+              !wait_bounded_warp(fullB(stage), ph, ab, kStatusWaitFull)) {
             aborted = true;
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = adesc0 + (uint64_t)((uint32_t)stage * a_stage16);
-          const uint64_t bdesc = bdesc0 + (uint64_t)((uint32_t)stage * b_stage16);
-          const uint32_t acc0 = kb > un.kb0 ? 1u : 0u;
-          const int rem = p.kg - kb * kBlockK;
-          if (rem >= kBlockK) {
-            mma_cta<kBf16>(d_tmem, adesc + a_step[0], bdesc, idesc, acc0);
-            mma_cta<kBf16>(d_tmem, adesc + a_step[1], bdesc + 2u, idesc, 1u);
-            mma_cta<kBf16>(d_tmem, adesc + a_step[2], bdesc + 4u, idesc, 1u);
-            mma_cta<kBf16>(d_tmem, adesc + a_step[3], bdesc + 6u, idesc, 1u);
-          } else {
-            const int nsteps = (rem + kMmaK - 1) / kMmaK;
+          if (elect_one()) {
+            const uint64_t adesc = adesc0 + (uint64_t)((uint32_t)stage * a_stage16);
+            const uint64_t bdesc = bdesc0 + (uint64_t)((uint32_t)stage * b_stage16);
+            const uint32_t acc0 = kb > un.kb0 ? 1u : 0u;
+            const int rem = p.kg - kb * kBlockK;
+            if (rem >= kBlockK) {
+              mma_cta<kBf16>(d_tmem, adesc + a_step[0], bdesc, idesc, acc0);
+              mma_cta<kBf16>(d_tmem, adesc + a_step[1], bdesc + 2u, idesc, 1u);
+              mma_cta<kBf16>(d_tmem, adesc + a_step[2], bdesc + 4u, idesc, 1u);
+              mma_cta<kBf16>(d_tmem, adesc + a_step[3], bdesc + 6u, idesc, 1u);
+            } else {
+              const int nsteps = (rem + kMmaK - 1) / kMmaK;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (j < nsteps)
-                mma_cta<kBf16>(d_tmem, adesc + a_step[j], bdesc + 2u * j, idesc, j > 0 ? 1u : acc0);
+              for (int j = 0; j < 4; ++j)
+                if (j < nsteps)
+                  mma_cta<kBf16>(d_tmem, adesc + a_step[j], bdesc + 2u * j, idesc,
+                                 j > 0 ? 1u : acc0);
+            }
+            mma_commit(empty(stage));
+            if (kb + 1 == un.kb1) mma_commit(accFull(buf));  // the unit's last stage
           }
-          mma_commit(empty(stage));
+          __syncwarp();
           ring.next(S);
         }
         if (aborted) break;
-        mma_commit(accFull(buf));
       }
-      // Every MMA must be complete before TMEM is released.
-      mma_commit(drain_bar);
+      // Every MMA must be complete before TMEM is released (elect.sync picks the same lane of a
+      // converged warp each time, the lane that issued them).
+      if (elect_one()) mma_commit(drain_bar);
+      __syncwarp();
       wait_drain(drain_bar, 0, p.timeout_ns, p.status, kStatusWaitDrain);
     }
     __syncwarp();

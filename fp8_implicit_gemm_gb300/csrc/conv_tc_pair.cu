@@ -252,7 +252,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     __syncwarp();
   } else if (warp == 9) {
     // ------------------------------------------------------------------------------ MMA issuer
-    if (lane == 0 && leader) {
+    // The whole warp runs the loop and waits on the barriers; one elected lane issues the MMAs of
+    // a stage together with the commits that track them.
+    if (leader) {
       const uint32_t idesc = make_idesc<kBf16>(2 * kBlockM, (uint32_t)p.block_n);
       const uint32_t a_cb = (uint32_t)p.a_cb;
       const uint32_t a_layout =
@@ -276,67 +278,73 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
       for (int u = cluster_id; u < p.num_units && !aborted; u += num_clusters, ++tc) {
         const Unit un = decode_unit(p, u);
         const int buf = tc & 1;
-        if (!wait_bounded<true>(accEmpty(buf), ((tc >> 1) & 1) ^ 1, ab, kStatusWaitAccEmpty))
+        if (!wait_bounded_warp<true>(accEmpty(buf), ((tc >> 1) & 1) ^ 1, ab,
+                                     kStatusWaitAccEmpty))
           break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)buf * p.acc_stride;
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
           const int stage = ring.stage;
-          if (!wait_bounded<true>(full(stage), ring.phase, ab, kStatusWaitFull)) {
+          if (!wait_bounded_warp<true>(full(stage), ring.phase, ab, kStatusWaitFull)) {
             aborted = true;
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = adesc0 + (uint64_t)((uint32_t)stage * a_stage16);
-          const uint32_t acc0 = kb > un.kb0 ? 1u : 0u;
-          if (kGrid) {
-            // The issuing thread must keep pace with the tensor pipe (one N=256 MMA per 128
-            // cycles): per tap, the K steps go out as straight-line code with constant descriptor
-            // offsets, and the per-tap offsets advance by one add each.
-            uint64_t a_tap = adesc;
-            uint64_t b_tap = bdesc_g0 + (uint64_t)((uint32_t)stage * b_stage16);
-            uint32_t acc = acc0;
-            for (int ss = 0; ss < p.S; ++ss) {
-              if (steps_cb == 4) {
-                mma_pair<kBf16>(d_tmem, a_tap, b_tap, idesc, acc);
-                mma_pair<kBf16>(d_tmem, a_tap + 2u, b_tap + 2u, idesc, 1u);
-                mma_pair<kBf16>(d_tmem, a_tap + 4u, b_tap + 4u, idesc, 1u);
-                mma_pair<kBf16>(d_tmem, a_tap + 6u, b_tap + 6u, idesc, 1u);
-              } else if (steps_cb == 2) {
-                mma_pair<kBf16>(d_tmem, a_tap, b_tap, idesc, acc);
-                mma_pair<kBf16>(d_tmem, a_tap + 2u, b_tap + 2u, idesc, 1u);
-              } else {
-                mma_pair<kBf16>(d_tmem, a_tap, b_tap, idesc, acc);
+          if (elect_one()) {
+            const uint64_t adesc = adesc0 + (uint64_t)((uint32_t)stage * a_stage16);
+            const uint32_t acc0 = kb > un.kb0 ? 1u : 0u;
+            if (kGrid) {
+              // The issuing thread must keep pace with the tensor pipe (one N=256 MMA per 128
+              // cycles): per tap, the K steps go out as straight-line code with constant descriptor
+              // offsets, and the per-tap offsets advance by one add each.
+              uint64_t a_tap = adesc;
+              uint64_t b_tap = bdesc_g0 + (uint64_t)((uint32_t)stage * b_stage16);
+              uint32_t acc = acc0;
+              for (int ss = 0; ss < p.S; ++ss) {
+                if (steps_cb == 4) {
+                  mma_pair<kBf16>(d_tmem, a_tap, b_tap, idesc, acc);
+                  mma_pair<kBf16>(d_tmem, a_tap + 2u, b_tap + 2u, idesc, 1u);
+                  mma_pair<kBf16>(d_tmem, a_tap + 4u, b_tap + 4u, idesc, 1u);
+                  mma_pair<kBf16>(d_tmem, a_tap + 6u, b_tap + 6u, idesc, 1u);
+                } else if (steps_cb == 2) {
+                  mma_pair<kBf16>(d_tmem, a_tap, b_tap, idesc, acc);
+                  mma_pair<kBf16>(d_tmem, a_tap + 2u, b_tap + 2u, idesc, 1u);
+                } else {
+                  mma_pair<kBf16>(d_tmem, a_tap, b_tap, idesc, acc);
+                }
+                acc = 1u;
+                a_tap += a_row16;
+                b_tap += b_tap16;
               }
-              acc = 1u;
-              a_tap += a_row16;
-              b_tap += b_tap16;
-            }
-          } else {
-            const uint64_t bdesc = bdesc0 + (uint64_t)((uint32_t)stage * b_stage16);
-            const int rem = p.kg - kb * kBlockK;
-            if (rem >= kBlockK) {
-              mma_pair<kBf16>(d_tmem, adesc + a_step[0], bdesc, idesc, acc0);
-              mma_pair<kBf16>(d_tmem, adesc + a_step[1], bdesc + 2u, idesc, 1u);
-              mma_pair<kBf16>(d_tmem, adesc + a_step[2], bdesc + 4u, idesc, 1u);
-              mma_pair<kBf16>(d_tmem, adesc + a_step[3], bdesc + 6u, idesc, 1u);
             } else {
-              const int nsteps = (rem + kMmaK - 1) / kMmaK;
+              const uint64_t bdesc = bdesc0 + (uint64_t)((uint32_t)stage * b_stage16);
+              const int rem = p.kg - kb * kBlockK;
+              if (rem >= kBlockK) {
+                mma_pair<kBf16>(d_tmem, adesc + a_step[0], bdesc, idesc, acc0);
+                mma_pair<kBf16>(d_tmem, adesc + a_step[1], bdesc + 2u, idesc, 1u);
+                mma_pair<kBf16>(d_tmem, adesc + a_step[2], bdesc + 4u, idesc, 1u);
+                mma_pair<kBf16>(d_tmem, adesc + a_step[3], bdesc + 6u, idesc, 1u);
+              } else {
+                const int nsteps = (rem + kMmaK - 1) / kMmaK;
 #pragma unroll
-              for (int j = 0; j < 4; ++j)
-                if (j < nsteps)
-                  mma_pair<kBf16>(d_tmem, adesc + a_step[j], bdesc + 2u * j, idesc,
-                                  j > 0 ? 1u : acc0);
+                for (int j = 0; j < 4; ++j)
+                  if (j < nsteps)
+                    mma_pair<kBf16>(d_tmem, adesc + a_step[j], bdesc + 2u * j, idesc,
+                                    j > 0 ? 1u : acc0);
+              }
             }
+            mma_commit_pair(empty(stage), 0x3);
+            if (kb + 1 == un.kb1) mma_commit_pair(accFull(buf), 0x3);  // the unit's last stage
           }
-          mma_commit_pair(empty(stage), 0x3);
+          __syncwarp();
           ring.next(S);
         }
         if (aborted) break;
-        mma_commit_pair(accFull(buf), 0x3);
       }
-      // Every MMA of the pair must be complete before TMEM is released.
-      mma_commit_pair(drain_bar, 0x1);
+      // Every MMA of the pair must be complete before TMEM is released (elect.sync picks the
+      // same lane of a converged warp each time, the lane that issued them).
+      if (elect_one()) mma_commit_pair(drain_bar, 0x1);
+      __syncwarp();
       wait_drain(drain_bar, 0, p.timeout_ns, p.status, kStatusWaitDrain);
     }
     __syncwarp();

@@ -109,6 +109,29 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
   }
 }
 
+// wait_bounded run by every lane of a converged warp; the warp gets one verdict (false if any
+// lane gave up), so that it stays converged for the elect.sync that follows.
+template <bool kClusterScope = false>
+__device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,
+                                                  const AbortState& ab, int code) {
+  return __all_sync(0xFFFFFFFFu, wait_bounded<kClusterScope>(bar, parity, ab, code));
+}
+
+// True in exactly one lane of a converged warp (elect.sync over all 32 lanes). The tcgen05 issue
+// roles run their loops on the whole warp and issue under this predicate: with the loop on one
+// lane alone, every mbarrier wait between two MMA batches was measured to leave the tensor pipe
+// idle for about 370 cycles (about a third of the time of twelve 256x128x32 pair MMAs), while
+// the warp-wide form keeps the MMAs back to back.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t e;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(e));
+  return e != 0;
+}
+
 // ------------------------------------------------------------------------------------ cp.async
 // 16-byte copy global -> shared, bypassing L1; src_bytes == 0 writes 16 zero bytes and reads
 // nothing.
