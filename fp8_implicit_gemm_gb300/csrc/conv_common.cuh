@@ -101,20 +101,21 @@ __device__ __forceinline__ RowDest row_dest(const ConvParams& p, int m_tile, int
   return r;
 }
 
-// Epilogue of one thread: its accumulator row (TMEM lane) of one unit, `trow` = TMEM address of the
-// row's first column in the current buffer. `row_in_tile` is the row within the unit's block_m
-// rows. A whole tile: y = bf16(acc * scale), stored only if the row is a real output and
-// col < K. A split unit: the raw fp32 row goes to the unit's slice of the partials,
-// [part][block_n][block_m]. kRowChk = false compiles the row test out (every row real).
+// Epilogue of one thread: columns [cc0, cc1) (multiples of 32) of its accumulator row (TMEM lane)
+// of one unit, `trow` = TMEM address of the row's first column in the current buffer.
+// `row_in_tile` is the row within the unit's block_m rows. A whole tile: y = bf16(acc * scale),
+// stored only if the row is a real output and col < K. A split unit: the raw fp32 row goes to the
+// unit's slice of the partials, [part][block_n][block_m]. kRowChk = false compiles the row test
+// out (every row real).
 template <bool kRowChk>
 __device__ __forceinline__ void epilogue_row(const ConvParams& p, const Unit& un, uint32_t trow,
-                                             int row_in_tile, float scale) {
+                                             int row_in_tile, float scale, int cc0, int cc1) {
   const int n0 = un.n_tile * p.block_n;
   if (un.part < 0) {
     const RowDest dst = row_dest(p, un.m_tile, row_in_tile);
     const bool row_ok = !kRowChk || dst.valid;
     uint16_t* ybase = p.y + dst.y_off;
-    for (int cc = 0; cc < p.block_n; cc += 32) {
+    for (int cc = cc0; cc < cc1; cc += 32) {
       if (n0 + cc >= p.K) break;  // warp-uniform
       uint32_t r[32];
       tmem_ld_32x32b_x32(trow + cc, r);
@@ -132,7 +133,7 @@ __device__ __forceinline__ void epilogue_row(const ConvParams& p, const Unit& un
     }
   } else {
     float* dst = p.partials + ((long long)un.part * p.block_n) * p.block_m + row_in_tile;
-    for (int cc = 0; cc < p.block_n; cc += 32) {
+    for (int cc = cc0; cc < cc1; cc += 32) {
       uint32_t r[32];
       tmem_ld_32x32b_x32(trow + cc, r);
       tmem_ld_wait();

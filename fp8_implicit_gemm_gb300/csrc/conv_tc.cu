@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         epilogue_tile_tma(p, un, &ymap, trow, un.m_tile * p.block_m, threadIdx.x, scale, sEpi,
                           chunk);
       else
-        epilogue_row<kRowChk>(p, un, trow, threadIdx.x, scale);
+        epilogue_row<kRowChk>(p, un, trow, threadIdx.x, scale, 0, p.block_n);
       tc_fence_before();
       mbar_arrive(accEmpty(buf));
     }
@@ -191,7 +191,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     }
   } else if (warp == 8) {
     // ------------------------------------------------------------------------------ TMA loader
-    if (lane == 0) {
+    // The whole warp runs the loop and waits on the barriers; one elected lane issues the copies.
+    {
       uint32_t it = 0;
       Ring ring;
       const bool skip_first = (p.debug_flags & 1) != 0;
@@ -206,32 +207,33 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         bool aborted = false;
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
           const int stage = ring.stage;
-          if (!wait_bounded(empty(stage), ring.phase ^ 1u, ab, kStatusWaitEmpty)) {
+          if (!wait_bounded_warp(empty(stage), ring.phase ^ 1u, ab, kStatusWaitEmpty)) {
             aborted = true;
             break;
           }
           const int kk0 = kb * kBlockK;
           const int nsub = im2col ? min(kBlockK, p.kg - kk0) / p.a_cb : 0;
-          const bool skip = skip_first && it == 0;
-          if (!skip) {
+          const bool issue = !(skip_first && it == 0) && elect_one();
+          if (issue) {
             mbar_arrive_expect_tx(fullB(stage), b_bytes + (uint32_t)(nsub * p.a_cb * kBlockM));
             tma_load_2d(sB_u32 + (uint32_t)stage * b_bytes, &wmap, fullB(stage), kk0,
                         un.n_tile * p.block_n);
           }
           const uint32_t a_dst = sA_u32 + (uint32_t)stage * kATileBytes;
           for (int q = 0; q < nsub; ++q) {
-            if (!skip)
+            if (issue)
               tma_load_im2col_5d(a_dst + (uint32_t)(q * kBlockM * p.a_cb), &xmap, fullB(stage),
                                  walk.c, px.w, px.h, px.d, px.n, (uint16_t)walk.s,
                                  (uint16_t)walk.r, (uint16_t)walk.t);
             walk.next(p);
           }
+          __syncwarp();
           ++it;
           ring.next(S);
         }
         if (aborted) break;
       }
-      // Before the CTA may exit, every tile this thread requested must have landed.
+      // Before the CTA may exit, every tile this warp requested must have landed.
       const uint32_t first = it > (uint32_t)S ? it - (uint32_t)S : 0u;
       for (uint32_t j = first; j < it; ++j) {
         if (skip_first && j == 0) continue;

@@ -10,8 +10,10 @@
 //     halves are read from both CTAs' shared memory at the same offsets and each CTA's TMEM
 //     receives its own 128 accumulator rows; tcgen05.commit multicasts the stage-empty and
 //     accumulator-full signals to both CTAs;
-//   - each CTA's epilogue warps drain their own TMEM rows (stores masked on real output rows and
-//     col < K) and release the accumulator on the leader's barrier (256 arrivals).
+//   - each CTA's eight epilogue warps drain their own TMEM rows (stores masked on real output
+//     rows and col < K): warps w and w + 4 read the same 32 TMEM lanes, w < 4 the first half of
+//     the 32-column chunks and w + 4 the rest; all of them release the accumulator on the
+//     leader's barrier (2 x 256 arrivals).
 // Compared with one CTA per 128-row tile, every SM stores and reads only half of the B tile per
 // K block, so shared-memory traffic per MMA cycle drops from 192 to 128 bytes and more stages fit.
 //
@@ -95,7 +97,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accFull(b), 1);
-      mbar_init(accEmpty(b), 2 * 128);
+      mbar_init(accEmpty(b), 2 * 256);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -121,32 +123,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
   const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
   const int row_base = (int)rank * kBlockM;  // this CTA's rows within the 256-row unit
 
-  if (warp < 4) {
+  if (warp < 8) {
     // ------------------------------------------------------------------------------ epilogue
+    // Warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31 (the rows); w < 4 converts the first
+    // half of the tile's 32-column chunks, w >= 4 the rest. The TMA-store epilogue, where the plan
+    // uses it, runs on warps 0-3 alone.
     const float scale = __ldg(p.scale_x) * __ldg(p.scale_w);
+    const int split_cc = ((p.block_n / 32 + 1) / 2) * 32;
+    const int cc0 = warp < 4 ? 0 : split_cc, cc1 = warp < 4 ? split_cc : p.block_n;
+    const int row = threadIdx.x & 127;  // this thread's row among the CTA's 128
     uint32_t tc = 0, chunk = 0;
     for (int u = cluster_id; u < p.num_units; u += num_clusters, ++tc) {
       const Unit un = decode_unit(p, u);
       const int buf = tc & 1;
       bool ok = wait_bounded<true>(accFull(buf), (tc >> 1) & 1, ab, kStatusWaitAccFull);
       // the TMA-store epilogue synchronises its 128 threads: they go on or stop together
-      if (p.epi_tma) ok = named_barrier_and(1, 128, ok);
+      if (p.epi_tma && warp < 4) ok = named_barrier_and(1, 128, ok);
       if (!ok) break;
       tc_fence_after();
       const uint32_t trow =
-          tmem_base + (uint32_t)buf * p.acc_stride + ((uint32_t)(warp * 32) << 16);
-      if (!kGrid && p.epi_tma && un.part < 0)
-        epilogue_tile_tma(p, un, &ymap, trow, un.m_tile * p.block_m + row_base, threadIdx.x,
-                          scale, sEpi, chunk);
-      else
-        epilogue_row<kRowChk>(p, un, trow, row_base + threadIdx.x, scale);
+          tmem_base + (uint32_t)buf * p.acc_stride + ((uint32_t)((warp & 3) * 32) << 16);
+      if (!kGrid && p.epi_tma && un.part < 0) {
+        if (warp < 4)
+          epilogue_tile_tma(p, un, &ymap, trow, un.m_tile * p.block_m + row_base, row, scale,
+                            sEpi, chunk);
+      } else {
+        epilogue_row<kRowChk>(p, un, trow, row_base + row, scale, cc0, cc1);
+      }
       tc_fence_before();
       mbar_arrive_cluster(leader_bars + (accEmpty(buf) - bars_u32));
     }
     if (p.epi_tma && threadIdx.x == 0) bulk_wait_group_all();  // stores done before exit
   } else if (warp == 8) {
     // ------------------------------------------------------------------------------ TMA loader
-    if (lane == 0) {
+    // The whole warp runs the loop and waits on the barriers; one elected lane issues the copies.
+    {
       uint32_t it = 0;
       Ring ring;
       const bool skip_first = (p.debug_flags & 1) != 0;
@@ -181,11 +192,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                                     (uint32_t)(p.S * half_n * p.a_cb));
           for (int g = un.kb0; g < un.kb1; ++g) {
             const int stage = ring.stage;
-            if (!wait_bounded<true>(empty(stage), ring.phase ^ 1u, ab, kStatusWaitEmpty)) {
+            if (!wait_bounded_warp<true>(empty(stage), ring.phase ^ 1u, ab, kStatusWaitEmpty)) {
               aborted = true;
               break;
             }
-            if (!(skip_first && it == 0)) {
+            if (!(skip_first && it == 0) && elect_one()) {
               const uint32_t bar = leader_bars + (full(stage) - bars_u32);
               if (leader) mbar_arrive_expect_tx(full(stage), tx);
               const int c0 = cb * p.a_cb;
@@ -201,6 +212,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
                 tma_load_2d_pair(b_dst + (uint32_t)(ss * half_n * p.a_cb), &wmap, bar,
                                  k_tap0 + ss * p.C, un.n_tile * p.block_n + (int)rank * half_n);
             }
+            __syncwarp();
             if (++cb == ncb) {
               cb = 0;
               if (++tr == p.R) {
@@ -220,15 +232,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
         walk.start(p, un.kb0 * kBlockK);
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
           const int stage = ring.stage;
-          if (!wait_bounded<true>(empty(stage), ring.phase ^ 1u, ab, kStatusWaitEmpty)) {
+          if (!wait_bounded_warp<true>(empty(stage), ring.phase ^ 1u, ab, kStatusWaitEmpty)) {
             aborted = true;
             break;
           }
           const int kk0 = kb * kBlockK;
           const int nsub = min(kBlockK, p.kg - kk0) / p.a_cb;
-          const bool skip = skip_first && it == 0;
+          const bool issue = !(skip_first && it == 0) && elect_one();
           const uint32_t bar = leader_bars + (full(stage) - bars_u32);
-          if (!skip) {
+          if (issue) {
             if (leader)  // arm the stage with the bytes of both CTAs' copies
               mbar_arrive_expect_tx(full(stage),
                                     2u * (b_bytes + (uint32_t)(nsub * p.a_cb * kBlockM)));
@@ -237,12 +249,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
           }
           const uint32_t a_dst = sA_u32 + (uint32_t)stage * a_bytes;
           for (int q = 0; q < nsub; ++q) {
-            if (!skip)
+            if (issue)
               tma_load_im2col_5d_pair(a_dst + (uint32_t)(q * kBlockM * p.a_cb), &xmap, bar,
                                       walk.c, px.w, px.h, px.d, px.n, (uint16_t)walk.s,
                                       (uint16_t)walk.r, (uint16_t)walk.t);
             walk.next(p);
           }
+          __syncwarp();
           ++it;
           ring.next(S);
         }
