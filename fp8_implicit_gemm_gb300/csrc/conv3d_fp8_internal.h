@@ -11,9 +11,7 @@ constexpr int kBlockM = 128;        // rows (output positions) per tile = TMEM l
 constexpr int kBlockK = 128;        // K_gemm bytes per pipeline stage (= one 128-byte swizzle row)
 constexpr int kMmaK = 32;           // K of one tcgen05.mma kind::f8f6f4
 constexpr int kATileBytes = kBlockM * kBlockK;  // 16 KB
-// 10 warps: epilogue (0-3), A gather loaders of the one-CTA kernel or more epilogue on the
-// CTA-pair kernel (4-7), TMA (8), MMA (9)
-constexpr int kNumThreads = 320;
+constexpr int kNumThreads = 320;    // 4 epilogue warps, 4 A-loader warps, 1 TMA warp, 1 MMA warp
 constexpr int kSmemBudget = 200 * 1024;
 constexpr int kMaxStages = 8;
 constexpr int kEpiStageBytes = 2 * 32 * kBlockM * 2;  // two bf16 boxes [32 columns][128 rows]

@@ -10,10 +10,10 @@
 //     halves are read from both CTAs' shared memory at the same offsets and each CTA's TMEM
 //     receives its own 128 accumulator rows; tcgen05.commit multicasts the stage-empty and
 //     accumulator-full signals to both CTAs;
-//   - each CTA's eight epilogue warps drain their own TMEM rows (stores masked on real output
-//     rows and col < K): warps w and w + 4 read the same 32 TMEM lanes, w < 4 the first half of
-//     the 32-column chunks and w + 4 the rest; all of them release the accumulator on the
-//     leader's barrier (2 x 256 arrivals).
+//   - each CTA's four epilogue warps drain their own TMEM rows (stores masked on real output rows
+//     and col < K) and release the accumulator on the leader's barrier (2 x 128 arrivals). (An
+//     eight-warp epilogue, warps 4-7 taking half of each row's columns, measured 1% slower on the
+//     large layer: the tile epilogues already overlap the next tile's MMAs.)
 // Compared with one CTA per 128-row tile, every SM stores and reads only half of the B tile per
 // K block, so shared-memory traffic per MMA cycle drops from 192 to 128 bytes and more stages fit.
 //
@@ -97,7 +97,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accFull(b), 1);
-      mbar_init(accEmpty(b), 2 * 256);
+      mbar_init(accEmpty(b), 2 * 128);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -123,33 +123,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
   const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
   const int row_base = (int)rank * kBlockM;  // this CTA's rows within the 256-row unit
 
-  if (warp < 8) {
+  if (warp < 4) {
     // ------------------------------------------------------------------------------ epilogue
-    // Warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31 (the rows); w < 4 converts the first
-    // half of the tile's 32-column chunks, w >= 4 the rest. The TMA-store epilogue, where the plan
-    // uses it, runs on warps 0-3 alone.
     const float scale = __ldg(p.scale_x) * __ldg(p.scale_w);
-    const int split_cc = ((p.block_n / 32 + 1) / 2) * 32;
-    const int cc0 = warp < 4 ? 0 : split_cc, cc1 = warp < 4 ? split_cc : p.block_n;
-    const int row = threadIdx.x & 127;  // this thread's row among the CTA's 128
     uint32_t tc = 0, chunk = 0;
     for (int u = cluster_id; u < p.num_units; u += num_clusters, ++tc) {
       const Unit un = decode_unit(p, u);
       const int buf = tc & 1;
       bool ok = wait_bounded<true>(accFull(buf), (tc >> 1) & 1, ab, kStatusWaitAccFull);
       // the TMA-store epilogue synchronises its 128 threads: they go on or stop together
-      if (p.epi_tma && warp < 4) ok = named_barrier_and(1, 128, ok);
+      if (p.epi_tma) ok = named_barrier_and(1, 128, ok);
       if (!ok) break;
       tc_fence_after();
       const uint32_t trow =
-          tmem_base + (uint32_t)buf * p.acc_stride + ((uint32_t)((warp & 3) * 32) << 16);
-      if (!kGrid && p.epi_tma && un.part < 0) {
-        if (warp < 4)
-          epilogue_tile_tma(p, un, &ymap, trow, un.m_tile * p.block_m + row_base, row, scale,
-                            sEpi, chunk);
-      } else {
-        epilogue_row<kRowChk>(p, un, trow, row_base + row, scale, cc0, cc1);
-      }
+          tmem_base + (uint32_t)buf * p.acc_stride + ((uint32_t)(warp * 32) << 16);
+      if (!kGrid && p.epi_tma && un.part < 0)
+        epilogue_tile_tma(p, un, &ymap, trow, un.m_tile * p.block_m + row_base, threadIdx.x,
+                          scale, sEpi, chunk);
+      else
+        epilogue_row<kRowChk>(p, un, trow, row_base + threadIdx.x, scale, 0, p.block_n);
       tc_fence_before();
       mbar_arrive_cluster(leader_bars + (accEmpty(buf) - bars_u32));
     }
