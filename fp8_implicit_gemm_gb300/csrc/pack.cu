@@ -11,6 +11,7 @@
 #include <cuda_bf16.h>
 
 #include "pack_items.cuh"
+#include "quant.cuh"
 
 namespace c3d {
 
@@ -23,14 +24,157 @@ __global__ void __launch_bounds__(256) pack_kernel(ConvParams p, PackPlan q) {
     pack_item(p, q, c, g);
 }
 
+// Tiled transpose of the interior of an NCDHW x into the e4m3 channels-last copy, quantising
+// fp32 / bfloat16 values (kType) on the way. A block takes kTileP consecutive positions of one
+// image's D x H x W volume and kCT channels:
+//   1. the kCT source rows (each kTileP contiguous elements of one channel plane) are copied into
+//      shared memory with 16-byte loads, all issued before any is used;
+//   2. each thread takes one (position, 16-channel chunk): it reads the 16 values of its column
+//      (consecutive threads read consecutive positions: no bank conflicts), quantises them and
+//      stores the 16 codes with one 16-byte store into the padded channels-last copy.
+// The source is read in runs of kTileP elements per channel plane (2 KB from fp32). The item path
+// (one thread = 16 channels x 4 pixels, 16 planes per thread) made the quantised step of the
+// large layer 450 us (fp32 x) and 409 us (bf16 x); with this kernel they take 385 and 342 us.
+// Blocks past the tiles run the remaining items (halo, weights) of the item path.
+constexpr int kTileP = 512;
+
+template <int kType>
+__host__ __device__ constexpr int src_bytes() {
+  return kType == kSrcF32 ? 4 : 2;  // fp32 or bfloat16
+}
+
+template <int kType, int kCT>
+__global__ void __launch_bounds__(256) pack_x_tiled_kernel(ConvParams p, PackPlan q,
+                                                           long long x_tiles) {
+  pdl_launch_dependents();  // the implicit GEMM may start its prologue while the pack runs
+  constexpr int kEB = src_bytes<kType>();
+  constexpr int kRowBytes = kTileP * kEB;
+  extern __shared__ __align__(16) uint8_t raw[];  // [kCT][kTileP] source elements
+  const long long b = blockIdx.x;
+  if (b >= x_tiles) {
+    const PackCtx c = pack_ctx(p, q);
+    const long long total = c.e3 + q.w_items;
+    const long long stride = ((long long)gridDim.x - x_tiles) * blockDim.x;
+    for (long long g = c.e1 + (b - x_tiles) * blockDim.x + threadIdx.x; g < total; g += stride)
+      pack_item(p, q, c, g);
+    return;
+  }
+  const long long dhw = (long long)p.D * p.H * p.W;
+  const long long pt = (dhw + kTileP - 1) / kTileP;
+  const int ctn = p.C / kCT;
+  const long long pi = b % pt;  // position tiles fastest, then channel groups, then images
+  const long long rest = b / pt;
+  const int ci = (int)(rest % ctn);
+  const int n = (int)(rest / ctn);
+  const long long q0 = pi * kTileP;
+  const int c0 = ci * kCT;
+  const int valid = dhw - q0 < kTileP ? (int)(dhw - q0) : kTileP;  // positions of this tile
+  const uint8_t* src = p.x + (((long long)n * p.C + c0) * dhw + q0) * kEB;
+  // 1. the source rows into shared memory
+  if ((dhw * kEB) % 16 == 0) {  // every row starts 16-byte aligned; vectors never straddle dhw
+    constexpr int kVecs = kRowBytes / 16;
+    constexpr int kIters = kCT * kVecs / 256;  // blockDim.x == 256
+    const int vec_valid = (valid * kEB + 15) / 16;
+    uint4 v[kIters];
+#pragma unroll
+    for (int i = 0; i < kIters; ++i) {  // every load in flight before the first store
+      const int t = threadIdx.x + 256 * i;
+      const int r = t / kVecs, c = t - r * kVecs;
+      if (c < vec_valid)
+        v[i] = __ldg(reinterpret_cast<const uint4*>(src + (long long)r * dhw * kEB) + c);
+    }
+#pragma unroll
+    for (int i = 0; i < kIters; ++i) {
+      const int t = threadIdx.x + 256 * i;
+      const int r = t / kVecs, c = t - r * kVecs;
+      if (c < vec_valid) *reinterpret_cast<uint4*>(raw + r * kRowBytes + c * 16) = v[i];
+    }
+  } else {
+    for (int t = threadIdx.x; t < kCT * kTileP; t += blockDim.x) {
+      const int r = t / kTileP, e = t - r * kTileP;
+      if (e < valid) {
+        const uint8_t* a = src + ((long long)r * dhw + e) * kEB;
+        uint8_t* o = raw + r * kRowBytes + e * kEB;
+        if (kEB == 4)
+          *reinterpret_cast<uint32_t*>(o) = __ldg(reinterpret_cast<const uint32_t*>(a));
+        else
+          *reinterpret_cast<uint16_t*>(o) = __ldg(reinterpret_cast<const uint16_t*>(a));
+      }
+    }
+  }
+  __syncthreads();
+  // 2. one (position, 16-channel chunk) per thread and step
+  const float qs = __ldg(p.scale_x);
+  constexpr int kChunks = kCT / 16;
+  for (int t = threadIdx.x; t < kTileP * kChunks; t += blockDim.x) {
+    const int k = t / kTileP, e = t - k * kTileP;  // positions fastest across threads
+    if (e >= valid) continue;
+    uint32_t w[4];
+#pragma unroll
+    for (int j4 = 0; j4 < 4; ++j4) {
+      const int r = 16 * k + 4 * j4;
+      float v[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (kType == kSrcF32)
+          v[i] = *reinterpret_cast<const float*>(raw + (r + i) * kRowBytes + 4 * e);
+        else
+          v[i] = __uint_as_float(
+              (uint32_t)*reinterpret_cast<const uint16_t*>(raw + (r + i) * kRowBytes + 2 * e)
+              << 16);
+      }
+      w[j4] = quant4(v[0], v[1], v[2], v[3], qs);
+    }
+    const long long qq = q0 + e;  // position within the image's volume -> (d, h, w)
+    const int wq = (int)(qq % p.W);
+    const long long dh = qq / p.W;
+    const int hq = (int)(dh % p.H), dq = (int)(dh / p.H);
+    uint8_t* dst = p.xp + ((((long long)n * p.Dp + dq + p.pk_pd) * p.Hp + hq + p.pk_ph) * p.Wp +
+                           wq + p.pk_pw) * p.C + c0 + 16 * k;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+template <int kType>
+static cudaError_t launch_tiled_typed(const ConvParams& p, const PackPlan& q, long long x_tiles,
+                                      unsigned blocks, cudaStream_t stream) {
+  if (p.C % 32 == 0) {
+    constexpr size_t smem = (size_t)32 * kTileP * src_bytes<kType>();
+    auto k = pack_x_tiled_kernel<kType, 32>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k<<<blocks, 256, smem, stream>>>(p, q, x_tiles);
+  } else {
+    constexpr size_t smem = (size_t)16 * kTileP * src_bytes<kType>();
+    auto k = pack_x_tiled_kernel<kType, 16>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k<<<blocks, 256, smem, stream>>>(p, q, x_tiles);
+  }
+  return cudaGetLastError();
+}
+
 cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream) {
   const PackPlan q = pack_plan(p);
-  const long long total = q.x_items + q.halo_row_items + q.halo_side_items + q.w_items;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  long long blocks = (total + 255) / 256;
   const long long cap = (long long)sms * 16;
+  const long long rest_items = q.halo_row_items + q.halo_side_items + q.w_items;
+  if (q.x_items > 0 && !q.copy && p.elem_bytes == 1 && p.x_src_type != kSrcE4m3) {
+    // an NCDHW x quantised on the way: the tiled transpose, plus blocks for the remaining items
+    // (for e4m3 bytes the item path measured faster: 26 us against 55 us on the large layer)
+    const int ct = p.C % 32 == 0 ? 32 : 16;
+    const long long dhw = (long long)p.D * p.H * p.W;
+    const long long x_tiles = (long long)p.N * (p.C / ct) * ((dhw + kTileP - 1) / kTileP);
+    long long rest_blocks = (rest_items + 255) / 256;
+    if (rest_blocks > cap) rest_blocks = cap;
+    const unsigned blocks = (unsigned)(x_tiles + rest_blocks);
+    if (p.x_src_type == kSrcF32) return launch_tiled_typed<kSrcF32>(p, q, x_tiles, blocks, stream);
+    return launch_tiled_typed<kSrcBf16>(p, q, x_tiles, blocks, stream);
+  }
+  const long long total = q.x_items + rest_items;
+  long long blocks = (total + 255) / 256;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   pack_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, q);

@@ -5,22 +5,23 @@
 #include <cuda_runtime.h>
 
 #include "conv_common.cuh"
-#include "quant.cuh"
 
 namespace c3d {
 
-// Work of the pack kernel, as consecutive index ranges of one grid-stride loop:
-//   [0, x_items)          interior of x: with W % 4 == 0, one item = 16 channels x 4 pixels (16
+// Work of the item path of the pack, as consecutive index ranges of one grid-stride loop:
+//   [0, x_items)          interior of x, where the tiled transpose (pack.cu) does not take it:
+//                         e4m3 bytes with W % 4 == 0 in items of 16 channels x 4 pixels (16
 //                         aligned 4-byte loads, a byte transpose in registers, four 16-byte
-//                         stores); otherwise one item = 16 channels x 1 pixel (16 byte loads);
-//                         an fp32 or bfloat16 x (x_src_type) is quantised to e4m3 on the way, with
-//                         the device scale *scale_x, in the same items;
-//                         from a channels-last x, one item = one 16-byte chunk copied into the
-//                         padded copy (no items when the TMA routes read that x directly)
+//                         stores; 16 pixels with 16-byte loads when W % 16 == 0), else 16
+//                         channels x 1 pixel; a bfloat16 x (the BF16 twin) in items of 8
+//                         channels x 2 pixels (x 1 when W is odd); a channels-last x copied in
+//                         16-byte chunks into the padded copy (no items when the TMA routes read
+//                         that x directly). An fp32 / bfloat16 x quantised to e4m3 on the way is
+//                         always transposed by the tiled kernel; its item loop starts at x_items.
 //   + halo_row_items      16-byte zero chunks of the padded rows (d or h in the halo)
 //   + halo_side_items     16-byte zero chunks of the W-halo pixels of interior rows
 //   + w_items             16 channels of one tap of one filter
-// Pixels (or pixel quads) run fastest across threads, so each load of a warp is a contiguous run
+// Pixels (or pixel groups) run fastest across threads, so each load of a warp is a contiguous run
 // along W of the NCDHW input.
 struct PackPlan {
   long long x_items, halo_row_items, halo_side_items, w_items;
@@ -35,7 +36,7 @@ __host__ __device__ inline PackPlan pack_plan(const ConvParams& p) {
   const long long cq = p.C / 16;
   q.copy = p.x_cl != 0;
   q.quad = !q.copy && p.elem_bytes == 1 && (p.W % 4) == 0;
-  q.hex = q.quad && p.x_src_type == kSrcE4m3 && (p.W % 16) == 0;
+  q.hex = q.quad && (p.W % 16) == 0;
   q.two = !q.copy && p.elem_bytes == 2 && (p.W % 2) == 0;
   const int per_row = q.hex ? p.W / 16 : q.quad ? p.W / 4 : (q.two ? p.W / 2 : p.W);
   q.x_items = p.xp == nullptr ? 0 : (long long)p.N * p.D * p.H * cq * per_row;
@@ -66,7 +67,6 @@ struct PackCtx {
   long long e1, e2, e3;  // ends of the interior, halo-row and halo-side ranges
   int cq_n;              // 16-byte chunks per pixel
   long long plane;       // D * H * W
-  float qs;              // scale that quantises an fp32 / bfloat16 x (1 otherwise)
 };
 
 __device__ __forceinline__ PackCtx pack_ctx(const ConvParams& p, const PackPlan& q) {
@@ -76,7 +76,6 @@ __device__ __forceinline__ PackCtx pack_ctx(const ConvParams& p, const PackPlan&
   c.e3 = c.e2 + q.halo_side_items;
   c.cq_n = p.C >> 4;
   c.plane = (long long)p.D * p.H * p.W;
-  c.qs = p.x_src_type != kSrcE4m3 ? __ldg(p.scale_x) : 1.0f;
   return c;
 }
 
@@ -86,7 +85,6 @@ __device__ __forceinline__ void pack_item(const ConvParams& p, const PackPlan& q
   const long long e1 = c.e1, e2 = c.e2, e3 = c.e3;
   const int cq_n = c.cq_n;
   const long long plane = c.plane;
-  const float qs = c.qs;
   if (g < e1 && q.copy) {
     // interior from a channels-last x: (chunk fastest, then pixel)
     const long long pix = g / cq_n;  // ((n*D + d)*H + h)*W + w
@@ -100,59 +98,6 @@ __device__ __forceinline__ void pack_item(const ConvParams& p, const PackPlan& q
     *reinterpret_cast<uint4*>(
         p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) * p.Wp + w + p.pk_pw) *
                    p.C + cq * 16) = v;
-  } else if (g < e1 && p.x_src_type != kSrcE4m3) {
-    // interior, quantised from fp32 / bfloat16 values: as the e4m3 items below, each channel's
-    // 4 (or 1) pixels quantised into one 32-bit word (or byte) before the byte transpose
-    const int per_row = q.quad ? p.W / 4 : p.W;
-    const int wi = (int)(g % per_row);
-    const long long rest = g / per_row;
-    const int cq = (int)(rest % cq_n);
-    const long long row = rest / cq_n;  // n*D*H + d*H + h
-    const int h = (int)(row % p.H);
-    const int d = (int)((row / p.H) % p.D);
-    const int n = (int)(row / ((long long)p.H * p.D));
-    const long long el0 = ((long long)n * p.C + cq * 16) * plane + ((long long)d * p.H + h) * p.W;
-    uint8_t* dst_row = p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) *
-                                   p.Wp + p.pk_pw) * p.C + cq * 16;
-    if (q.quad) {
-      uint32_t v[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const long long e = el0 + j * plane + 4 * wi;
-        float a[4];
-        if (p.x_src_type == kSrcF32) {
-          const float4 f = __ldg(reinterpret_cast<const float4*>(p.x) + e / 4);
-          a[0] = f.x; a[1] = f.y; a[2] = f.z; a[3] = f.w;
-        } else {
-          const uint2 u = __ldg(reinterpret_cast<const uint2*>(p.x) + e / 4);
-          a[0] = __uint_as_float(u.x << 16);
-          a[1] = __uint_as_float(u.x & 0xFFFF0000u);
-          a[2] = __uint_as_float(u.y << 16);
-          a[3] = __uint_as_float(u.y & 0xFFFF0000u);
-        }
-        v[j] = quant4(a[0], a[1], a[2], a[3], qs);
-      }
-      uint32_t o[4][4];  // o[pixel][word of 4 channels]
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        uint32_t t[4];
-        transpose4x4(v + 4 * b, t);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) o[j][b] = t[j];
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        *reinterpret_cast<uint4*>(dst_row + (long long)(4 * wi + j) * p.C) =
-            make_uint4(o[j][0], o[j][1], o[j][2], o[j][3]);
-    } else {
-      uint32_t v[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float a = src_value(p.x, p.x_src_type, el0 + j * plane + wi);
-        v[j >> 2] |= (quant4(a, 0.0f, 0.0f, 0.0f, qs) & 0xFFu) << ((j & 3) * 8);
-      }
-      *reinterpret_cast<uint4*>(dst_row + (long long)wi * p.C) = make_uint4(v[0], v[1], v[2], v[3]);
-    }
   } else if (g < e1 && p.elem_bytes == 2) {
     // interior, bfloat16: one item = 8 channels (one 16-byte chunk) x 2 pixels (or 1 when W is
     // odd); pixels fastest, then chunk, then (n, d, h) row
