@@ -18,6 +18,8 @@
 //   warp 9     MMA issuer: 4 x tcgen05.mma (M=128, N=block_n, K=32 bytes) per 128-byte K block;
 //              kind::f8f6f4 on e4m3 bytes, or kind::f16 on bfloat16 pairs (kBf16): the tiles,
 //              stages and descriptors are the same in bytes
+// Warps 8 and 9 run their loops on all 32 lanes (every lane waits on the barriers) and issue the
+// copies, MMAs and commits of a stage from one lane chosen by elect.sync.
 // Stages are handed over with mbarriers: TMA-full (transaction bytes of A and/or B), A-full (128
 // gather arrivals, gather route), stage-empty (tcgen05.commit). Two TMEM accumulators let the
 // epilogue of one tile overlap the main loop of the next. Every wait is bounded; a wait that runs
