@@ -15,12 +15,19 @@
 
 namespace c3d {
 
-__global__ void __launch_bounds__(256) pack_kernel(ConvParams p, PackPlan q) {
+// Blocks [0, item_blocks) run the items in a grid-stride loop; the blocks after them one weight
+// tile each (pack_w_tile, kWTileBytes of dynamic shared memory).
+__global__ void __launch_bounds__(256) pack_kernel(ConvParams p, PackPlan q, int item_blocks) {
   pdl_launch_dependents();  // the implicit GEMM may start its prologue while the pack runs
+  extern __shared__ __align__(16) uint8_t wsm[];
+  if ((int)blockIdx.x >= item_blocks) {
+    pack_w_tile(p, q, (long long)blockIdx.x - item_blocks, wsm);
+    return;
+  }
   const PackCtx c = pack_ctx(p, q);
   const long long total = c.e3 + q.w_items;
   for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < total;
-       g += (long long)gridDim.x * blockDim.x)
+       g += (long long)item_blocks * blockDim.x)
     pack_item(p, q, c, g);
 }
 
@@ -35,7 +42,8 @@ __global__ void __launch_bounds__(256) pack_kernel(ConvParams p, PackPlan q) {
 // The source is read in runs of kTileP elements per channel plane (2 KB from fp32). The item path
 // (one thread = 16 channels x 4 pixels, 16 planes per thread) made the quantised step of the
 // large layer 450 us (fp32 x) and 409 us (bf16 x); with this kernel they take 385 and 342 us.
-// Blocks past the tiles run the remaining items (halo, weights) of the item path.
+// Blocks past the tiles run the remaining items (halo, weights by items) of the item path, then
+// one weight tile each (pack_w_tile).
 constexpr int kTileP = 512;
 
 template <int kType>
@@ -45,16 +53,21 @@ __host__ __device__ constexpr int src_bytes() {
 
 template <int kType, int kCT>
 __global__ void __launch_bounds__(256) pack_x_tiled_kernel(ConvParams p, PackPlan q,
-                                                           long long x_tiles) {
+                                                           long long x_tiles,
+                                                           long long rest_blocks) {
   pdl_launch_dependents();  // the implicit GEMM may start its prologue while the pack runs
   constexpr int kEB = src_bytes<kType>();
   constexpr int kRowBytes = kTileP * kEB;
   extern __shared__ __align__(16) uint8_t raw[];  // [kCT][kTileP] source elements
   const long long b = blockIdx.x;
+  if (b >= x_tiles + rest_blocks) {
+    pack_w_tile(p, q, b - x_tiles - rest_blocks, raw);  // the stage buffer holds kWTileBytes
+    return;
+  }
   if (b >= x_tiles) {
     const PackCtx c = pack_ctx(p, q);
     const long long total = c.e3 + q.w_items;
-    const long long stride = ((long long)gridDim.x - x_tiles) * blockDim.x;
+    const long long stride = rest_blocks * blockDim.x;
     for (long long g = c.e1 + (b - x_tiles) * blockDim.x + threadIdx.x; g < total; g += stride)
       pack_item(p, q, c, g);
     return;
@@ -137,19 +150,20 @@ __global__ void __launch_bounds__(256) pack_x_tiled_kernel(ConvParams p, PackPla
 
 template <int kType>
 static cudaError_t launch_tiled_typed(const ConvParams& p, const PackPlan& q, long long x_tiles,
-                                      unsigned blocks, cudaStream_t stream) {
+                                      long long rest_blocks, unsigned blocks,
+                                      cudaStream_t stream) {
   if (p.C % 32 == 0) {
     constexpr size_t smem = (size_t)32 * kTileP * src_bytes<kType>();
     auto k = pack_x_tiled_kernel<kType, 32>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k<<<blocks, 256, smem, stream>>>(p, q, x_tiles);
+    k<<<blocks, 256, smem, stream>>>(p, q, x_tiles, rest_blocks);
   } else {
     constexpr size_t smem = (size_t)16 * kTileP * src_bytes<kType>();
     auto k = pack_x_tiled_kernel<kType, 16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k<<<blocks, 256, smem, stream>>>(p, q, x_tiles);
+    k<<<blocks, 256, smem, stream>>>(p, q, x_tiles, rest_blocks);
   }
   return cudaGetLastError();
 }
@@ -163,21 +177,24 @@ cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream) {
   const long long rest_items = q.halo_row_items + q.halo_side_items + q.w_items;
   if (q.x_items > 0 && !q.copy && p.elem_bytes == 1 && p.x_src_type != kSrcE4m3) {
     // an NCDHW x quantised on the way: the tiled transpose, plus blocks for the remaining items
-    // (for e4m3 bytes the item path measured faster: 26 us against 55 us on the large layer)
+    // and the weight tiles (for e4m3 bytes the item path measured faster: 26 us against 55 us on
+    // the large layer)
     const int ct = p.C % 32 == 0 ? 32 : 16;
     const long long dhw = (long long)p.D * p.H * p.W;
     const long long x_tiles = (long long)p.N * (p.C / ct) * ((dhw + kTileP - 1) / kTileP);
     long long rest_blocks = (rest_items + 255) / 256;
     if (rest_blocks > cap) rest_blocks = cap;
-    const unsigned blocks = (unsigned)(x_tiles + rest_blocks);
-    if (p.x_src_type == kSrcF32) return launch_tiled_typed<kSrcF32>(p, q, x_tiles, blocks, stream);
-    return launch_tiled_typed<kSrcBf16>(p, q, x_tiles, blocks, stream);
+    const unsigned blocks = (unsigned)(x_tiles + rest_blocks + q.w_blocks);
+    if (p.x_src_type == kSrcF32)
+      return launch_tiled_typed<kSrcF32>(p, q, x_tiles, rest_blocks, blocks, stream);
+    return launch_tiled_typed<kSrcBf16>(p, q, x_tiles, rest_blocks, blocks, stream);
   }
   const long long total = q.x_items + rest_items;
-  long long blocks = (total + 255) / 256;
-  if (blocks > cap) blocks = cap;
-  if (blocks < 1) blocks = 1;
-  pack_kernel<<<(unsigned)blocks, 256, 0, stream>>>(p, q);
+  long long item_blocks = (total + 255) / 256;
+  if (item_blocks > cap) item_blocks = cap;
+  if (item_blocks + q.w_blocks < 1) item_blocks = 1;
+  pack_kernel<<<(unsigned)(item_blocks + q.w_blocks), 256,
+                q.w_blocks > 0 ? (size_t)kWTileBytes : 0, stream>>>(p, q, (int)item_blocks);
   return cudaGetLastError();
 }
 

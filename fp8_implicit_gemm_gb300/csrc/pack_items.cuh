@@ -23,8 +23,14 @@ namespace c3d {
 //   + w_items             16 channels of one tap of one filter
 // Pixels (or pixel groups) run fastest across threads, so each load of a warp is a contiguous run
 // along W of the NCDHW input.
+constexpr long long kWTileBytes = 16384;  // shared-memory buffer of one weight tile
+
 struct PackPlan {
   long long x_items, halo_row_items, halo_side_items, w_items;
+  // Weights by tiles (pack_w_tile) when a 16-byte column of every tap fits the tile buffer: one
+  // block per (filter k, w_group 16-byte channel chunks); w_items is then 0.
+  long long w_blocks;
+  int w_group;
   bool hex;   // e4m3 bytes and W % 16 == 0: 16-pixel items (16-byte loads)
   bool quad;  // e4m3 and W % 4 == 0: 4-pixel items
   bool two;   // bfloat16 and W % 2 == 0: 2-pixel items
@@ -44,6 +50,14 @@ __host__ __device__ inline PackPlan pack_plan(const ConvParams& p) {
   q.halo_row_items = (long long)p.N * halo_rows_per_image * p.Wp * cq;
   q.halo_side_items = (long long)p.N * p.D * p.H * (p.Wp - p.W) * cq;
   q.w_items = (long long)p.K * p.taps * cq;
+  q.w_blocks = 0;
+  q.w_group = 0;
+  if (16LL * p.taps <= kWTileBytes) {
+    q.w_group = (int)(kWTileBytes / (16LL * p.taps));
+    if (q.w_group > cq) q.w_group = (int)cq;
+    q.w_blocks = (long long)p.K * ((cq + q.w_group - 1) / q.w_group);
+    q.w_items = 0;
+  }
   if (p.halo_once) {  // the plan zeroed its padded copy once: the halo is never written again
     q.halo_row_items = 0;
     q.halo_side_items = 0;
@@ -266,6 +280,41 @@ __device__ __forceinline__ void pack_item(const ConvParams& p, const PackPlan& q
     uint4* dst =
         reinterpret_cast<uint4*>(p.wp + ((long long)k * p.taps + tap) * p.C + cq * 16);
     *dst = make_uint4(v[0], v[1], v[2], v[3]);
+  }
+}
+
+// Weight tile wb of the re-layout KCTRS -> K x taps x C: filter k and the w_group 16-byte channel
+// chunks from cq0 on. Their source is one contiguous run of nq * 16 * taps bytes (channel-major,
+// taps innermost), copied into `sm` with 16-byte loads; then each thread gathers one 16-byte chunk
+// of one tap (16 e4m3 or 8 bfloat16 channels, taps bytes apart in shared memory) and stores it
+// with one 16-byte store. Every thread of the block must call it (it synchronises the block).
+__device__ __forceinline__ void pack_w_tile(const ConvParams& p, const PackPlan& q, long long wb,
+                                            uint8_t* sm) {
+  const int cq_n = p.C >> 4;
+  const int ng = (cq_n + q.w_group - 1) / q.w_group;
+  const int k = (int)(wb / ng);
+  const int cq0 = (int)(wb - (long long)k * ng) * q.w_group;
+  const int nq = min(q.w_group, cq_n - cq0);
+  const int taps = p.taps;
+  const uint8_t* src = p.w + ((long long)k * p.C + (long long)cq0 * 16) * taps;
+  const int vecs = nq * taps;  // 16-byte vectors of the run
+  for (int v = threadIdx.x; v < vecs; v += blockDim.x)
+    reinterpret_cast<uint4*>(sm)[v] = __ldg(reinterpret_cast<const uint4*>(src) + v);
+  __syncthreads();
+  for (int t = threadIdx.x; t < vecs; t += blockDim.x) {
+    const int cl = t / taps, tap = t - cl * taps;  // chunk within the tile, tap
+    uint32_t v[4] = {0u, 0u, 0u, 0u};
+    if (p.elem_bytes == 2) {
+      const uint16_t* s16 = reinterpret_cast<const uint16_t*>(sm) + (cl * 8) * taps + tap;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j >> 1] |= (uint32_t)s16[j * taps] << ((j & 1) * 16);
+    } else {
+      const uint8_t* s8 = sm + (cl * 16) * taps + tap;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j >> 2] |= (uint32_t)s8[j * taps] << ((j & 3) * 8);
+    }
+    *reinterpret_cast<uint4*>(p.wp + ((long long)k * taps + tap) * p.C +
+                              (long long)(cq0 + cl) * 16) = make_uint4(v[0], v[1], v[2], v[3]);
   }
 }
 
