@@ -85,9 +85,10 @@ def main_kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def committed_traffic(workload: str):
+def committed_traffic(workload: str, input_layout: str = "NCDHW"):
     """DRAM bytes per launch of the main kernel from a committed ncu summary, if that summary was
-    taken on the current kernel source for this workload (line: ``bench-traffic: {json}``)."""
+    taken on the current kernel source for this workload and input layout (line:
+    ``bench-traffic: {json}``; a line without "input_layout" is an NCDHW capture)."""
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
@@ -102,7 +103,8 @@ def committed_traffic(workload: str):
                         d = json.loads(line.split(":", 1)[1])
                     except ValueError:
                         continue
-                    if d.get("workload") == workload and d.get("source_sha256") == want:
+                    if (d.get("workload") == workload and d.get("source_sha256") == want and
+                            d.get("input_layout", "NCDHW") == input_layout):
                         return d.get("dram_bytes_per_launch")
     return None
 
@@ -461,7 +463,7 @@ def run_ours(args):
     t_flop = fig["flop"] / (fp8_peak * 1e12)
     t_hbm = fig["alg_bytes"] / (hbm_peak * 1e9)
     workload = shape.name + (" [bf16 inputs]" if bf16 else "")
-    traffic = committed_traffic(workload)
+    traffic = committed_traffic(workload, "NDHWC" if channels_last else "NCDHW")
     if t_flop >= t_hbm:
         achieved = fig["flop"] / (mean_kern_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak, 1),
