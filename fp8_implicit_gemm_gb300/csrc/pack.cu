@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(256) pack_kernel(ConvParams p, PackPlan q, int
 // fp32 / bfloat16 values (kType) on the way. A block takes kTileP consecutive positions of one
 // image's D x H x W volume and kCT channels:
 //   1. the kCT source rows (each kTileP contiguous elements of one channel plane) are copied into
-//      shared memory with 16-byte loads, all issued before any is used;
+//      shared memory with 16-byte cp.async copies, all in flight at once;
 //   2. each thread takes one (position, 16-channel chunk): it reads the 16 values of its column
 //      (consecutive threads read consecutive positions: no bank conflicts), quantises them and
 //      stores the 16 codes with one 16-byte store into the padded channels-last copy.
@@ -52,7 +52,7 @@ __host__ __device__ constexpr int src_bytes() {
 }
 
 template <int kType, int kCT>
-__global__ void __launch_bounds__(256) pack_x_tiled_kernel(ConvParams p, PackPlan q,
+__global__ void __launch_bounds__(256, 3) pack_x_tiled_kernel(ConvParams p, PackPlan q,
                                                            long long x_tiles,
                                                            long long rest_blocks) {
   pdl_launch_dependents();  // the implicit GEMM may start its prologue while the pack runs
@@ -88,20 +88,15 @@ __global__ void __launch_bounds__(256) pack_x_tiled_kernel(ConvParams p, PackPla
     constexpr int kVecs = kRowBytes / 16;
     constexpr int kIters = kCT * kVecs / 256;  // blockDim.x == 256
     const int vec_valid = (valid * kEB + 15) / 16;
-    uint4 v[kIters];
 #pragma unroll
-    for (int i = 0; i < kIters; ++i) {  // every load in flight before the first store
+    for (int i = 0; i < kIters; ++i) {  // every copy in flight at once, none through registers
       const int t = threadIdx.x + 256 * i;
       const int r = t / kVecs, c = t - r * kVecs;
       if (c < vec_valid)
-        v[i] = __ldg(reinterpret_cast<const uint4*>(src + (long long)r * dhw * kEB) + c);
+        cp_async_16_zfill(smem_u32(raw + r * kRowBytes + c * 16),
+                          src + (long long)r * dhw * kEB + (long long)c * 16, 16);
     }
-#pragma unroll
-    for (int i = 0; i < kIters; ++i) {
-      const int t = threadIdx.x + 256 * i;
-      const int r = t / kVecs, c = t - r * kVecs;
-      if (c < vec_valid) *reinterpret_cast<uint4*>(raw + r * kRowBytes + c * 16) = v[i];
-    }
+    cp_async_wait_all();
   } else {
     for (int t = threadIdx.x; t < kCT * kTileP; t += blockDim.x) {
       const int r = t / kTileP, e = t - r * kTileP;
