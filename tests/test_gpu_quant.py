@@ -37,6 +37,38 @@ def _values(kind, n, seed):
     raise ValueError(kind)
 
 
+def _near_boundaries(amax: float, seed: int, ulps: int = 4) -> np.ndarray:
+    """Values whose quotient by the scale of `amax` falls on, or within a few fp32 units of, each
+    rounding boundary of the e4m3 grid (the midpoints between neighbouring codes, both signs):
+    the cases where any shortcut for the IEEE quotient v / s (a multiply by fp32(1/s), say) can
+    pick a different code."""
+    s = Q.scale_of(np.float32(amax))
+    grid = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8)).astype(np.float64)
+    mids = (grid[:-1] + grid[1:]) / 2
+    base = (mids * np.float64(s)).astype(np.float32)  # v with v / s near a midpoint
+    out = [np.float32(amax)]
+    for k in range(-ulps, ulps + 1):
+        step = base.copy()
+        for _ in range(abs(k)):
+            step = np.nextafter(step, np.float32(np.inf if k > 0 else -np.inf)).astype(np.float32)
+        out += [step, -step]
+    rng = np.random.default_rng(seed)
+    v = np.concatenate([np.atleast_1d(o) for o in out]).astype(np.float32)
+    v = v[np.abs(v) <= np.float32(amax)]
+    return v[rng.permutation(v.size)]
+
+
+@pytest.mark.parametrize("amax", [448.0, 1.0, 3.7, 1234.567, 2.0 ** -20 * 5.3, 0.0625 * 7.1])
+def test_quantize_quotients_near_code_boundaries(amax):
+    # a multiply by fp32(1/s) would get up to 94 of these codes wrong; the quantiser divides,
+    # and every value must get the code of the IEEE quotient
+    v = _near_boundaries(amax, seed=int(amax * 1000) % 1000)
+    q, s = _gpu_quantize(torch.from_numpy(v).cuda())
+    ref_q, ref_s = Q.quantize(v)
+    assert s == ref_s
+    assert np.array_equal(q, ref_q), int(np.sum(q != ref_q))
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("kind", ["normal", "wide", "zeros"])
 @pytest.mark.parametrize("n", [1, 15, 16, 17, 1000, 65541])
