@@ -7,6 +7,8 @@
 // gather route it carries an explicit zero halo of `pad` pixels on every spatial side, so that an
 // A-tile row needs no bounds test, only the padded-row test (row < npq). The weights are re-laid
 // from KCTRS to K x taps x C to match.
+#include <algorithm>
+
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -32,19 +34,22 @@ __global__ void __launch_bounds__(256) pack_kernel(ConvParams p, PackPlan q, int
 }
 
 // Tiled transpose of the interior of an NCDHW x into the e4m3 channels-last copy, quantising
-// fp32 / bfloat16 values (kType) on the way. A block takes kTileP consecutive positions of one
-// image's D x H x W volume and kCT channels:
-//   1. the kCT source rows (each kTileP contiguous elements of one channel plane) are copied into
-//      shared memory with 16-byte cp.async copies, all in flight at once;
-//   2. each thread takes one (position, 16-channel chunk): it reads the 16 values of its column
-//      (consecutive threads read consecutive positions: no bank conflicts), quantises them and
-//      stores the 16 codes with one 16-byte store into the padded channels-last copy.
+// fp32 / bfloat16 values (kType) on the way. A tile is kTileP consecutive positions of one image's
+// D x H x W volume and kCT channels. The first tile_blocks blocks walk the tiles blockIdx.x,
+// + tile_blocks, ... through two shared-memory stages (one tile each when tile_blocks == x_tiles):
+//   1. the kCT source rows of the next tile (each kTileP contiguous elements of one channel plane)
+//      go into the free stage with 16-byte cp.async copies, in flight while
+//   2. each thread takes one (position, 16-channel chunk) of the current tile: it reads the 16
+//      values of its column (consecutive threads read consecutive positions: no bank conflicts),
+//      quantises them and stores the 16 codes with one 16-byte store into the padded
+//      channels-last copy.
 // The source is read in runs of kTileP elements per channel plane (2 KB from fp32). The item path
-// (one thread = 16 channels x 4 pixels, 16 planes per thread) made the quantised step of the
-// large layer 450 us (fp32 x) and 409 us (bf16 x); with this kernel they take 385 and 342 us.
-// Blocks past the tiles run the remaining items (halo, weights by items) of the item path, then
-// one weight tile each (pack_w_tile).
+// it replaced (one thread = 16 channels x 4 pixels, 16 planes per thread) made the quantised step
+// of the large layer 450 us (fp32 x) and 409 us (bf16 x).
+// Blocks past the persistent ones run the remaining items (halo, weights by items) of the item
+// path, then one weight tile each (pack_w_tile).
 constexpr int kTileP = 512;
+constexpr int kTiledBlocksPerSm = 3;  // 2 stages of <= 32 KB each, <= 80 registers a thread
 
 template <int kType>
 __host__ __device__ constexpr int src_bytes() {
@@ -52,114 +57,132 @@ __host__ __device__ constexpr int src_bytes() {
 }
 
 template <int kType, int kCT>
-__global__ void __launch_bounds__(256, 3) pack_x_tiled_kernel(ConvParams p, PackPlan q,
-                                                           long long x_tiles,
-                                                           long long rest_blocks) {
+__global__ void __launch_bounds__(256, kTiledBlocksPerSm) pack_x_tiled_kernel(
+    ConvParams p, PackPlan q, long long x_tiles, int tile_blocks, long long rest_blocks) {
   pdl_launch_dependents();  // the implicit GEMM may start its prologue while the pack runs
   constexpr int kEB = src_bytes<kType>();
   constexpr int kRowBytes = kTileP * kEB;
-  extern __shared__ __align__(16) uint8_t raw[];  // [kCT][kTileP] source elements
+  constexpr int kStageBytes = kCT * kRowBytes;
+  extern __shared__ __align__(16) uint8_t raw[];  // [2][kCT][kTileP] source elements
   const long long b = blockIdx.x;
-  if (b >= x_tiles + rest_blocks) {
-    pack_w_tile(p, q, b - x_tiles - rest_blocks, raw);  // the stage buffer holds kWTileBytes
+  if (b >= tile_blocks + rest_blocks) {
+    pack_w_tile(p, q, b - tile_blocks - rest_blocks, raw);  // the stages hold kWTileBytes
     return;
   }
-  if (b >= x_tiles) {
+  if (b >= tile_blocks) {
     const PackCtx c = pack_ctx(p, q);
     const long long total = c.e3 + q.w_items;
     const long long stride = rest_blocks * blockDim.x;
-    for (long long g = c.e1 + (b - x_tiles) * blockDim.x + threadIdx.x; g < total; g += stride)
+    for (long long g = c.e1 + (b - tile_blocks) * blockDim.x + threadIdx.x; g < total; g += stride)
       pack_item(p, q, c, g);
     return;
   }
   const long long dhw = (long long)p.D * p.H * p.W;
   const long long pt = (dhw + kTileP - 1) / kTileP;
   const int ctn = p.C / kCT;
-  const long long pi = b % pt;  // position tiles fastest, then channel groups, then images
-  const long long rest = b / pt;
-  const int ci = (int)(rest % ctn);
-  const int n = (int)(rest / ctn);
-  const long long q0 = pi * kTileP;
-  const int c0 = ci * kCT;
-  const int valid = dhw - q0 < kTileP ? (int)(dhw - q0) : kTileP;  // positions of this tile
-  const uint8_t* src = p.x + (((long long)n * p.C + c0) * dhw + q0) * kEB;
-  // 1. the source rows into shared memory
-  if ((dhw * kEB) % 16 == 0) {  // every row starts 16-byte aligned; vectors never straddle dhw
+  // every row starts 16-byte aligned, and vectors never straddle dhw: cp.async copies
+  const bool vec = (dhw * kEB) % 16 == 0;
+  const float qs = __ldg(p.scale_x);
+  struct Tile {
+    int n, c0, valid;
+    long long q0;
+    const uint8_t* src;
+  };
+  auto tile_at = [&](long long t) {  // position tiles fastest, then channel groups, then images
+    Tile tl;
+    const long long pi = t % pt, rest = t / pt;
+    tl.n = (int)(rest / ctn);
+    tl.c0 = (int)(rest % ctn) * kCT;
+    tl.q0 = pi * kTileP;
+    tl.valid = dhw - tl.q0 < kTileP ? (int)(dhw - tl.q0) : kTileP;
+    tl.src = p.x + (((long long)tl.n * p.C + tl.c0) * dhw + tl.q0) * kEB;
+    return tl;
+  };
+  auto issue = [&](const Tile& tl, uint8_t* stage) {  // cp.async copies of a tile, no wait
     constexpr int kVecs = kRowBytes / 16;
     constexpr int kIters = kCT * kVecs / 256;  // blockDim.x == 256
-    const int vec_valid = (valid * kEB + 15) / 16;
+    const int vec_valid = (tl.valid * kEB + 15) / 16;
 #pragma unroll
-    for (int i = 0; i < kIters; ++i) {  // every copy in flight at once, none through registers
+    for (int i = 0; i < kIters; ++i) {
       const int t = threadIdx.x + 256 * i;
       const int r = t / kVecs, c = t - r * kVecs;
       if (c < vec_valid)
-        cp_async_16_zfill(smem_u32(raw + r * kRowBytes + c * 16),
-                          src + (long long)r * dhw * kEB + (long long)c * 16, 16);
+        cp_async_16_zfill(smem_u32(stage + r * kRowBytes + c * 16),
+                          tl.src + (long long)r * dhw * kEB + (long long)c * 16, 16);
     }
-    cp_async_wait_all();
-  } else {
-    for (int t = threadIdx.x; t < kCT * kTileP; t += blockDim.x) {
-      const int r = t / kTileP, e = t - r * kTileP;
-      if (e < valid) {
-        const uint8_t* a = src + ((long long)r * dhw + e) * kEB;
-        uint8_t* o = raw + r * kRowBytes + e * kEB;
-        if (kEB == 4)
-          *reinterpret_cast<uint32_t*>(o) = __ldg(reinterpret_cast<const uint32_t*>(a));
-        else
-          *reinterpret_cast<uint16_t*>(o) = __ldg(reinterpret_cast<const uint16_t*>(a));
+  };
+  int sidx = 0;
+  if (vec) issue(tile_at(b), raw);
+  cp_async_commit();
+  for (long long t = b; t < x_tiles; t += tile_blocks) {
+    const Tile tl = tile_at(t);
+    uint8_t* stage = raw + sidx * kStageBytes;
+    const long long nt = t + tile_blocks;
+    if (vec && nt < x_tiles) issue(tile_at(nt), raw + (sidx ^ 1) * kStageBytes);
+    cp_async_commit();
+    if (vec) {
+      cp_async_wait_group<1>();  // this thread's copies of tile t have landed
+    } else {
+      for (int i = threadIdx.x; i < kCT * kTileP; i += blockDim.x) {
+        const int r = i / kTileP, e = i - r * kTileP;
+        if (e < tl.valid) {
+          const uint8_t* a = tl.src + ((long long)r * dhw + e) * kEB;
+          uint8_t* o = stage + r * kRowBytes + e * kEB;
+          if (kEB == 4)
+            *reinterpret_cast<uint32_t*>(o) = __ldg(reinterpret_cast<const uint32_t*>(a));
+          else
+            *reinterpret_cast<uint16_t*>(o) = __ldg(reinterpret_cast<const uint16_t*>(a));
+        }
       }
     }
-  }
-  __syncthreads();
-  // 2. one (position, 16-channel chunk) per thread and step
-  const float qs = __ldg(p.scale_x);
-  constexpr int kChunks = kCT / 16;
-  for (int t = threadIdx.x; t < kTileP * kChunks; t += blockDim.x) {
-    const int k = t / kTileP, e = t - k * kTileP;  // positions fastest across threads
-    if (e >= valid) continue;
-    uint32_t w[4];
+    __syncthreads();
+    constexpr int kChunks = kCT / 16;
+    for (int i = threadIdx.x; i < kTileP * kChunks; i += blockDim.x) {
+      const int k = i / kTileP, e = i - k * kTileP;  // positions fastest across threads
+      if (e >= tl.valid) continue;
+      uint32_t w[4];
 #pragma unroll
-    for (int j4 = 0; j4 < 4; ++j4) {
-      const int r = 16 * k + 4 * j4;
-      float v[4];
+      for (int j4 = 0; j4 < 4; ++j4) {
+        const int r = 16 * k + 4 * j4;
+        float v[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (kType == kSrcF32)
-          v[i] = *reinterpret_cast<const float*>(raw + (r + i) * kRowBytes + 4 * e);
-        else
-          v[i] = __uint_as_float(
-              (uint32_t)*reinterpret_cast<const uint16_t*>(raw + (r + i) * kRowBytes + 2 * e)
-              << 16);
+        for (int m = 0; m < 4; ++m) {
+          if (kType == kSrcF32)
+            v[m] = *reinterpret_cast<const float*>(stage + (r + m) * kRowBytes + 4 * e);
+          else
+            v[m] = __uint_as_float(
+                (uint32_t)*reinterpret_cast<const uint16_t*>(stage + (r + m) * kRowBytes + 2 * e)
+                << 16);
+        }
+        w[j4] = quant4(v[0], v[1], v[2], v[3], qs);
       }
-      w[j4] = quant4(v[0], v[1], v[2], v[3], qs);
+      const long long qq = tl.q0 + e;  // position within the image's volume -> (d, h, w)
+      const int wq = (int)(qq % p.W);
+      const long long dh = qq / p.W;
+      const int hq = (int)(dh % p.H), dq = (int)(dh / p.H);
+      uint8_t* dst = p.xp + ((((long long)tl.n * p.Dp + dq + p.pk_pd) * p.Hp + hq + p.pk_ph) *
+                                 p.Wp + wq + p.pk_pw) * p.C + tl.c0 + 16 * k;
+      *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
     }
-    const long long qq = q0 + e;  // position within the image's volume -> (d, h, w)
-    const int wq = (int)(qq % p.W);
-    const long long dh = qq / p.W;
-    const int hq = (int)(dh % p.H), dq = (int)(dh / p.H);
-    uint8_t* dst = p.xp + ((((long long)n * p.Dp + dq + p.pk_pd) * p.Hp + hq + p.pk_ph) * p.Wp +
-                           wq + p.pk_pw) * p.C + c0 + 16 * k;
-    *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+    __syncthreads();  // the stage is free for the copies two tiles on
+    sidx ^= 1;
   }
+  cp_async_wait_all();
 }
 
-template <int kType>
-static cudaError_t launch_tiled_typed(const ConvParams& p, const PackPlan& q, long long x_tiles,
-                                      long long rest_blocks, unsigned blocks,
-                                      cudaStream_t stream) {
-  if (p.C % 32 == 0) {
-    constexpr size_t smem = (size_t)32 * kTileP * src_bytes<kType>();
-    auto k = pack_x_tiled_kernel<kType, 32>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k<<<blocks, 256, smem, stream>>>(p, q, x_tiles, rest_blocks);
-  } else {
-    constexpr size_t smem = (size_t)16 * kTileP * src_bytes<kType>();
-    auto k = pack_x_tiled_kernel<kType, 16>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k<<<blocks, 256, smem, stream>>>(p, q, x_tiles, rest_blocks);
-  }
+// tile_blocks == x_tiles: one tile per block, no prefetch, so one stage of shared memory is enough
+template <int kType, int kCT>
+static cudaError_t launch_tiled_ct(const ConvParams& p, const PackPlan& q, long long x_tiles,
+                                   long long tile_blocks, long long rest_blocks,
+                                   cudaStream_t stream) {
+  constexpr size_t stage = (size_t)kCT * kTileP * src_bytes<kType>();
+  static_assert(stage >= (size_t)kWTileBytes, "the weight tiles use the stages");
+  const size_t smem = tile_blocks < x_tiles ? 2 * stage : stage;
+  const unsigned blocks = (unsigned)(tile_blocks + rest_blocks + q.w_blocks);
+  auto k = pack_x_tiled_kernel<kType, kCT>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k<<<blocks, 256, smem, stream>>>(p, q, x_tiles, (int)tile_blocks, rest_blocks);
   return cudaGetLastError();
 }
 
@@ -173,16 +196,24 @@ cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream) {
   if (q.x_items > 0 && !q.copy && p.elem_bytes == 1 && p.x_src_type != kSrcE4m3) {
     // an NCDHW x quantised on the way: the tiled transpose, plus blocks for the remaining items
     // and the weight tiles (for e4m3 bytes the item path measured faster: 26 us against 55 us on
-    // the large layer)
+    // the large layer). bfloat16 x: persistent blocks over 32-channel tiles in two 32 KB stages
+    // (large layer step 332 -> 323 us against one tile per block); fp32 x: one 32-channel tile
+    // (64 KB) per block (the two-stage forms measured 364 us with 16 channels, 399 us with 32 on
+    // one block per SM, against 362 us).
+    const bool f32 = p.x_src_type == kSrcF32;
     const int ct = p.C % 32 == 0 ? 32 : 16;
     const long long dhw = (long long)p.D * p.H * p.W;
     const long long x_tiles = (long long)p.N * (p.C / ct) * ((dhw + kTileP - 1) / kTileP);
+    const long long tile_blocks =
+        f32 ? x_tiles : std::min<long long>(x_tiles, (long long)sms * kTiledBlocksPerSm);
     long long rest_blocks = (rest_items + 255) / 256;
     if (rest_blocks > cap) rest_blocks = cap;
-    const unsigned blocks = (unsigned)(x_tiles + rest_blocks + q.w_blocks);
-    if (p.x_src_type == kSrcF32)
-      return launch_tiled_typed<kSrcF32>(p, q, x_tiles, rest_blocks, blocks, stream);
-    return launch_tiled_typed<kSrcBf16>(p, q, x_tiles, rest_blocks, blocks, stream);
+    if (f32 && ct == 32)
+      return launch_tiled_ct<kSrcF32, 32>(p, q, x_tiles, tile_blocks, rest_blocks, stream);
+    if (f32) return launch_tiled_ct<kSrcF32, 16>(p, q, x_tiles, tile_blocks, rest_blocks, stream);
+    if (ct == 32)
+      return launch_tiled_ct<kSrcBf16, 32>(p, q, x_tiles, tile_blocks, rest_blocks, stream);
+    return launch_tiled_ct<kSrcBf16, 16>(p, q, x_tiles, tile_blocks, rest_blocks, stream);
   }
   const long long total = q.x_items + rest_items;
   long long item_blocks = (total + 255) / 256;
