@@ -152,12 +152,12 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
   if (block_n == 0) block_n = (int)std::min<long long>(256, round_up(K, 32));
   if (block_n < 32 || block_n > 256 || block_n % 32 != 0) return CONV3D_EINVAL;
 
-  // CTA pairs (cta_group::2, 256-row tiles) run the im2col and padded-grid routes; by default
-  // the im2col route uses them whenever the problem has more than one 128-row tile.
+  // CTA pairs (cta_group::2, 256-row tiles) run the im2col and padded-grid routes. The im2col
+  // route runs on one CTA unless asked: on every shape measured the one-CTA kernel was faster
+  // there (N tile 64-256, 4-10%: e.g. 313.6 against 342.2 us on the large layer, 61.9 against
+  // 68.2 us on a stride-2 layer of the vae shape).
   if (o.cta_pair == 2 && route == kRouteGather) return CONV3D_EUNSUPPORTED;
-  const bool pair = route == kRouteGrid ||
-                    (route == kRouteIm2col &&
-                     (o.cta_pair == 2 || (o.cta_pair == 0 && npq > kBlockM)));
+  const bool pair = route == kRouteGrid || (route == kRouteIm2col && o.cta_pair == 2);
   const int block_m = pair ? 2 * kBlockM : kBlockM;
   // co-resident units: one per SM, or one per CTA pair; a CTA cap given in the options counts
   long long slots = pair ? std::max(1, sm_count / 2) : sm_count;

@@ -52,13 +52,13 @@ def test_describe_configs(lib):
     # stride 2 on 4x16x16 with pad 1 gives a 2x8x8 output: npq = 128
     assert npq == [288, 3840, 65536, 128, 244800]
     assert [i["k_gemm"] for i in infos] == [2592, 1728, 3456, 13824, 6912]
-    # CTA pairs (256-row tiles) wherever there is more than one 128-row tile; stride-1 layers whose
-    # padded output grid adds at most 30% rows take the padded-grid route
-    assert [i["cta_pair"] for i in infos] == [2, 2, 2, 1, 2]
-    assert [i["block_m"] for i in infos] == [256, 256, 256, 128, 256]
+    # stride-1 layers whose padded output grid adds at most 30% rows take the padded-grid route,
+    # on CTA pairs (256-row tiles); the others the TMA im2col route on one CTA (128-row tiles)
+    assert [i["cta_pair"] for i in infos] == [1, 2, 2, 1, 2]
+    assert [i["block_m"] for i in infos] == [128, 256, 256, 128, 256]
     assert [i["route"] for i in infos] == [2, 3, 3, 2, 3]
     # grid route: N * ceil(Do*Hp*Wp / 256) tiles, (t, r, channel block) groups as K blocks
-    assert [i["m_tiles"] for i in infos] == [2, 2 * 10, 273, 1, 990]
+    assert [i["m_tiles"] for i in infos] == [3, 2 * 10, 273, 1, 990]
     assert [i["k_blocks"] for i in infos] == [21, 9, 9, 108, 18]
     assert [i["row_chk"] for i in infos] == [1, 1, 1, 0, 1]
     assert [i["block_n"] for i in infos] == [96, 128, 128, 256, 256]
