@@ -182,13 +182,22 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
   // a quarter as many tiles as slots, every tile is split to fill the machine (with more tiles
   // the reduction of the partials costs more than the shorter K loops save); with more tiles
   // than slots, only the tiles of a last, mostly idle wave are split, over the slots that wave
-  // would leave idle. A split count in the options splits every tile that many ways.
+  // would leave idle, and only when a tile's main loop is long enough (at least 16384 tensor-core
+  // cycles: about 8 us) for the shorter tail to repay the reduction's launch and partial traffic
+  // (measured: 2 x 64 x 16 x 64 x 64 -> 128, 546 tiles whose K loop is ~3500 cycles: 40.7 us
+  // unsplit against 47.4 us with its 14-tile tail split 5 ways; the large layer and a stride-2
+  // layer, ~27600 cycles a tile, gain ~6%). A split count in the options splits every tile that
+  // many ways.
+  // tensor-core cycles of one tile's K loop: MMAs of K = 32 bytes, N / 2 cycles each (M = 128
+  // rows per CTA; the padded-grid route issues S taps x a_cb / 32 of them per K block)
+  const long long mmas_per_kb = route == kRouteGrid ? (long long)S * (a_cb / 32) : kBlockK / 32;
+  const long long tile_cycles = k_blocks * mmas_per_kb * (block_n / 2);
   long long full_tiles = 0;
   if (splits == 0) {
     splits = 1;
     if (tiles * 4 <= slots && k_blocks >= 8) {
       splits = std::max<long long>(1, std::min<long long>(slots / tiles, k_blocks / 4));
-    } else if (tiles > slots && k_blocks >= 4) {
+    } else if (tiles > slots && k_blocks >= 4 && tile_cycles >= 16384) {
       const long long tail = tiles % slots;
       if (tail > 0 && tail * 2 <= slots) {
         full_tiles = tiles - tail;

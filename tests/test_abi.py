@@ -131,6 +131,12 @@ def test_describe_tail_split(lib):
     assert _describe(synth.CONFIGS[4], splits=1)["full_tiles"] == 990
     i = _describe(synth.CONFIGS[4], splits=3)
     assert i["full_tiles"] == 0 and i["splits"] == 3
+    # a short K loop is not worth a reduction: 546 tiles of 9 groups of 6 N = 128 MMAs (~3500
+    # tensor cycles a tile) keep their 14-tile tail whole
+    short = synth.ConvShape(2, 64, 16, 64, 64, 128)
+    i = _describe(short)
+    assert i["m_tiles"] * i["n_tiles"] == 546 and i["splits"] == 1
+    assert _describe(short, max_ctas=150)["splits"] == 1
 
 
 def test_describe_channels_last_input(lib):

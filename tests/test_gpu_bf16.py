@@ -115,8 +115,9 @@ def test_forced_splits(splits, kernel):
 
 @pytest.mark.parametrize("kernel", ["im2col-1cta", "grid-pair"])
 def test_tail_tiles_split_along_k(kernel):
-    res, info = _full_case(synth.CONFIGS[1], synth.config_seed(1),
-                           max_ctas={"im2col-1cta": 12, "grid-pair": 16}[kernel], **KERNELS[kernel])
+    # a CTA cap leaves a last wave at most half full, and the K loops are long enough to split it
+    res, info = _full_case(synth.ConvShape(1, 256, 8, 10, 12, 256), 2719,
+                           max_ctas={"im2col-1cta": 6, "grid-pair": 8}[kernel], **KERNELS[kernel])
     assert 0 < info["full_tiles"] < info["m_tiles"] * info["n_tiles"]
 
 

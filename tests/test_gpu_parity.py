@@ -137,13 +137,15 @@ def test_max_ctas_small_grid_many_tiles(kernel):
 # A CTA cap that leaves a mostly idle last wave: its tiles are split along K over the idle slots
 # while the others are computed whole, in one launch (whole tiles store bf16, split tiles fp32
 # partials that the reduction then sums).
-TAIL_CASES = {"gather-1cta": 12, "im2col-1cta": 12, "im2col-pair": 12, "grid-pair": 16}
+# A CTA cap leaves a last wave at most half full; the tiles' K loops (54 or 18 K blocks of N = 256
+# MMAs) are long enough for the planner to split that wave's tiles along K.
+TAIL_SHAPE = synth.ConvShape(1, 256, 8, 10, 12, 256)
+TAIL_CASES = {"gather-1cta": 6, "im2col-1cta": 6, "im2col-pair": 6, "grid-pair": 8}
 
 
 @pytest.mark.parametrize("kernel", list(TAIL_CASES))
 def test_tail_tiles_split_along_k(kernel):
-    res, info = _full_case(synth.CONFIGS[1], synth.config_seed(1), max_ctas=TAIL_CASES[kernel],
-                           **KERNELS[kernel])
+    res, info = _full_case(TAIL_SHAPE, 2718, max_ctas=TAIL_CASES[kernel], **KERNELS[kernel])
     tiles = info["m_tiles"] * info["n_tiles"]
     assert 0 < info["full_tiles"] < tiles and info["splits"] > 1, info
 
