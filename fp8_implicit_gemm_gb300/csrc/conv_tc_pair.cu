@@ -11,9 +11,11 @@
 //     receives its own 128 accumulator rows; tcgen05.commit multicasts the stage-empty and
 //     accumulator-full signals to both CTAs;
 //   - each CTA's four epilogue warps drain their own TMEM rows (stores masked on real output rows
-//     and col < K) and release the accumulator on the leader's barrier (2 x 128 arrivals). (An
+//     and col < K) and release the accumulator on the leader's barrier (2 x 128 arrivals). An
 //     eight-warp epilogue, warps 4-7 taking half of each row's columns, measured 1% slower on the
-//     large layer: the tile epilogues already overlap the next tile's MMAs.)
+//     large layer when every tile used it: those epilogues already overlap the next tile's MMAs.
+//     Only the pair's last unit, whose epilogue nothing hides, is split with warps 4-7 (the large
+//     layer's step 261.8-262.8 against 263.8-264.9 us, interleaved on one GPU).
 // Compared with one CTA per 128-row tile, every SM stores and reads only half of the B tile per
 // K block, so shared-memory traffic per MMA cycle drops from 192 to 128 bytes and more stages fit.
 //
@@ -76,6 +78,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
   // bars: full[S] (leader's is used), empty[S], accFull[2], accEmpty[2] (leader's), drain
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // last-unit hand-off to warps 4-7: the TMEM buffer of the pair's last unit, or -1 (none, or
+  // the epilogue stopped early)
+  volatile int* last_buf = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
   const uint32_t sA_u32 = smem_u32(sA), sB_u32 = smem_u32(sB);
   const uint32_t bars_u32 = smem_u32(bars);
@@ -101,6 +106,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
+    *last_buf = -1;
     fence_mbar_init();
   }
   if (warp == 8) {
@@ -123,29 +129,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
   const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
   const int row_base = (int)rank * kBlockM;  // this CTA's rows within the 256-row unit
 
+  // The last unit's epilogue is not hidden behind any MMA: unless the TMA-store epilogue is on,
+  // warps 4-7 take the second half of its columns. Warps 0-3 hand it over at named barrier 3
+  // (256 threads), which they reach exactly once on every path: at the last unit, or on their
+  // way out when there is none or they stopped early.
+  const bool split_last = !p.epi_tma && p.block_n >= 64;
   if (warp < 4) {
     // ------------------------------------------------------------------------------ epilogue
     const float scale = __ldg(p.scale_x) * __ldg(p.scale_w);
     uint32_t tc = 0, chunk = 0;
+    bool handed = false;
     for (int u = cluster_id; u < p.num_units; u += num_clusters, ++tc) {
       const Unit un = decode_unit(p, u);
       const int buf = tc & 1;
+      const bool last = u + num_clusters >= p.num_units;
       bool ok = wait_bounded<true>(accFull(buf), (tc >> 1) & 1, ab, kStatusWaitAccFull);
-      // the TMA-store epilogue synchronises its 128 threads: they go on or stop together
-      if (p.epi_tma) ok = named_barrier_and(1, 128, ok);
+      // the TMA-store epilogue and the hand-off synchronise the 128 threads: they go on or stop
+      // together
+      if (p.epi_tma || split_last) ok = named_barrier_and(1, 128, ok);
       if (!ok) break;
       tc_fence_after();
       const uint32_t trow =
           tmem_base + (uint32_t)buf * p.acc_stride + ((uint32_t)(warp * 32) << 16);
+      int cc1 = p.block_n;
+      if (split_last && last) {
+        if (threadIdx.x == 0) *last_buf = buf;
+        named_barrier_sync(3, 256);
+        handed = true;
+        cc1 = (p.block_n / 2 + 31) & ~31;
+      }
       if (!kGrid && p.epi_tma && un.part < 0)
         epilogue_tile_tma(p, un, &ymap, trow, un.m_tile * p.block_m + row_base, threadIdx.x,
                           scale, sEpi, chunk);
       else
-        epilogue_row<kRowChk>(p, un, trow, row_base + threadIdx.x, scale, 0, p.block_n);
+        epilogue_row<kRowChk>(p, un, trow, row_base + threadIdx.x, scale, 0, cc1);
       tc_fence_before();
       mbar_arrive_cluster(leader_bars + (accEmpty(buf) - bars_u32));
     }
+    if (split_last && !handed) named_barrier_arrive(3, 256);  // nothing handed over
     if (p.epi_tma && threadIdx.x == 0) bulk_wait_group_all();  // stores done before exit
+  } else if (warp < 8) {
+    // ------------------------------------------------------------------- last-unit epilogue
+    if (split_last) {
+      int last_u = -1;
+      for (int u = cluster_id; u < p.num_units; u += num_clusters) last_u = u;
+      named_barrier_sync(3, 256);
+      const int buf = *last_buf;
+      if (last_u >= 0 && buf >= 0) {
+        tc_fence_after();
+        const Unit un = decode_unit(p, last_u);
+        const float scale = __ldg(p.scale_x) * __ldg(p.scale_w);
+        const uint32_t trow = tmem_base + (uint32_t)buf * p.acc_stride +
+                              ((uint32_t)((warp - 4) * 32) << 16);
+        epilogue_row<kRowChk>(p, un, trow, row_base + threadIdx.x - 128, scale,
+                              (p.block_n / 2 + 31) & ~31, p.block_n);
+        tc_fence_before();
+      }
+    }
   } else if (warp == 8) {
     // ------------------------------------------------------------------------------ TMA loader
     // The whole warp runs the loop and waits on the barriers; one elected lane issues the copies.

@@ -201,6 +201,10 @@ __device__ __forceinline__ void pdl_wait_primary() {
 __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Arrive at named barrier `id` without waiting for it.
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
 // Named barrier that also ANDs a predicate over its `count` threads (all of them get the result).
 __device__ __forceinline__ bool named_barrier_and(uint32_t id, uint32_t count, bool pred) {
   uint32_t r;
