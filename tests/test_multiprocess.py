@@ -36,7 +36,9 @@ def _rank_main(rank, world, port, out):
 
 def test_dist_max_over_two_gloo_ranks():
     port = _free_port()
-    with mp.Manager() as m:
+    # the manager's server process starts by spawn: earlier tests may have left threads running
+    # in this process, and a fork taken while another thread holds a lock can hang the child
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_rank_main, args=(2, port, out), nprocs=2, join=True)
         assert dict(out) == {0: 13.5, 1: 13.5}
