@@ -266,6 +266,116 @@ def cpu_oracle_sample(inp, shape, target_s: float, seed: int, min_points: int = 
             "sample": f"{n} random outputs of {total} (fp64 direct sum, one by one)"}
 
 
+# ------------------------------------------------------------------------------ per workload
+def pack_alg_bytes(fig, packs_x: bool) -> int:
+    """Compulsory bytes of the operand re-layout: the weights read and written once, and x read
+    and its channels-last interior written once when the run transposes x."""
+    return 2 * fig["w_bytes"] + (2 * fig["x_bytes"] if packs_x else 0)
+
+
+def roofline_of(fig, kernel_ms: float, fp8_peak: float, hbm_peak: float) -> dict:
+    """Roofline of one launch: the slower of the dense tensor rate and HBM bandwidth for the
+    algorithmic FLOP and bytes (x + w + y once), against the measured kernel time."""
+    t_flop = fig["flop"] / (fp8_peak * 1e12)
+    t_hbm = fig["alg_bytes"] / (hbm_peak * 1e9)
+    s = kernel_ms * 1e-3
+    if t_flop >= t_hbm:
+        ach = fig["flop"] / s / 1e12
+        return {"bound": "tensor", "achieved": round(ach, 1), "peak": round(fp8_peak, 1),
+                "unit": "TFLOP/s", "frac": round(ach / fp8_peak, 4)}
+    ach = fig["alg_bytes"] / s / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": round(hbm_peak, 1),
+            "unit": "GB/s", "frac": round(ach / hbm_peak, 4)}
+
+
+def measure_config(index: int, inp, dev, stream, flush, fp8_peak: float, hbm_peak: float,
+                   steps: int = 100, warmup: int = 5) -> dict:
+    """One workload's default e4m3 plan: step time (events around each run), main-kernel time and
+    pack time (the library's events), TFLOP/s and the roofline fraction. L2 is flushed before
+    every step; medians over `steps` steps."""
+    import torch
+    from fp8_implicit_gemm_gb300 import capi, synth
+
+    shape = synth.CONFIGS[index]
+    fig = problem_figures(shape)
+    if inp is None:
+        inp = synth.make_config_inputs(index)
+    plan = capi.conv3d_fp8_plan(shape.N, shape.C, shape.D, shape.H, shape.W, shape.K, shape.T,
+                                shape.R, shape.S, shape.stride, shape.pad, dev)
+    try:
+        info = capi.conv3d_fp8_get_info(plan)
+        x, w = inp["x"].to(dev), inp["w"].to(dev)
+        sx = torch.tensor([inp["sx"]], dtype=torch.float32, device=dev)
+        sw = torch.tensor([inp["sw"]], dtype=torch.float32, device=dev)
+        y = torch.full((shape.N, shape.K, fig["Do"], fig["Ho"], fig["Wo"]), float("nan"),
+                       dtype=torch.bfloat16, device=dev)
+
+        def run():
+            capi.conv3d_fp8_run(plan, x, w, sx, sw, y, shape.stride, shape.pad, stream)
+
+        for _ in range(warmup):
+            flush.fill_(3)
+            run()
+        torch.cuda.synchronize()
+        if torch.isnan(y).any().item():
+            raise RuntimeError(f"{shape.name}: outputs left unwritten")
+        mk = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+        ev = [(mk(), mk()) for _ in range(steps)]
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record(stream)
+            run()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        step = [a.elapsed_time(b) for a, b in ev]
+        evk = [(mk(), mk(), mk()) for _ in range(steps)]
+        for e in evk:
+            for e_ in e:
+                e_.record(stream)
+        torch.cuda.synchronize()
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            capi.conv3d_fp8_set_pack_timing_event(plan, evk[i][0])
+            capi.conv3d_fp8_set_timing_events(plan, evk[i][1], evk[i][2])
+            run()
+        torch.cuda.synchronize()
+        capi.conv3d_fp8_set_pack_timing_event(plan, None)
+        capi.conv3d_fp8_set_timing_events(plan, None, None)
+        if capi.conv3d_fp8_check(plan) != capi.CONV3D_OK:
+            raise RuntimeError(f"{shape.name}: a kernel reported a timed-out wait")
+        kern = [b.elapsed_time(c) for _, b, c in evk]
+        pack = [a.elapsed_time(b) for a, b, _ in evk]
+    finally:
+        capi.conv3d_fp8_destroy(plan)
+    k_ms, s_ms, p_ms = (statistics.median(kern), statistics.median(step),
+                        statistics.median(pack))
+    roof = roofline_of(fig, k_ms, fp8_peak, hbm_peak)
+    step_roof = roofline_of(fig, s_ms, fp8_peak, hbm_peak)
+    pbytes = pack_alg_bytes(fig, True)
+    split = info["full_tiles"] < info["m_tiles"] * info["n_tiles"]
+    return {
+        "workload": shape.name, "config_index": index,
+        "plan": {k: info[k] for k in ("route", "cta_pair", "block_m", "block_n", "m_tiles",
+                                      "n_tiles", "full_tiles", "splits", "stages", "grid")},
+        "gflop": round(fig["flop"] / 1e9, 4), "alg_bytes": fig["alg_bytes"],
+        "kernel": ("conv3d_fp8_tc_pair_kernel" if info["cta_pair"] == 2 else
+                   "conv3d_fp8_tc_kernel") + (" + splitk_reduce_kernel" if split else ""),
+        "kernel_ms": round(k_ms, 5), "kernel_ms_min": round(min(kern), 5),
+        "step_ms": round(s_ms, 5), "step_ms_min": round(min(step), 5),
+        "pack_ms": round(p_ms, 5),
+        "kernel_tflops": round(fig["flop"] / (k_ms * 1e-3) / 1e12, 2),
+        "step_tflops": round(fig["flop"] / (s_ms * 1e-3) / 1e12, 2),
+        "kernel_gbs": round(fig["alg_bytes"] / (k_ms * 1e-3) / 1e9, 1),
+        "step_gbs": round(fig["alg_bytes"] / (s_ms * 1e-3) / 1e9, 1),
+        "roofline": roof, "step_roofline_frac": step_roof["frac"],
+        "pack": {"alg_bytes": pbytes, "ms": round(p_ms, 5),
+                 "achieved_gbs": round(pbytes / (p_ms * 1e-3) / 1e9, 1),
+                 "frac_of_hbm": round(pbytes / (p_ms * 1e-3) / 1e9 / hbm_peak, 4)},
+        "steps": steps, "timing": "medians; CUDA events on the launching stream; L2 flushed "
+                                  "before every step",
+    }
+
+
 # ----------------------------------------------------------------------------------------- ours
 def run_ours(args):
     import numpy as np
@@ -331,7 +441,8 @@ def run_ours(args):
 
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True))
           for _ in range(K)]
     for e in ev:  # materialise the lazily created events before they are handed to the library
         for x_ in e:
@@ -350,7 +461,7 @@ def run_ours(args):
     t_wall0 = time.perf_counter()
     for i in range(K):
         flush.fill_(i & 0xFF)
-        s0, s1, _, _ = ev[i]
+        s0, s1 = ev[i][0], ev[i][1]
         s0.record(stream)
         step()
         s1.record(stream)
@@ -360,20 +471,23 @@ def run_ours(args):
     K2 = min(K, 500)  # kernel-time pass
     for i in range(K2):
         flush.fill_(i & 0xFF)
+        capi.conv3d_fp8_set_pack_timing_event(plan, ev[i][4])
         capi.conv3d_fp8_set_timing_events(plan, ev[i][2], ev[i][3])
         step()
     torch.cuda.synchronize()
     sampler.stop()
+    capi.conv3d_fp8_set_pack_timing_event(plan, None)
     capi.conv3d_fp8_set_timing_events(plan, None, None)
     if capi.conv3d_fp8_check(plan) != capi.CONV3D_OK:
         raise RuntimeError("a kernel reported a timed-out wait")
     step_ms = [e[0].elapsed_time(e[1]) for e in ev]
     kern_ms = [ev[i][2].elapsed_time(ev[i][3]) for i in range(K2)]
+    pack_ms = [ev[i][4].elapsed_time(ev[i][2]) for i in range(K2)]
     # L2-warm figure (reported beside the headline, not instead of it): the same steps back to
     # back without the flush, so each step finds the previous step's operands in L2
     K3 = min(K, 500)
     for i in range(K3):
-        s0, s1, _, _ = ev[i]
+        s0, s1 = ev[i][0], ev[i][1]
         s0.record(stream)
         step()
         s1.record(stream)
@@ -487,6 +601,24 @@ def run_ours(args):
     roof["alg_flop"] = fig["flop"]
     roof["alg_bytes"] = fig["alg_bytes"]
     roof["step_roofline_frac"] = round(max(t_flop, t_hbm) / (mean_step_ms * 1e-3), 4)
+    # the operand re-layout of the same steps (HBM-bound): the pack alone, by the library's events
+    packs_x = not channels_last or info["route"] == 1
+    p_bytes = (pack_alg_bytes(fig, packs_x) if not quant else
+               2 * fig["w_bytes"] + x.numel() * x.element_size() + fig["x_bytes"])
+    p_ms = statistics.mean(pack_ms)
+    pack = {"kernel": "pack_kernel", "alg_bytes": int(p_bytes), "ms": round(p_ms, 5),
+            "achieved": round(p_bytes / (p_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "peak": round(hbm_peak, 1), "frac": round(p_bytes / (p_ms * 1e-3) / 1e9 / hbm_peak, 4),
+            "timing": "library events before the pack and before the main kernel, same steps as "
+                      "kernel_ms"}
+
+    # ---- every workload's default e4m3 plan (NCDHW x), one record each
+    per_config = None
+    if not bf16 and not quant and not channels_last and not args.no_per_config:
+        per_config = []
+        for ci in range(len(synth.CONFIGS)):
+            per_config.append(measure_config(ci, inp if ci == args.config else None, dev, stream,
+                                             flush, fp8_peak, hbm_peak))
 
     # ---- the device quantiser alone (two passes over x: amax, then the cast), HBM-bound
     quantiser = None
@@ -545,6 +677,8 @@ def run_ours(args):
                          "per-step events)",
                    "parallelism": f"replicas x{dist.world}"},
         "roofline": roof,
+        "pack": pack,
+        "per_config": per_config,
         "quantiser": quantiser,
         "cpu_baseline": cpu,
         "e2e": e2e,
@@ -636,6 +770,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-workload records (every config's default e4m3 plan)")
     ap.add_argument("--dtype", choices=["e4m3", "bf16"], default="e4m3",
                     help="input type: the e4m3 path, or its BF16-input twin")
     ap.add_argument("--quantize-x", choices=["fp32", "bf16"], default=None,

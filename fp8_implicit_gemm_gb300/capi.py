@@ -77,6 +77,8 @@ def load() -> ctypes.CDLL:
             lib.conv3d_fp8_run.argtypes = [vp, vp, vp, vp, vp, vp, i3, i3, vp]
             lib.conv3d_fp8_set_timing_events.restype = ci
             lib.conv3d_fp8_set_timing_events.argtypes = [vp, vp, vp]
+            lib.conv3d_fp8_set_pack_timing_event.restype = ci
+            lib.conv3d_fp8_set_pack_timing_event.argtypes = [vp, vp]
             lib.conv3d_fp8_run_noalloc.restype = ci
             lib.conv3d_fp8_run_noalloc.argtypes = [ci] * 9 + [i3, i3, vp, vp, vp, vp, vp, vp]
             lib.conv3d_fp8_check.restype = ci
@@ -206,19 +208,28 @@ def conv3d_fp8_run_noalloc(N, C, D, H, W, K, T, R, S, stride, pad, x, w, scale_x
                                          scale_w, y, stream), "conv3d_fp8_run_noalloc")
 
 
+def _raw_event(ev):
+    if ev is None:
+        return None
+    if isinstance(ev, int):
+        return ev
+    if not ev.cuda_event:       # torch creates its event lazily, on first record
+        ev.record()
+    return ev.cuda_event
+
+
 def conv3d_fp8_set_timing_events(plan, ev_begin, ev_end) -> None:
     """Record the given events (torch.cuda.Event or raw cudaEvent_t ints; None to clear) around
     the main kernel of every later run of the plan."""
-    def raw(ev):
-        if ev is None:
-            return None
-        if isinstance(ev, int):
-            return ev
-        if not ev.cuda_event:       # torch creates its event lazily, on first record
-            ev.record()
-        return ev.cuda_event
-    _raise(load().conv3d_fp8_set_timing_events(plan, raw(ev_begin), raw(ev_end)),
+    _raise(load().conv3d_fp8_set_timing_events(plan, _raw_event(ev_begin), _raw_event(ev_end)),
            "conv3d_fp8_set_timing_events")
+
+
+def conv3d_fp8_set_pack_timing_event(plan, ev_pack) -> None:
+    """Record the given event (None to clear) right before the pack kernel of every later run
+    of the plan; with the begin event of conv3d_fp8_set_timing_events it brackets the pack."""
+    _raise(load().conv3d_fp8_set_pack_timing_event(plan, _raw_event(ev_pack)),
+           "conv3d_fp8_set_pack_timing_event")
 
 
 def conv3d_fp8_check(plan) -> int:

@@ -29,6 +29,7 @@ struct conv3d_fp8_plan_s {
   void* workspace = nullptr;
   cudaEvent_t ev_begin = nullptr;  // measurement hook, caller-owned
   cudaEvent_t ev_end = nullptr;
+  cudaEvent_t ev_pack = nullptr;   // measurement hook before the pack, caller-owned
 };
 
 namespace {
@@ -501,6 +502,13 @@ conv3d_status plan_impl(int elem_bytes, conv3d_fp8_plan_t* out, int N, int C, in
     delete plan;
     return st;
   }
+  // The attribute is per kernel and per device, shared by every plan: grant the device's opt-in
+  // maximum once, so that a later plan with a smaller tile cannot shrink it under this one. It
+  // comes before the occupancy query below, which counts clusters at this plan's shared memory.
+  if (conv_set_smem_attr((size_t)prop.sharedMemPerBlockOptin) != cudaSuccess) {
+    delete plan;
+    return CONV3D_ECUDA;
+  }
   if (plan->p.pair) {  // plan for the CTA pairs the device can actually hold at once
     const int clusters = conv_pair_max_active_clusters(plan->p);
     if (clusters > 0 && clusters < prop.multiProcessorCount / 2) {
@@ -523,12 +531,6 @@ conv3d_status plan_impl(int elem_bytes, conv3d_fp8_plan_t* out, int N, int C, in
   if ((int)smem > prop.sharedMemPerBlockOptin) {
     delete plan;
     return CONV3D_EUNSUPPORTED;
-  }
-  // The attribute is per kernel and per device, shared by every plan: grant the device's opt-in
-  // maximum once, so that a later plan with a smaller tile cannot shrink it under this one.
-  if (conv_set_smem_attr((size_t)prop.sharedMemPerBlockOptin) != cudaSuccess) {
-    delete plan;
-    return CONV3D_ECUDA;
   }
   if (cudaMalloc(&plan->workspace, L.total) != cudaSuccess) {
     cudaGetLastError();
@@ -605,6 +607,7 @@ conv3d_status run_impl(conv3d_fp8_plan_t plan, const void* x, const void* w,
     if (st != CONV3D_OK) return st;
     plan->ymap_src = y;
   }
+  if (plan->ev_pack && cudaEventRecord(plan->ev_pack, s) != cudaSuccess) return CONV3D_ECUDA;
   if (launch_pack(p, s) != cudaSuccess) return CONV3D_ECUDA;
   if (plan->ev_begin && cudaEventRecord(plan->ev_begin, s) != cudaSuccess) return CONV3D_ECUDA;
   if (launch_conv(p, plan->wmap, plan->xmap, plan->ymap, plan->info.row_chk != 0,
@@ -711,6 +714,12 @@ conv3d_status conv3d_fp8_set_timing_events(conv3d_fp8_plan_t plan, void* ev_begi
   if (!plan) return CONV3D_EINVAL;
   plan->ev_begin = static_cast<cudaEvent_t>(ev_begin);
   plan->ev_end = static_cast<cudaEvent_t>(ev_end);
+  return CONV3D_OK;
+}
+
+conv3d_status conv3d_fp8_set_pack_timing_event(conv3d_fp8_plan_t plan, void* ev_pack) {
+  if (!plan) return CONV3D_EINVAL;
+  plan->ev_pack = static_cast<cudaEvent_t>(ev_pack);
   return CONV3D_OK;
 }
 
@@ -854,6 +863,14 @@ extern "C" conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int 
     return CONV3D_ECUDA;
   if (major != 10 || minor != 3) return CONV3D_EUNSUPPORTED;
 
+  // the scratch address and the kernels' shared-memory grant, before any occupancy query
+  void* base = nullptr;
+  st = noalloc_setup(dev, &base);
+  if (st != CONV3D_OK) return st;
+  int optin = 0;
+  if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+    return CONV3D_ECUDA;
+
   ConvParams p{};
   Layout L{};
   st = decide(1, N, C, D, H, W, K, T, R, S, stride, pad, sms, nullptr, &info, &p, &L);
@@ -867,10 +884,10 @@ extern "C" conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int 
     }
   }
   if (L.total > (size_t)CONV3D_FP8_NOALLOC_SCRATCH_BYTES) return CONV3D_EUNSUPPORTED;
+  const size_t smem = p.pair ? conv_pair_smem_bytes(p)
+                             : conv_smem_bytes(p.block_n, p.stages, p.epi_tma != 0);
+  if ((long long)smem > (long long)optin) return CONV3D_EUNSUPPORTED;
 
-  void* base = nullptr;
-  st = noalloc_setup(dev, &base);
-  if (st != CONV3D_OK) return st;
   uint8_t* ws = static_cast<uint8_t*>(base);
   p.xp = L.xp_bytes ? ws + L.xp_off : nullptr;
   p.wp = ws + L.wp_off;

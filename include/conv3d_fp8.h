@@ -115,12 +115,16 @@ typedef struct {
  * Allocates the plan and its device workspace (packed operands, split-K partials, the status
  * word). Errors: EINVAL (bad shape, empty output), EUNSUPPORTED (C % 16 != 0, not sm_103, index
  * ranges beyond 32 bits), ENOMEM, ECUDA. On error *plan is set to NULL.
+ * Defined by: "Root cause" (the GEMM view M = npq, N = K, K_gemm = C*T*R*S and grid_m =
+ * ceil(npq / TILE_M), the tiling whose padded rows the store guard must drop). The page prints
+ * no host interface: the argument list is this library's.
  */
 conv3d_status conv3d_fp8_plan(conv3d_fp8_plan_t *plan, int N, int C, int D, int H, int W, int K,
                               int T, int R, int S, const int stride[3], const int pad[3],
                               int device);
 
-/* As conv3d_fp8_plan, with planning knobs (opts may be NULL). */
+/* As conv3d_fp8_plan, with planning knobs (opts may be NULL). Defined by: as conv3d_fp8_plan;
+ * the knobs are this library's (none of them changes what is computed). */
 conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t *plan, int N, int C, int D, int H, int W,
                                  int K, int T, int R, int S, const int stride[3],
                                  const int pad[3], int device, const conv3d_fp8_options *opts);
@@ -139,6 +143,10 @@ conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t *plan, int N, int C, int D, i
  * The plan's workspace is shared by its runs: at most one run of a plan may be in flight at a
  * time (use one plan per concurrent stream). Errors: EINVAL, ECUDA (launch failure).
  * Kernel-side errors are reported later, by conv3d_fp8_check.
+ * Defined by: "Problem" (e4m3 x and w with per-tensor scales from the fp8 cast, BF16 output),
+ * "Root cause" (NCDHW store offset, padding taps read zero, padded rows carry a zero
+ * accumulator) and "Fix" (stores masked on row < npq as well as col < K; the split-K path guards
+ * its reduction the same way).
  */
 conv3d_status conv3d_fp8_run(conv3d_fp8_plan_t plan, const void *x_ncdhw, const void *w_kctrs,
                              const float *scale_x, const float *scale_w, void *y_ncdhw,
@@ -150,8 +158,18 @@ conv3d_status conv3d_fp8_run(conv3d_fp8_plan_t plan, const void *x_ncdhw, const 
  * main implicit-GEMM kernel and ev_end immediately after it, or after the reduction of its
  * split tiles when it has some, so a caller can time the GEMM apart from the operand packing.
  * The caller owns the events. Pass NULL, NULL to stop. Errors: EINVAL for a NULL plan.
+ * Defined by: none (library plumbing, for measurement).
  */
 conv3d_status conv3d_fp8_set_timing_events(conv3d_fp8_plan_t plan, void *ev_begin, void *ev_end);
+
+/*
+ * Measurement hook of the operand re-layout (defined by: none, library plumbing). While ev_pack
+ * (a cudaEvent_t passed as void*) is set, every run of this plan records it on its stream
+ * immediately before the pack kernel; with ev_begin of conv3d_fp8_set_timing_events also set, the
+ * interval ev_pack -> ev_begin is the pack alone. The caller owns the event; NULL stops.
+ * Errors: EINVAL for a NULL plan.
+ */
+conv3d_status conv3d_fp8_set_pack_timing_event(conv3d_fp8_plan_t plan, void *ev_pack);
 
 /*
  * Allocation-free run (no counterpart on the subject page; it exists for callers of this library).
@@ -165,7 +183,10 @@ conv3d_status conv3d_fp8_set_timing_events(conv3d_fp8_plan_t plan, void *ev_begi
  *   Shape, stride and pad are as for conv3d_fp8_plan (default planning, current device); x, w,
  *   the scales and y are as for conv3d_fp8_run. The call is asynchronous on `stream`.
  *   The first call on each device takes the array's device address and sets a kernel attribute;
- *   make that first call before any stream capture on that device.
+ *   make that first call before any stream capture on that device. The address is kept for the
+ *   life of the process: after cudaDeviceReset the entry point must not be called again.
+ *   Each call rewrites everything of the array it reads: the packed operands (the zero halo of
+ *   the padded copy included) and the status word; partials are written before they are read.
  *   All calls share the one array and it keeps the last call's contents: calls whose work overlaps
  *   on the GPU race on it, so serialise them. Kernel-side bounded-wait errors are not reported
  *   here (use a plan and conv3d_fp8_check when you need them).
@@ -180,30 +201,35 @@ conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int W, int K, i
                                      const float *scale_x, const float *scale_w, void *y_ncdhw,
                                      void *stream);
 
-/* Synchronise the plan's device, then report (and clear) its status word: OK or EDEVICE. */
+/* Synchronise the plan's device, then report (and clear) its status word: OK or EDEVICE.
+ * Defined by: none (library plumbing: the status word of the kernels' bounded waits). */
 conv3d_status conv3d_fp8_check(conv3d_fp8_plan_t plan);
 
-/* Fill *info for an existing plan. */
+/* Fill *info for an existing plan. Defined by: none (library plumbing); its tile counts are the
+ * grid_m = ceil(npq / TILE_M) of "Root cause" for this library's tiles. */
 conv3d_status conv3d_fp8_get_info(conv3d_fp8_plan_t plan, conv3d_fp8_plan_info *info);
 
 /*
  * Host-only: what conv3d_fp8_plan_ex would decide for this shape on a GPU with `sm_count` SMs.
  * Touches no device. Same validation and error codes as planning (except ENOMEM / ECUDA).
+ * Defined by: none (library plumbing).
  */
 conv3d_status conv3d_fp8_describe(int N, int C, int D, int H, int W, int K, int T, int R, int S,
                                   const int stride[3], const int pad[3], int sm_count,
                                   const conv3d_fp8_options *opts, conv3d_fp8_plan_info *info);
 
-/* Bytes of device workspace the plan owns (0 for a NULL plan). */
+/* Bytes of device workspace the plan owns (0 for a NULL plan). Defined by: none (plumbing). */
 size_t conv3d_fp8_workspace_size(conv3d_fp8_plan_t plan);
 
-/* Output extents of the plan. */
+/* Output extents of the plan: floor((in + 2*pad - filter) / stride) + 1 per axis. Defined by:
+ * none (plumbing; the plain convolution's output size, which the page assumes). */
 conv3d_status conv3d_fp8_out_dims(conv3d_fp8_plan_t plan, int *Do, int *Ho, int *Wo);
 
-/* Synchronise the plan's device, free its workspace and the plan. NULL is a no-op. */
+/* Synchronise the plan's device, free its workspace and the plan. NULL is a no-op.
+ * Defined by: none (library plumbing). */
 void conv3d_fp8_destroy(conv3d_fp8_plan_t plan);
 
-/* Static description of a status code. */
+/* Static description of a status code. Defined by: none (library plumbing). */
 const char *conv3d_fp8_strerror(conv3d_status status);
 
 /*

@@ -239,3 +239,5 @@ def test_null_plan_entry_points(lib):
     assert capi.conv3d_fp8_workspace_size(None) == 0
     assert lib.conv3d_fp8_check(None) == capi.CONV3D_EINVAL
     capi.conv3d_fp8_destroy(None)
+    assert lib.conv3d_fp8_set_timing_events(None, None, None) == capi.CONV3D_EINVAL
+    assert lib.conv3d_fp8_set_pack_timing_event(None, None) == capi.CONV3D_EINVAL

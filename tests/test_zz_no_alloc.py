@@ -1,12 +1,20 @@
-"""The allocation-free entry point against the planned one.
+"""The allocation-free entry point against the planned one and against the oracle.
 
 conv3d_fp8_run_noalloc is for callers that cannot call cudaMalloc (a framework whose caching
 allocator owns the device memory, a plugin interface with no way to request memory, a loop that
 cannot take cudaFree's synchronisation). It keeps its scratch in one fixed device array that
-every call reuses, so the test makes two calls in a row on different workloads -- the second one
-finds the first one's packed operands and partials still in the array -- and checks each against
-conv3d_fp8_run on a plan, within the parity tolerances of the other GPU tests. It also checks
-that a problem too big for the array is refused before anything runs.
+every call reuses, so the test makes several calls in a row on different workloads, each one
+finding the previous call's packed operands and partials still in the array:
+
+  1. the deep stride-2 layer: split-K partials, and a packed copy of x with no halo that fills
+     the start of the array with nonzero bytes;
+  2. the two-image layer on the padded-grid route: its packed copy of x carries a zero halo, and
+     that halo now lies on the bytes call 1 left behind, so the pack must rewrite it;
+  3. a 48-channel layer on the cp.async gather route, whose packed copy also has a halo;
+  4. the padded-row layer of the subject page (row guard on).
+
+Each result must be bit for bit the planned run's (same kernels, same plan) and within the parity
+gates against the oracle. A problem too big for the array is refused before anything runs.
 
 This file sorts last so that a run stopping at its first failure has run every other test.
 """
@@ -14,10 +22,13 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from fp8_implicit_gemm_gb300 import capi, synth
 from _gpu_common import GpuConv, bits, check_against
 
 pytestmark = pytest.mark.gpu
+
+GATHER_48 = synth.ConvShape(2, 48, 4, 6, 5, 80, name="gather_2x48x4x6x5_k80_s1")
 
 
 def _noalloc(g: GpuConv) -> np.ndarray:
@@ -35,20 +46,27 @@ def _planned(g: GpuConv) -> np.ndarray:
     return out
 
 
-def test_noalloc_matches_planned_run_on_two_calls_in_a_row():
-    # a split-K workload (partials in the array), then the padded-row one (row guard on): the
-    # second call runs on an array still holding the first call's data
+def test_noalloc_matches_planned_run_and_oracle_on_calls_in_a_row():
+    shapes = [(synth.CONFIGS[3], synth.make_config_inputs(3), 2),
+              (synth.CONFIGS[1], synth.make_config_inputs(1), 3),
+              (GATHER_48, synth.make_inputs(GATHER_48, 4848), 1),
+              (synth.CONFIGS[0], synth.make_config_inputs(0), 2)]
     cases = []
-    for cfg in (3, 0):
-        g = GpuConv(synth.CONFIGS[cfg], synth.make_config_inputs(cfg))
-        cases.append((cfg, g, _planned(g)))
     try:
-        outs = [_noalloc(g) for _, g, _ in cases]
-        for (cfg, g, ref), got in zip(cases, outs):
-            ref64 = (ref.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-            check_against(got, ref64, ref, f"no-alloc vs planned, config {cfg}")
+        for shape, inp, route in shapes:
+            g = GpuConv(shape, inp)
+            cases.append((shape, inp, g))
+            assert g.info["route"] == route, (shape.name, g.info["route"])
+        planned = [_planned(g) for _, _, g in cases]
+        got = [_noalloc(g) for _, _, g in cases]
+        for (shape, inp, g), ref, out in zip(cases, planned, got):
+            assert np.array_equal(out, ref), (
+                f"{shape.name}: {int(np.sum(out != ref))} outputs differ from the planned run")
+            y64, yb = oracle.conv3d_fp8(inp["x"].numpy(), inp["w"].numpy(), inp["sx"],
+                                        inp["sw"], shape.stride, shape.pad)
+            check_against(out, y64, yb, f"no-alloc, {shape.name}")
     finally:
-        for _, g, _ in cases:
+        for _, _, g in cases:
             g.close()
 
 
