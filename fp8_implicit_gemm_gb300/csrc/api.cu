@@ -23,6 +23,7 @@ struct conv3d_fp8_plan_s {
   const void* xmap_src = nullptr;  // caller's x the A map was last encoded for (channels-last x)
   CUtensorMap ymap{};              // y as [N][K][dhw] bf16 (TMA-store epilogue)
   const void* ymap_src = nullptr;  // caller's y the map was last encoded for
+  const void* wmap_src = nullptr;  // caller's w the B map was last encoded for (direct route)
   int elem_bytes = 1;              // 1: e4m3 plan (conv3d_fp8_*), 2: bfloat16 plan (conv3d_bf16_*)
   const float* ones = nullptr;     // device fp32 {1, 1}: the scales of a bfloat16 plan's runs
   conv3d_fp8_plan_info info{};
@@ -90,7 +91,7 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
   const long long kg = taps * C;
   conv3d_fp8_options o{};
   if (opts) o = *opts;
-  if (o.route < 0 || o.route > 3 || o.cta_pair < 0 || o.cta_pair > 2 || o.input_layout < 0 ||
+  if (o.route < 0 || o.route > 4 || o.cta_pair < 0 || o.cta_pair > 2 || o.input_layout < 0 ||
       o.input_layout > 1 || o.epilogue < 0 || o.epilogue > 2)
     return CONV3D_EINVAL;
   const bool x_cl = o.input_layout == 1;  // the caller's x is channels-last
@@ -112,6 +113,15 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
                        S <= 129 && o.cta_pair != 1 &&
                        (!x_cl || (pad[0] <= 15 && pad[1] <= 15 && pad[2] <= 15));
   if (o.route == 3 && !grid_ok) return CONV3D_EUNSUPPORTED;
+  // The direct route (one CTA) leaves the weights as the caller holds them: B is read by TMA
+  // tiles of the KCTRS weights viewed as [K][C*T*R*S] (rows of a multiple of 16 bytes), and the
+  // pre-pass writes A = im2col(x) explicitly, [npq][C*T*R*S] in the same (channel, tap) order, for
+  // TMA tiles too. By default it is taken for layers with at most four 128-row tiles and no more
+  // output positions than output channels, where the explicit A (npq rows) is smaller than the
+  // weights (K rows) that the other routes re-lay every run.
+  const long long x_bytes_in = (long long)N * C * D * H * W;
+  const bool direct_ok = !x_cl && kg % 16 == 0 && x_bytes_in < (1LL << 31) && o.cta_pair != 2;
+  if (o.route == 4 && !direct_ok) return CONV3D_EUNSUPPORTED;
   const double grid_overhead =
       (double)(H + 2LL * pad[1]) * (double)(W + 2LL * pad[2]) / ((double)Ho * (double)Wo);
   int route;
@@ -121,8 +131,12 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
     route = kRouteIm2col;
   else if (o.route == 3)
     route = kRouteGrid;
+  else if (o.route == 4)
+    route = kRouteDirect;
   else if (grid_ok && grid_overhead <= 1.3 && npq > kBlockM)
     route = kRouteGrid;
+  else if (direct_ok && npq <= 4LL * kBlockM && npq <= K)
+    route = kRouteDirect;
   else
     route = im2col_ok ? kRouteIm2col : kRouteGather;
   const int a_cb = C % 128 == 0 ? 128 : (C % 64 == 0 ? 64 : 32);
@@ -135,14 +149,16 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
   // A zero-padded channels-last copy of x for the gather route, and for the padded-grid route
   // when the library transposes x anyway; the TMA routes read a channels-last x of the caller
   // directly (no copy at all), and the im2col route's copy needs no halo.
-  const bool keep_copy = !x_cl || route == kRouteGather;
+  const bool direct = route == kRouteDirect;
+  const bool keep_copy = (!x_cl || route == kRouteGather) && !direct;
   const bool halo_on = route == kRouteGather || (route == kRouteGrid && !x_cl);
   const int halo[3] = {halo_on ? pad[0] : 0, halo_on ? pad[1] : 0, halo_on ? pad[2] : 0};
   const long long Dp = D + 2LL * halo[0], Hp = H + 2LL * halo[1], Wp = W + 2LL * halo[2];
   const long long Dg = D + 2LL * pad[0], Hg = H + 2LL * pad[1], Wg = W + 2LL * pad[2];
   const long long y_elems = npq * K;
   const long long x_elems = (long long)N * C * D * H * W;
-  const long long xp_elems = keep_copy ? (long long)N * Dp * Hp * Wp * C : 0;
+  // the direct route's buffer is the explicit A = im2col(x), npq rows of kg bytes
+  const long long xp_elems = keep_copy ? (long long)N * Dp * Hp * Wp * C : (direct ? npq * kg : 0);
   // 32-bit limits of the index arithmetic inside the kernels.
   if (npq + kBlockM >= (1LL << 31) || kg + kBlockK >= (1LL << 31) || y_elems >= (1LL << 40) ||
       x_elems >= (1LL << 40) || xp_elems >= (1LL << 40) || Dg >= (1LL << 30) ||
@@ -158,6 +174,7 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
   // there (N tile 64-256, 4-10%: e.g. 313.6 against 342.2 us on the large layer, 61.9 against
   // 68.2 us on a stride-2 layer of the vae shape).
   if (o.cta_pair == 2 && route == kRouteGather) return CONV3D_EUNSUPPORTED;
+  if (o.cta_pair == 2 && direct) return CONV3D_EUNSUPPORTED;
   const bool pair = route == kRouteGrid || (route == kRouteIm2col && o.cta_pair == 2);
   const int block_m = pair ? 2 * kBlockM : kBlockM;
   // co-resident units: one per SM, or one per CTA pair; a CTA cap given in the options counts
@@ -227,7 +244,7 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
   L.xp_off = 0;
   L.xp_bytes = (size_t)xp_elems;
   L.wp_off = (size_t)round_up((long long)L.xp_off + L.xp_bytes, 256);
-  L.wp_bytes = (size_t)(K * kg);
+  L.wp_bytes = direct ? 0 : (size_t)(K * kg);  // the direct route reads the caller's weights
   L.part_off = (size_t)round_up((long long)L.wp_off + L.wp_bytes, 256);
   L.part_bytes = (size_t)((tiles - full_tiles) * splits * block_n * block_m * 4);
   L.status_off = (size_t)round_up((long long)L.part_off + L.part_bytes, 256);
@@ -253,7 +270,7 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
   info->grid = (int)grid;
   info->sm_count = sm_count;
   info->workspace_bytes = L.total;
-  info->route = route == kRouteGrid ? 3 : (route == kRouteIm2col ? 2 : 1);
+  info->route = route == kRouteGrid ? 3 : route == kRouteIm2col ? 2 : route == kRouteDirect ? 4 : 1;
   info->cta_pair = pair ? 2 : 1;
 
   if (pp) {
@@ -421,17 +438,28 @@ conv3d_status encode_xmap(CUtensorMap* xmap, const ConvParams& p, const void* x_
     return encode_2d(xmap, src, (long long)p.N * p.Dg * p.Hg * p.Wg, p.C, p.a_cb,
                      kBlockM + p.S - 1);
   }
+  // direct route: 128-row tiles of one 128-byte K block of the explicit A = im2col(x)
+  if (p.route == kRouteDirect) return encode_2d(xmap, src, p.npq, p.kg, kBlockK, kBlockM);
   return CONV3D_OK;
 }
 
-// Tensor maps of a plan. B: the packed weights [K][kg]; a box is one K block (128 bytes, or a_cb
-// bytes of one tap on the grid route) of block_n rows (block_n / 2 per CTA of a pair). A: as
-// above, unless it reads the caller's x (then each run encodes it).
-conv3d_status encode_maps(CUtensorMap* wmap, CUtensorMap* xmap, const ConvParams& p) {
+// B tensor map: weights viewed as [K][kg] bytes (the packed K x taps x C copy, or on the direct
+// route the caller's KCTRS w, whose rows hold the same kg bytes in channel-outer order); a box is
+// one K block (128 bytes, or a_cb bytes of one tap on the grid route) of block_n rows
+// (block_n / 2 per CTA of a pair).
+conv3d_status encode_wmap(CUtensorMap* wmap, const ConvParams& p, const void* w) {
   const int b_rows = p.pair ? p.block_n / 2 : p.block_n;
   const int b_cols = p.route == kRouteGrid ? p.a_cb : kBlockK;
-  conv3d_status st = encode_2d(wmap, p.wp, p.K, p.kg, b_cols, b_rows);
-  if (st != CONV3D_OK) return st;
+  return encode_2d(wmap, const_cast<void*>(w), p.K, p.kg, b_cols, b_rows);
+}
+
+// Tensor maps of a plan: B over the packed weights (the direct route encodes it per run, over the
+// caller's w); A as above, unless it reads the caller's x (then each run encodes it).
+conv3d_status encode_maps(CUtensorMap* wmap, CUtensorMap* xmap, const ConvParams& p) {
+  if (p.route != kRouteDirect) {
+    const conv3d_status st = encode_wmap(wmap, p, p.wp);
+    if (st != CONV3D_OK) return st;
+  }
   if (xmap_reads_caller_x(p)) return CONV3D_OK;
   return encode_xmap(xmap, p, nullptr);
 }
@@ -606,6 +634,12 @@ conv3d_status run_impl(conv3d_fp8_plan_t plan, const void* x, const void* w,
     const conv3d_status st = encode_ymap(&plan->ymap, p, y);
     if (st != CONV3D_OK) return st;
     plan->ymap_src = y;
+  }
+  const bool direct = p.route == kRouteDirect;  // B is read from the caller's w as it is
+  if (direct && plan->wmap_src != w) {
+    const conv3d_status st = encode_wmap(&plan->wmap, p, w);
+    if (st != CONV3D_OK) return st;
+    plan->wmap_src = w;
   }
   if (plan->ev_pack && cudaEventRecord(plan->ev_pack, s) != cudaSuccess) return CONV3D_ECUDA;
   if (launch_pack(p, s) != cudaSuccess) return CONV3D_ECUDA;
@@ -907,6 +941,7 @@ extern "C" conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int 
   }
   CUtensorMap wmap{}, xmap{};
   st = encode_maps(&wmap, &xmap, p);
+  if (st == CONV3D_OK && p.route == kRouteDirect) st = encode_wmap(&wmap, p, w);
   if (st != CONV3D_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(p.status, 0, sizeof(int), s) != cudaSuccess) return CONV3D_ECUDA;

@@ -23,6 +23,10 @@ enum : int {
   kRouteGrid = 2,    // stride 1: M indexes the zero-padded grid of the input, so every tap is a
                      // shift along that grid; one TMA load of 128 + S - 1 grid positions feeds
                      // the S taps along W (CTA pairs only)
+  kRouteDirect = 3,  // K_gemm in the caller's KCTRS order (channel outer, tap inner): B by TMA
+                     // tiles of the caller's weights (no re-layout), A by TMA tiles of an
+                     // explicit im2col of x that the pre-pass writes (one CTA; for layers with
+                     // few output positions, whose weights are the bulk of the bytes)
 };
 
 // Source types of the quantiser (and of x when a run quantises it in the pack).
@@ -75,7 +79,8 @@ struct ConvParams {
   const uint8_t* x;      // e4m3 NCDHW, or NDHWC when x_cl (caller's)
   const uint8_t* w;      // e4m3 KCTRS (caller's)
   uint8_t* xp;           // e4m3 [N][Dp][Hp][Wp][C], zero halo (workspace; null when the TMA
-                         // routes read a channels-last x of the caller directly)
+                         // routes read a channels-last x of the caller directly). Direct route:
+                         // the explicit A = im2col(x), [npq][kg] bytes in (channel, tap) order
   uint8_t* wp;           // e4m3 [K][taps][C] (workspace)
   uint16_t* y;           // bf16 NCDHW (caller's)
   const float* scale_x;

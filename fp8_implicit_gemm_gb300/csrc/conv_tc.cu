@@ -8,13 +8,19 @@
 // Warp roles:
 //   warps 0-3  epilogue: TMEM -> registers, scale, bf16, stores masked on row < npq and col < K
 //              (warp w owns TMEM lanes 32w..32w+31, i.e. rows 32w..32w+31 of the tile)
-//   warp 8     TMA loader: per stage one 2D tile of the packed weights (B) and, on the im2col
-//              route, the A tile as 128/a_cb im2col loads (one per tap and channel block) of 128
-//              consecutive output positions from the channels-last input; the TMA unit zero-fills
-//              taps outside the volume and rows past the last image. Also owns the TMEM allocation.
-//   warps 4-7  gather route only (C % 32 != 0 or paddings beyond the im2col corner range): A by
+//   warp 8     TMA loader: per stage one 2D tile of the weights (B: the packed copy, or the
+//              caller's KCTRS w on the direct route) and, on the im2col route, the A tile as
+//              128/a_cb im2col loads (one per tap and channel block) of 128 consecutive output
+//              positions from the channels-last input (the TMA unit zero-fills taps outside the
+//              volume and rows past the last image), or on the direct route one 2D tile of the
+//              explicit im2col of x (rows past npq and K bytes past K_gemm read zero). Also owns
+//              the TMEM allocation.
+//   warps 4-7  gather route (C % 32 != 0 or paddings beyond the im2col corner range): A by
 //              16-byte cp.async gathers from the zero-padded channels-last input into the
-//              128-byte-swizzled stage; rows at or past npq are zero-filled
+//              128-byte-swizzled stage; rows at or past npq are zero-filled.
+//   (direct route: A and B are both plain TMA tiles, of the explicit im2col of x that the
+//              pre-pass wrote and of the caller's KCTRS weights, in the same K order: warps 4-7
+//              stay idle)
 //   warp 9     MMA issuer: 4 x tcgen05.mma (M=128, N=block_n, K=32 bytes) per 128-byte K block;
 //              kind::f8f6f4 on e4m3 bytes, or kind::f16 on bfloat16 pairs (kBf16): the tiles,
 //              stages and descriptors are the same in bytes
@@ -83,7 +89,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     tmem_relinquish();
     if (lane == 0) {
       prefetch_tensormap(&wmap);
-      if (p.route == kRouteIm2col) prefetch_tensormap(&xmap);
+      if (p.route == kRouteIm2col || p.route == kRouteDirect) prefetch_tensormap(&xmap);
       if (p.epi_tma) prefetch_tensormap(&ymap);
     }
   }
@@ -95,6 +101,8 @@ __global__ void __launch_bounds__(kNumThreads, 1)
   pdl_launch_dependents();   // the reduction of split tiles may be scheduled
   const AbortState ab{abort_flag, p.status, p.timeout_ns};
   const bool im2col = p.route == kRouteIm2col;
+  const bool direct = p.route == kRouteDirect;
+  const bool a_tma = im2col || direct;  // A arrives by TMA on the B barrier (no loader warps)
 
   if (warp < 4) {
     // ------------------------------------------------------------------------------ epilogue
@@ -121,7 +129,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
     if (p.epi_tma && threadIdx.x == 0) bulk_wait_group_all();  // stores done before exit
   } else if (warp < 8) {
     // ------------------------------------------------------------------------------ A gather
-    if (!im2col) {
+    if (!a_tma) {
       const int pt = threadIdx.x - 128;
       const int q = pt & 7;    // 16-byte chunk of the 128-byte K block
       const int rb = pt >> 3;  // rows rb, rb+16, ..., rb+112
@@ -217,9 +225,13 @@ __global__ void __launch_bounds__(kNumThreads, 1)
           const int nsub = im2col ? min(kBlockK, p.kg - kk0) / p.a_cb : 0;
           const bool issue = !(skip_first && it == 0) && elect_one();
           if (issue) {
-            mbar_arrive_expect_tx(fullB(stage), b_bytes + (uint32_t)(nsub * p.a_cb * kBlockM));
+            mbar_arrive_expect_tx(fullB(stage), b_bytes + (uint32_t)(nsub * p.a_cb * kBlockM) +
+                                                    (direct ? (uint32_t)kATileBytes : 0u));
             tma_load_2d(sB_u32 + (uint32_t)stage * b_bytes, &wmap, fullB(stage), kk0,
                         un.n_tile * p.block_n);
+            if (direct)  // the full 16 KB box lands (out-of-range rows and bytes as zeros)
+              tma_load_2d(sA_u32 + (uint32_t)stage * kATileBytes, &xmap, fullB(stage), kk0,
+                          un.m_tile * kBlockM);
           }
           const uint32_t a_dst = sA_u32 + (uint32_t)stage * kATileBytes;
           for (int q = 0; q < nsub; ++q) {
@@ -277,7 +289,7 @@ __global__ void __launch_bounds__(kNumThreads, 1)
         for (int kb = un.kb0; kb < un.kb1; ++kb) {
           const int stage = ring.stage;
           const uint32_t ph = ring.phase;
-          if ((!im2col && !wait_bounded_warp(fullA(stage), ph, ab, kStatusWaitFull)) ||
+          if ((!a_tma && !wait_bounded_warp(fullA(stage), ph, ab, kStatusWaitFull)) ||
               !wait_bounded_warp(fullB(stage), ph, ab, kStatusWaitFull)) {
             aborted = true;
             break;

@@ -56,6 +56,38 @@ __host__ __device__ inline void pair_stage_bytes(const ConvParams& p, bool grid,
   }
 }
 
+// Padded-grid route: where the A loads of one CTA's 128 rows of unit `un` start. xrow0 is the
+// first grid position as a row of the [N*Dg*Hg*Wg][C] view of the zero-padded copy (2D loads);
+// (w0, h0, d0, n0) are the unpadded coordinates the im2col traversal starts from (rows past an
+// image's grid continue into the next image, as the traversal does); (tt, tr, cb) is the
+// (t, r, channel block) of the unit's first K group.
+struct GridStart {
+  int xrow0, w0, h0, d0, n0, tt, tr, cb;
+};
+
+__device__ __forceinline__ GridStart grid_start(const ConvParams& p, const Unit& un,
+                                                int row_base) {
+  GridStart s;
+  const int n = un.m_tile / p.tiles_per_image;
+  const int g0 = (un.m_tile - n * p.tiles_per_image) * p.block_m + row_base;
+  s.xrow0 = n * p.Dg * p.Hg * p.Wg + g0;
+  const int plane = p.Hg * p.Wg;
+  int gd = g0 / plane;
+  const int grem = g0 - gd * plane;
+  const int gh = grem / p.Wg;
+  s.w0 = grem - gh * p.Wg - p.pw;
+  s.h0 = gh - p.ph;
+  s.n0 = n + gd / p.Dg;
+  gd = gd % p.Dg;
+  s.d0 = gd - p.pd;
+  const int ncb = p.C / p.a_cb;
+  const int trg = un.kb0 / ncb;
+  s.cb = un.kb0 - trg * ncb;
+  s.tt = trg / p.R;
+  s.tr = trg - s.tt * p.R;
+  return s;
+}
+
 template <bool kRowChk, bool kGrid, bool kBf16>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     conv3d_fp8_tc_pair_kernel(const __grid_constant__ CUtensorMap wmap,
@@ -94,6 +126,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
   const uint32_t rank = cluster_ctarank();
   const bool leader = rank == 0;
   const uint32_t leader_bars = map_to_cta(bars_u32, 0);  // the leader's barriers, cluster window
+  const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
+  const int row_base = (int)rank * kBlockM;  // this CTA's rows within the 256-row unit
+
+  // The TMA warp's first unit and where its loads start, computed before the set-up barriers:
+  // the first reads of the kernel parameters and the integer divisions then overlap the barrier
+  // initialisation, the TMEM allocation (done by the MMA warp) and the cluster barrier, instead
+  // of delaying the first copy by about a microsecond after them.
+  Unit tma_un0{};
+  GridStart tma_gs0{};
+  if (warp == 8 && cluster_id < p.num_units) {
+    tma_un0 = decode_unit(p, cluster_id);
+    if (kGrid) tma_gs0 = grid_start(p, tma_un0, row_base);
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -109,14 +154,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
     *last_buf = -1;
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == 9) {
     tmem_alloc_pair(smem_u32(tmem_slot), (uint32_t)p.tmem_cols);
     tmem_relinquish_pair();
-    if (lane == 0) {
-      prefetch_tensormap(&wmap);
-      prefetch_tensormap(&xmap);
-      if (p.epi_tma) prefetch_tensormap(&ymap);
-    }
+  }
+  if (warp == 8 && lane == 0) {
+    prefetch_tensormap(&wmap);
+    prefetch_tensormap(&xmap);
+    if (p.epi_tma) prefetch_tensormap(&ymap);
   }
   tc_fence_before();
   __syncthreads();
@@ -126,8 +171,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
   pdl_wait_primary();        // the pack's output (launched dependent on it), complete and visible
   pdl_launch_dependents();   // the reduction of split tiles may be scheduled
   const AbortState ab{abort_flag, p.status, p.timeout_ns};
-  const int cluster_id = blockIdx.x >> 1, num_clusters = gridDim.x >> 1;
-  const int row_base = (int)rank * kBlockM;  // this CTA's rows within the 256-row unit
 
   // The last unit's epilogue is not hidden behind any MMA: unless the TMA-store epilogue is on,
   // warps 4-7 take the second half of its columns. Warps 0-3 hand it over at named barrier 3
@@ -194,32 +237,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
       Ring ring;
       const bool skip_first = (p.debug_flags & 1) != 0;
       for (int u = cluster_id; u < p.num_units; u += num_clusters) {
-        const Unit un = decode_unit(p, u);
+        const Unit un = u == cluster_id ? tma_un0 : decode_unit(p, u);
         bool aborted = false;
         if (kGrid) {
-          // first padded-grid position of this CTA's 128 rows: as a row of the [N*Dg*Hg*Wg][C]
-          // view of the zero-padded copy (2D loads), or as the unpadded coordinates the im2col
-          // traversal starts from (rows past an image's grid continue into the next image, as
-          // the traversal does)
-          const int n = un.m_tile / p.tiles_per_image;
-          const int g0 = (un.m_tile - n * p.tiles_per_image) * p.block_m + row_base;
-          const int xrow0 = n * p.Dg * p.Hg * p.Wg + g0;
-          const int plane = p.Hg * p.Wg;
-          int gd = g0 / plane;
-          const int grem = g0 - gd * plane;
-          const int gh = grem / p.Wg;
-          const int w0 = grem - gh * p.Wg - p.pw, h0 = gh - p.ph;
-          const int n0 = n + gd / p.Dg;
-          gd = gd % p.Dg;
-          const int d0 = gd - p.pd;
+          const GridStart gs = u == cluster_id ? tma_gs0 : grid_start(p, un, row_base);
+          const int xrow0 = gs.xrow0, w0 = gs.w0, h0 = gs.h0, d0 = gs.d0, n0 = gs.n0;
           const int ncb = p.C / p.a_cb;
-          int tt, tr, cb;  // (t, r, channel block) of the unit's first group
-          {
-            const int trg = un.kb0 / ncb;
-            cb = un.kb0 - trg * ncb;
-            tt = trg / p.R;
-            tr = trg - tt * p.R;
-          }
+          int tt = gs.tt, tr = gs.tr, cb = gs.cb;  // (t, r, channel block) of the current group
           const uint32_t tx = 2u * ((uint32_t)(kBlockM + p.S - 1) * (uint32_t)p.a_cb +
                                     (uint32_t)(p.S * half_n * p.a_cb));
           for (int g = un.kb0; g < un.kb1; ++g) {
@@ -400,7 +424,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kNumThreads, 1)
   __syncthreads();
   cluster_sync();  // neither CTA leaves while the other may still signal or read its memory
   tc_fence_after();
-  if (warp == 8) tmem_dealloc_pair(tmem_base, (uint32_t)p.tmem_cols);
+  if (warp == 9) tmem_dealloc_pair(tmem_base, (uint32_t)p.tmem_cols);
 }
 
 size_t conv_pair_smem_bytes(const ConvParams& p) {

@@ -186,7 +186,96 @@ static cudaError_t launch_tiled_ct(const ConvParams& p, const PackPlan& q, long 
   return cudaGetLastError();
 }
 
+// Direct route: the explicit A = im2col(x), [npq][kg] bytes with K_gemm in the caller's KCTRS
+// order: A[row][e] = x[n, c, od*sd + t - pd, oh*sh + r - ph, ow*sw + s - pw] for element
+// e = c*taps + tap, zero where the tap falls outside the volume. The weights are not touched: the
+// implicit GEMM reads them as they are. A thread writes one 16-byte chunk of a row; consecutive
+// threads take consecutive rows of the same chunk, so the (c, t, r, s) walk of a warp is uniform
+// and each of its loads reads 32 neighbouring output positions' taps. kType: kSrcE4m3 copies the
+// elements (e4m3 bytes, or the BF16 twin's bfloat16 halves); kSrcF32 / kSrcBf16 quantise fp32 /
+// bfloat16 values with the device scale *scale_x. kEl: bytes of an output element.
+template <int kType, int kEl>
+__global__ void __launch_bounds__(256) im2col_kernel(ConvParams p) {
+  pdl_launch_dependents();  // the implicit GEMM may start its prologue while this runs
+  constexpr bool kQuant = kType != kSrcE4m3;
+  constexpr int el = kEl;
+  constexpr int per = 16 / el;  // elements per 16-byte chunk
+  const int cpr = p.kg / 16;                 // chunks per row
+  const long long total = (long long)p.npq * cpr;
+  const int taps = p.taps, RS = p.R * p.S, HW = p.H * p.W, DHW = p.D * HW;
+  const int c_el = p.C / el;  // channels
+  const float qs = kQuant ? __ldg(p.scale_x) : 1.0f;
+  for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < total;
+       g += (long long)gridDim.x * blockDim.x) {
+    const int row = (int)(g % p.npq);
+    const int q = (int)(g / p.npq);
+    const int n = row / p.dhw;
+    const int pix = row - n * p.dhw;
+    const int ow = pix % p.Wo;
+    const int t2 = pix / p.Wo;
+    const int oh = t2 % p.Ho;
+    const int od = t2 / p.Ho;
+    const int d0 = od * p.sd - p.pd, h0 = oh * p.sh - p.ph, w0 = ow * p.sw - p.pw;
+    const long long img = (long long)n * c_el * DHW;  // x index of x[n, 0, 0, 0, 0]
+    const int e0 = q * per;
+    int c = e0 / taps, tap = e0 - c * taps;
+    int t = tap / RS;
+    const int rs = tap - t * RS;
+    int r = rs / p.S, s = rs - r * p.S;
+    uint32_t v[4] = {0u, 0u, 0u, 0u};
+    float f[per];
+#pragma unroll
+    for (int j = 0; j < per; ++j) {
+      const bool in = (unsigned)(d0 + t) < (unsigned)p.D && (unsigned)(h0 + r) < (unsigned)p.H &&
+                      (unsigned)(w0 + s) < (unsigned)p.W;
+      const long long idx = img + (long long)c * DHW + ((d0 + t) * p.H + (h0 + r)) * p.W + (w0 + s);
+      if (kQuant) {
+        f[j] = in ? src_value(p.x, kType, idx) : 0.0f;
+      } else if (in) {
+        const uint32_t e = el == 1 ? (uint32_t)__ldg(p.x + idx)
+                                   : (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(p.x) + idx);
+        v[(j * el) >> 2] |= e << (((j * el) & 3) * 8);
+      }
+      if (++tap == taps) {
+        tap = t = r = s = 0;
+        ++c;
+      } else if (++s == p.S) {
+        s = 0;
+        if (++r == p.R) {
+          r = 0;
+          ++t;
+        }
+      }
+    }
+    if constexpr (kQuant) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        v[k] = quant4(f[4 * k], f[4 * k + 1], f[4 * k + 2], f[4 * k + 3], qs);
+    }
+    *reinterpret_cast<uint4*>(p.xp + (long long)row * p.kg + (long long)q * 16) =
+        make_uint4(v[0], v[1], v[2], v[3]);
+  }
+}
+
 cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream) {
+  if (p.route == kRouteDirect) {  // the explicit im2col of x; the weights stay as they are
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long total = (long long)p.npq * (p.kg / 16);
+    long long blocks = (total + 255) / 256;
+    if (blocks > (long long)sms * 16) blocks = (long long)sms * 16;
+    if (blocks < 1) blocks = 1;
+    if (p.x_src_type == kSrcF32)
+      im2col_kernel<kSrcF32, 1><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    else if (p.x_src_type == kSrcBf16)
+      im2col_kernel<kSrcBf16, 1><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    else if (p.elem_bytes == 2)
+      im2col_kernel<kSrcE4m3, 2><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    else
+      im2col_kernel<kSrcE4m3, 1><<<(unsigned)blocks, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
   const PackPlan q = pack_plan(p);
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);

@@ -64,7 +64,13 @@ typedef struct {
                             only: M runs over the zero-padded grid of the input and one TMA
                             im2col load of 128 + S - 1 grid positions feeds the S taps along W
                             (EUNSUPPORTED unless every stride is 1, C % 32 == 0, S <= 129 and
-                            every pad <= 15) */
+                            every pad <= 15); 4: direct route, one CTA: K_gemm in the KCTRS
+                            order of the caller's w, which is read as it is by TMA tiles (no
+                            weight re-layout), while a pre-pass writes A = im2col(x) explicitly
+                            ([npq][C*T*R*S] bytes in the plan's workspace) for TMA tiles too; the
+                            default for GEMMs of at most four 128-row tiles with npq <= K
+                            (EUNSUPPORTED with a channels-last x, on CTA pairs, or when x holds
+                            2^31 bytes or more) */
     int cta_pair;        /* 0: the library chooses; 1: one CTA per 128-row tile; 2: CTA pairs on
                             256-row tiles (tcgen05 cta_group::2; not on the gather route) */
     int input_layout;    /* 0: x is NCDHW (the library transposes it to channels-last every
@@ -99,7 +105,8 @@ typedef struct {
     int grid;                 /* persistent CTAs launched by the main kernel (2 per pair) */
     int sm_count;
     size_t workspace_bytes;   /* device workspace the plan owns */
-    int route;                /* 1: gather, 2: TMA im2col, 3: padded grid (as in options) */
+    int route;                /* 1: gather, 2: TMA im2col, 3: padded grid, 4: direct (as in
+                                 options) */
     int cta_pair;             /* 1: one CTA per tile, 2: CTA pairs (as in options) */
     int full_tiles;           /* tiles computed whole; the other m_tiles*n_tiles - full_tiles
                                  are split `splits` ways. With splits == 1 every tile is whole;

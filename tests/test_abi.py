@@ -53,10 +53,12 @@ def test_describe_configs(lib):
     assert npq == [288, 3840, 65536, 128, 244800]
     assert [i["k_gemm"] for i in infos] == [2592, 1728, 3456, 13824, 6912]
     # stride-1 layers whose padded output grid adds at most 30% rows take the padded-grid route,
-    # on CTA pairs (256-row tiles); the others the TMA im2col route on one CTA (128-row tiles)
+    # on CTA pairs (256-row tiles); the deep layer (one 128-row tile, 512 output channels) the
+    # direct route on one CTA (the weights are read as they are); the first layer the TMA im2col
+    # route on one CTA
     assert [i["cta_pair"] for i in infos] == [1, 2, 2, 1, 2]
     assert [i["block_m"] for i in infos] == [128, 256, 256, 128, 256]
-    assert [i["route"] for i in infos] == [2, 3, 3, 2, 3]
+    assert [i["route"] for i in infos] == [2, 3, 3, 4, 3]
     # grid route: N * ceil(Do*Hp*Wp / 256) tiles, (t, r, channel block) groups as K blocks
     assert [i["m_tiles"] for i in infos] == [3, 2 * 10, 273, 1, 990]
     assert [i["k_blocks"] for i in infos] == [21, 9, 9, 108, 18]
@@ -87,7 +89,7 @@ def test_describe_routes(lib):
     assert capi.conv3d_fp8_describe_status(1, 128, 4, 8, 8, 64, 3, 3, 3, 1, 1, 152, route=3,
                                            cta_pair=1) == capi.CONV3D_EUNSUPPORTED  # one CTA
     assert _describe(synth.CONFIGS[0], route=3)["route"] == 3
-    odd = synth.ConvShape(1, 48, 4, 4, 4, 16)
+    odd = synth.ConvShape(1, 48, 8, 8, 8, 16)                   # npq > K: not direct
     assert _describe(odd)["route"] == 1                         # C % 32 != 0 -> gather
     assert capi.conv3d_fp8_describe_status(1, 48, 4, 4, 4, 16, 3, 3, 3, 1, 1, 152,
                                            route=2) == capi.CONV3D_EUNSUPPORTED
@@ -99,6 +101,33 @@ def test_describe_routes(lib):
     s = synth.CONFIGS[2]
     ws = {r: _describe(s, route=r, splits=1)["workspace_bytes"] for r in (1, 2, 3)}
     assert ws[1] > ws[2] and ws[3] == ws[1]
+
+
+def test_describe_direct_route(lib):
+    # any NCDHW shape can be forced onto it; it runs on one CTA, re-lays no weights (its
+    # workspace holds the explicit im2col of x, npq rows of C*T*R*S bytes, instead) and keeps
+    # K_gemm in the KCTRS order of the caller's weights
+    for s in synth.CONFIGS:
+        i = _describe(s, route=4)
+        kg = s.C * s.T * s.R * s.S
+        assert i["route"] == 4 and i["cta_pair"] == 1 and i["block_m"] == 128
+        assert i["k_blocks"] == -(-kg // 128)
+        assert i["workspace_bytes"] >= i["npq"] * kg
+    deep = synth.CONFIGS[3]
+    w_bytes = deep.K * deep.C * 27
+    a_bytes = 128 * deep.C * 27
+    assert (_describe(deep, route=2)["workspace_bytes"] - _describe(deep, route=4)["workspace_bytes"]
+            >= w_bytes - a_bytes)
+    # not with a channels-last x, not on CTA pairs
+    assert capi.conv3d_fp8_describe_status(1, 512, 4, 16, 16, 512, 3, 3, 3, 2, 1, 152, route=4,
+                                           input_layout=1) == capi.CONV3D_EUNSUPPORTED
+    assert capi.conv3d_fp8_describe_status(1, 512, 4, 16, 16, 512, 3, 3, 3, 2, 1, 152, route=4,
+                                           cta_pair=2) == capi.CONV3D_EUNSUPPORTED
+    # by default only for small GEMMs (at most four 128-row tiles) with no more output positions
+    # than output channels (the explicit A is then no bigger than the weights)
+    assert _describe(synth.ConvShape(1, 512, 4, 16, 16, 512, stride=2))["route"] == 4
+    assert _describe(synth.ConvShape(1, 512, 4, 16, 16, 64, stride=2))["route"] == 2  # npq > K
+    assert _describe(synth.ConvShape(1, 512, 8, 32, 32, 512, stride=2))["route"] == 2  # npq 2048
 
 
 def test_describe_pair_rules(lib):
@@ -175,11 +204,13 @@ def test_describe_bf16_twin(lib):
         else:
             assert b["k_blocks"] == -(-2 * b["k_gemm"] // 128)
     # C in 16-byte units: 8 bfloat16 channels suffice (gather route), 4 do not
-    assert d(synth.ConvShape(1, 8, 4, 4, 4, 16))["route"] == 1
+    assert d(synth.ConvShape(1, 8, 8, 8, 8, 8))["route"] == 1
     assert capi.conv3d_bf16_describe_status(1, 4, 4, 4, 4, 16, 3, 3, 3, 1, 1,
                                             152) == capi.CONV3D_EUNSUPPORTED
     # 16 channels = 32 bytes: the TMA routes apply
-    assert d(synth.ConvShape(1, 16, 4, 8, 8, 16))["route"] in (2, 3)
+    assert d(synth.ConvShape(1, 16, 8, 8, 8, 16))["route"] in (2, 3)
+    # the direct route's explicit im2col holds two-byte elements in the same KCTRS order
+    assert d(synth.ConvShape(1, 8, 2, 4, 4, 64))["route"] == 4
 
 
 def test_describe_tma_epilogue(lib):

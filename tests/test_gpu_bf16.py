@@ -23,7 +23,8 @@ def check_bf16(gpu_bits, y64, yb, what):
 pytestmark = pytest.mark.gpu
 
 KERNELS = {"gather-1cta": dict(route=1, cta_pair=1), "im2col-1cta": dict(route=2, cta_pair=1),
-           "im2col-pair": dict(route=2, cta_pair=2), "grid-pair": dict(route=3, cta_pair=2)}
+           "im2col-pair": dict(route=2, cta_pair=2), "grid-pair": dict(route=3, cta_pair=2),
+           "direct-1cta": dict(route=4, cta_pair=1)}
 
 
 def _oracle_full(shape, inp):
@@ -143,7 +144,8 @@ def test_repeated_launches_write_every_element_once(cfg, repeats):
         g.close()
 
 
-@pytest.mark.parametrize("kernel", [dict(cta_pair=1, route=2), dict(cta_pair=2, route=3)])
+@pytest.mark.parametrize("kernel", [dict(cta_pair=1, route=2), dict(cta_pair=2, route=3),
+                                    dict(cta_pair=1, route=4)])
 def test_bounded_wait_reports_instead_of_hanging(kernel):
     shape = synth.CONFIGS[0]
     inp = synth.make_config_inputs_bf16(0)

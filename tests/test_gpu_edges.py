@@ -31,7 +31,7 @@ EDGES = [
 ]
 KERNELS = {"auto": {}, "gather-1cta": dict(route=1, cta_pair=1),
            "im2col-1cta": dict(route=2, cta_pair=1), "im2col-pair": dict(route=2, cta_pair=2),
-           "grid-pair": dict(route=3, cta_pair=2)}
+           "grid-pair": dict(route=3, cta_pair=2), "direct-1cta": dict(route=4, cta_pair=1)}
 
 
 @pytest.mark.parametrize("kernel", list(KERNELS))

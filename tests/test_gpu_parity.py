@@ -34,7 +34,8 @@ ROUTES = {"gather": 1, "im2col": 2, "grid": 3}
 # (route, kernel): the cp.async gather route runs on one CTA, im2col on one CTA or on CTA pairs,
 # the padded-grid route on CTA pairs
 KERNELS = {"gather-1cta": dict(route=1, cta_pair=1), "im2col-1cta": dict(route=2, cta_pair=1),
-           "im2col-pair": dict(route=2, cta_pair=2), "grid-pair": dict(route=3, cta_pair=2)}
+           "im2col-pair": dict(route=2, cta_pair=2), "grid-pair": dict(route=3, cta_pair=2),
+           "direct-1cta": dict(route=4, cta_pair=1)}
 
 
 @pytest.mark.parametrize("kernel", list(KERNELS))
@@ -65,7 +66,8 @@ def _large_reference(cfg):
 
 
 @pytest.mark.parametrize("cfg,kernel", [(c, k) for c in (2, 4)
-                                        for k in ("auto", "im2col-1cta", "im2col-pair")])
+                                        for k in ("auto", "im2col-1cta", "im2col-pair")] +
+                         [(2, "direct-1cta")])
 def test_config_full_output_large(cfg, kernel):
     shape = synth.CONFIGS[cfg]
     inp, y64, yb = _large_reference(cfg)
@@ -124,6 +126,12 @@ def test_odd_shapes_grid_route(i):
     assert info["route"] == 3
 
 
+@pytest.mark.parametrize("i", range(len(ODD)))
+def test_odd_shapes_direct_route(i):
+    res, info = _full_case(ODD[i], 77 + i, route=4)
+    assert info["route"] == 4 and info["cta_pair"] == 1
+
+
 @pytest.mark.parametrize("i", [i for i, s in enumerate(ODD) if s.C % 32 == 0])
 def test_odd_shapes_one_cta(i):
     res, info = _full_case(ODD[i], 77 + i, cta_pair=1)
@@ -176,7 +184,7 @@ def test_tail_tiles_split_along_k(kernel):
 # Channels-last input (input_layout = 1): the TMA routes read the caller's NDHWC x directly (the
 # padded-grid route through an im2col traversal of its zero-padded grid), the gather route copies
 # it into its zero-padded buffer.
-@pytest.mark.parametrize("kernel", list(KERNELS))
+@pytest.mark.parametrize("kernel", [k for k in KERNELS if k != "direct-1cta"])
 @pytest.mark.parametrize("cfg", [0, 1, 3])
 def test_channels_last_input_full_output(cfg, kernel):
     if kernel == "grid-pair" and cfg == 3:

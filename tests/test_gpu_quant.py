@@ -131,7 +131,7 @@ def _fused_run(shape, x, w, sw, **opts):
 
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("route", [0, 1, 2])
+@pytest.mark.parametrize("route", [0, 1, 2, 4])
 @pytest.mark.parametrize("cfg", [0, 1, 3])
 def test_fused_run_full_output(cfg, route, dtype):
     shape, x, w, sw = _fused_inputs(cfg, dtype)

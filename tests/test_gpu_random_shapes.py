@@ -19,7 +19,7 @@ from _gpu_common import GpuConv, GpuConvBf16, bits, check_against, FROB_TOL_BF16
 pytestmark = pytest.mark.gpu
 
 KERNELS = [dict(route=1, cta_pair=1), dict(route=2, cta_pair=1), dict(route=2, cta_pair=2),
-           dict(route=3, cta_pair=2)]
+           dict(route=3, cta_pair=2), dict(route=4, cta_pair=1)]
 MAX_MACS = 1.5e8  # keeps the oracle to a fraction of a second a case
 
 

@@ -68,7 +68,7 @@ def test_repeated_launches_write_every_element_once(cfg):
 
 
 @pytest.mark.parametrize("kernel", [dict(cta_pair=1, route=2), dict(cta_pair=2, route=2),
-                                    dict(cta_pair=2, route=3)])
+                                    dict(cta_pair=2, route=3), dict(cta_pair=1, route=4)])
 def test_bounded_wait_reports_instead_of_hanging(kernel):
     """A stage that never arrives: the MMA warp's bounded wait runs out, the kernel winds down
     (on CTA pairs: both CTAs), the status word says so, and the context stays usable."""
