@@ -267,9 +267,13 @@ def cpu_oracle_sample(inp, shape, target_s: float, seed: int, min_points: int = 
 
 
 # ------------------------------------------------------------------------------ per workload
-def pack_alg_bytes(fig, packs_x: bool) -> int:
+def pack_alg_bytes(fig, packs_x: bool, route: int = 0, elem_bytes: int = 1) -> int:
     """Compulsory bytes of the operand re-layout: the weights read and written once, and x read
-    and its channels-last interior written once when the run transposes x."""
+    and its channels-last interior written once when the run transposes x. On the direct route
+    (4) the weights stay as they are and the pre-pass reads x and writes the explicit im2col of
+    x once (npq rows of C*T*R*S elements)."""
+    if route == 4:
+        return fig["x_bytes"] + elem_bytes * fig["npq"] * fig["k_gemm"]
     return 2 * fig["w_bytes"] + (2 * fig["x_bytes"] if packs_x else 0)
 
 
@@ -351,7 +355,7 @@ def measure_config(index: int, inp, dev, stream, flush, fp8_peak: float, hbm_pea
                         statistics.median(pack))
     roof = roofline_of(fig, k_ms, fp8_peak, hbm_peak)
     step_roof = roofline_of(fig, s_ms, fp8_peak, hbm_peak)
-    pbytes = pack_alg_bytes(fig, True)
+    pbytes = pack_alg_bytes(fig, True, info["route"])
     split = info["full_tiles"] < info["m_tiles"] * info["n_tiles"]
     return {
         "workload": shape.name, "config_index": index,
@@ -603,8 +607,12 @@ def run_ours(args):
     roof["step_roofline_frac"] = round(max(t_flop, t_hbm) / (mean_step_ms * 1e-3), 4)
     # the operand re-layout of the same steps (HBM-bound): the pack alone, by the library's events
     packs_x = not channels_last or info["route"] == 1
-    p_bytes = (pack_alg_bytes(fig, packs_x) if not quant else
-               2 * fig["w_bytes"] + x.numel() * x.element_size() + fig["x_bytes"])
+    if not quant:
+        p_bytes = pack_alg_bytes(fig, packs_x, info["route"], 2 if bf16 else 1)
+    elif info["route"] == 4:  # the pre-pass quantises x into the explicit im2col
+        p_bytes = x.numel() * x.element_size() + fig["npq"] * fig["k_gemm"]
+    else:
+        p_bytes = 2 * fig["w_bytes"] + x.numel() * x.element_size() + fig["x_bytes"]
     p_ms = statistics.mean(pack_ms)
     pack = {"kernel": "pack_kernel", "alg_bytes": int(p_bytes), "ms": round(p_ms, 5),
             "achieved": round(p_bytes / (p_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
