@@ -37,6 +37,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 DEFAULT_CONFIG = 4
+# --route: the planner's choice, or one route forced (conv3d_fp8_options.route)
+ROUTES = {"auto": 0, "gather": 1, "im2col": 2, "grid": 3, "direct": 4}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_PER_BF16 = 2.0  # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 METRIC = "conv3d fp8 TFLOP/s and % of FP8/HBM roofline at 1 GB300"
@@ -407,7 +409,8 @@ def run_ours(args):
 
     make_plan = capi.conv3d_bf16_plan if bf16 else capi.conv3d_fp8_plan
     plan = make_plan(shape.N, shape.C, shape.D, shape.H, shape.W, shape.K, shape.T, shape.R,
-                     shape.S, shape.stride, shape.pad, dev, input_layout=1 if channels_last else 0)
+                     shape.S, shape.stride, shape.pad, dev, input_layout=1 if channels_last else 0,
+                     route=ROUTES[args.route])
     info = capi.conv3d_fp8_get_info(plan)
     stream = torch.cuda.current_stream()
     x = x_lib.to(dev)
@@ -614,7 +617,9 @@ def run_ours(args):
     else:
         p_bytes = 2 * fig["w_bytes"] + x.numel() * x.element_size() + fig["x_bytes"]
     p_ms = statistics.mean(pack_ms)
-    pack = {"kernel": "pack_kernel", "alg_bytes": int(p_bytes), "ms": round(p_ms, 5),
+    pack = {"kernel": "im2col_kernel" if info["route"] == 4 else
+            ("pack_x_tiled_kernel + pack items" if quant else "pack_kernel"),
+            "alg_bytes": int(p_bytes), "ms": round(p_ms, 5),
             "achieved": round(p_bytes / (p_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "peak": round(hbm_peak, 1), "frac": round(p_bytes / (p_ms * 1e-3) / 1e9 / hbm_peak, 4),
             "timing": "library events before the pack and before the main kernel, same steps as "
@@ -784,6 +789,8 @@ def main():
                     help="input type: the e4m3 path, or its BF16-input twin")
     ap.add_argument("--quantize-x", choices=["fp32", "bf16"], default=None,
                     help="hand x over as fp32 / bf16 values: each step quantises it on the device")
+    ap.add_argument("--route", choices=list(ROUTES), default="auto",
+                    help="how A reaches the tensor cores: the library's choice, or one route forced")
     ap.add_argument("--input-layout", choices=["ncdhw", "ndhwc"], default="ncdhw",
                     help="layout of x handed to the library (y is NCDHW either way)")
     args = ap.parse_args()

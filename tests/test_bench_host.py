@@ -1,0 +1,56 @@
+"""Host-side arithmetic of bench.py, on the CPU: problem figures (GEMM view, FLOP, bytes), the
+roofline bound and fraction, and the algorithmic bytes of the operand re-layout per route."""
+import os
+import sys
+
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+from fp8_implicit_gemm_gb300 import synth  # noqa: E402
+
+
+def test_problem_figures_match_the_workloads():
+    figs = [bench.problem_figures(s) for s in synth.CONFIGS]
+    assert [f["npq"] for f in figs] == [288, 3840, 65536, 128, 244800]
+    assert [f["k_gemm"] for f in figs] == [2592, 1728, 3456, 13824, 6912]
+    # FLOP = 2 npq K K_gemm, padding taps counted
+    assert figs[2]["flop"] == 2.0 * 65536 * 128 * 3456
+    assert round(figs[4]["flop"] / 1e9, 1) == 866.3
+    # bytes: x and w in e4m3 (one byte), y in bf16
+    s = synth.CONFIGS[4]
+    assert figs[4]["x_bytes"] == s.N * s.C * s.D * s.H * s.W
+    assert figs[4]["w_bytes"] == s.K * s.C * 27
+    assert figs[4]["y_bytes"] == 2 * 244800 * 256
+    assert figs[4]["alg_bytes"] == figs[4]["x_bytes"] + figs[4]["w_bytes"] + figs[4]["y_bytes"]
+    # the BF16 twin's inputs take two bytes an element
+    b = bench.problem_figures(s, 2)
+    assert b["x_bytes"] == 2 * figs[4]["x_bytes"] and b["w_bytes"] == 2 * figs[4]["w_bytes"]
+
+
+def test_roofline_picks_the_slower_bound():
+    fp8, hbm = 3859.2, 6685.1
+    big = bench.problem_figures(synth.CONFIGS[4])
+    deep = bench.problem_figures(synth.CONFIGS[3])
+    r = bench.roofline_of(big, 0.2298, fp8, hbm)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["achieved"] == pytest.approx(big["flop"] / 0.2298e-3 / 1e12, rel=1e-3)
+    assert r["frac"] == pytest.approx(r["achieved"] / fp8, abs=1e-4)
+    r = bench.roofline_of(deep, 0.0164, fp8, hbm)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert r["achieved"] == pytest.approx(deep["alg_bytes"] / 0.0164e-3 / 1e9, rel=1e-3)
+    # a time at the roofline reads a fraction of one
+    t_roof_ms = max(big["flop"] / (fp8 * 1e12), big["alg_bytes"] / (hbm * 1e9)) * 1e3
+    assert bench.roofline_of(big, t_roof_ms, fp8, hbm)["frac"] == pytest.approx(1.0, abs=1e-3)
+
+
+def test_pack_bytes_per_route():
+    big = bench.problem_figures(synth.CONFIGS[4])
+    deep = bench.problem_figures(synth.CONFIGS[3])
+    # transpose of x plus the weight re-layout: each read once and written once
+    assert bench.pack_alg_bytes(big, True) == 2 * big["x_bytes"] + 2 * big["w_bytes"]
+    # a channels-last x read by TMA directly: only the weights move
+    assert bench.pack_alg_bytes(big, False) == 2 * big["w_bytes"]
+    # direct route: x read, the explicit im2col (npq x K_gemm elements) written, weights untouched
+    assert bench.pack_alg_bytes(deep, True, 4) == deep["x_bytes"] + 128 * 13824
+    assert bench.pack_alg_bytes(deep, True, 4, 2) == deep["x_bytes"] + 2 * 128 * 13824
