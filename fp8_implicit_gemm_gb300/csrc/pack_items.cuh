@@ -22,7 +22,9 @@ namespace c3d {
 //   + halo_side_items     16-byte zero chunks of the W-halo pixels of interior rows
 //   + w_items             16 channels of one tap of one filter
 // Pixels (or pixel groups) run fastest across threads, so each load of a warp is a contiguous run
-// along W of the NCDHW input.
+// along W of the NCDHW input; with 16 or more 16-byte channel chunks a pixel, the 16-pixel items
+// run their channel chunk fastest instead, so that each store of a warp writes whole pixel rows
+// of the channels-last copy.
 constexpr long long kWTileBytes = 16384;  // shared-memory buffer of one weight tile
 
 struct PackPlan {
@@ -35,6 +37,10 @@ struct PackPlan {
   bool quad;  // e4m3 and W % 4 == 0: 4-pixel items
   bool two;   // bfloat16 and W % 2 == 0: 2-pixel items
   bool copy;  // x is channels-last already: 16-byte chunk copies
+  bool cfast; // hex items with the channel chunk fastest across threads (>= 16 chunks a pixel):
+              // a warp's stores of one instruction cover whole pixel rows (C = 256: large layer
+              // step 262.4 -> 260.9 us); below 16 chunks the pixel-group-fastest order measured
+              // faster (vae layer, C = 128: 32.3 against 33.6 us)
 };
 
 __host__ __device__ inline PackPlan pack_plan(const ConvParams& p) {
@@ -44,6 +50,7 @@ __host__ __device__ inline PackPlan pack_plan(const ConvParams& p) {
   q.quad = !q.copy && p.elem_bytes == 1 && (p.W % 4) == 0;
   q.hex = q.quad && (p.W % 16) == 0;
   q.two = !q.copy && p.elem_bytes == 2 && (p.W % 2) == 0;
+  q.cfast = q.hex && cq >= 16;
   const int per_row = q.hex ? p.W / 16 : q.quad ? p.W / 4 : (q.two ? p.W / 2 : p.W);
   q.x_items = p.xp == nullptr ? 0 : (long long)p.N * p.D * p.H * cq * per_row;
   const long long halo_rows_per_image = (long long)p.Dp * p.Hp - (long long)p.D * p.H;
@@ -152,12 +159,22 @@ __device__ __forceinline__ void pack_item(const ConvParams& p, const PackPlan& q
       *reinterpret_cast<uint4*>(dst_row + (long long)wi * p.C) = make_uint4(v[0], v[1], v[2], v[3]);
     }
   } else if (g < e1) {
-    // interior: (pixel group fastest, then channel chunk, then (n, d, h) row)
+    // interior: (pixel group fastest, then channel chunk, then (n, d, h) row), or with the
+    // channel chunk fastest (q.cfast)
     const int per_row = q.hex ? p.W / 16 : q.quad ? p.W / 4 : p.W;
-    const int wi = (int)(g % per_row);
-    const long long rest = g / per_row;
-    const int cq = (int)(rest % cq_n);
-    const long long row = rest / cq_n;  // n*D*H + d*H + h
+    int wi, cq;
+    long long row;  // n*D*H + d*H + h
+    if (q.cfast) {
+      cq = (int)(g % cq_n);
+      const long long rest = g / cq_n;
+      wi = (int)(rest % per_row);
+      row = rest / per_row;
+    } else {
+      wi = (int)(g % per_row);
+      const long long rest = g / per_row;
+      cq = (int)(rest % cq_n);
+      row = rest / cq_n;
+    }
     const int h = (int)(row % p.H);
     const int d = (int)((row / p.H) % p.D);
     const int n = (int)(row / ((long long)p.H * p.D));
