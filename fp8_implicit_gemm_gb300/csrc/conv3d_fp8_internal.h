@@ -47,7 +47,8 @@ struct ConvParams {
   int elem_bytes;        // 1: e4m3 inputs (kind::f8f6f4); 2: bfloat16 inputs (kind::f16)
   int sd, sh, sw, pd, ph, pw;
   int Do, Ho, Wo;
-  int route;             // kRouteGather or kRouteIm2col (how A reaches shared memory)
+  int route;             // kRouteGather, kRouteIm2col, kRouteGrid or kRouteDirect (how A, and on
+                         // the direct route B, reach shared memory)
   int a_cb;              // im2col route: channels per A sub-tile (32, 64 or 128 = its row bytes)
   int pk_pd, pk_ph, pk_pw;  // zero halo of the packed channels-last x (gather route only)
   int Dp, Hp, Wp;        // extents of the packed channels-last copy of x (halo included)

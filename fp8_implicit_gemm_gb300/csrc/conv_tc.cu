@@ -17,10 +17,10 @@
 //              the TMEM allocation.
 //   warps 4-7  gather route (C % 32 != 0 or paddings beyond the im2col corner range): A by
 //              16-byte cp.async gathers from the zero-padded channels-last input into the
-//              128-byte-swizzled stage; rows at or past npq are zero-filled.
-//   (direct route: A and B are both plain TMA tiles, of the explicit im2col of x that the
-//              pre-pass wrote and of the caller's KCTRS weights, in the same K order: warps 4-7
-//              stay idle)
+//              128-byte-swizzled stage; rows at or past npq are zero-filled. On the im2col and
+//              direct routes A arrives by TMA with B and these warps stay idle (on the direct
+//              route A and B are the explicit im2col of x and the caller's KCTRS weights, in the
+//              same K order).
 //   warp 9     MMA issuer: 4 x tcgen05.mma (M=128, N=block_n, K=32 bytes) per 128-byte K block;
 //              kind::f8f6f4 on e4m3 bytes, or kind::f16 on bfloat16 pairs (kBf16): the tiles,
 //              stages and descriptors are the same in bytes
