@@ -175,7 +175,8 @@ __device__ __forceinline__ void epilogue_tile_tma(const ConvParams& p, const Uni
     tmem_ld_32x32b_x32(trow + cc, r);
     tmem_ld_wait();
     uint16_t* buf = stage + (chunk & 1u) * (32 * kBlockM);
-    if (chunk >= 2) {  // the box stored from this buffer two chunks ago must have been read
+    if (chunk >= 2) {  // the box stored from this buffer two chunks ago must have been read:
+      // every chunk commits one group, so all but the newest having read covers it
       if (threadIdx.x == 0) bulk_wait_group_read<1>();
       named_barrier_sync(1, 128);
     }
@@ -188,9 +189,9 @@ __device__ __forceinline__ void epilogue_tile_tma(const ConvParams& p, const Uni
     }
     fence_proxy_async_smem();  // the staged values, visible to the TMA unit
     named_barrier_sync(1, 128);
-    if (threadIdx.x == 0 && any) {
-      tma_store_3d(ymap, smem_u32(buf), pix0, col0 + cc, n0);
-      bulk_commit_group();
+    if (threadIdx.x == 0) {
+      if (any) tma_store_3d(ymap, smem_u32(buf), pix0, col0 + cc, n0);
+      bulk_commit_group();  // a group per chunk, empty for a tile whose rows are all padding
     }
     ++chunk;
   }
