@@ -156,6 +156,17 @@ def test_describe_tail_split(lib):
     # a last wave more than half full is left alone (one CTA per tile: 1913 = 12 * 152 + 89)
     i = _describe(synth.CONFIGS[4], cta_pair=1)
     assert i["full_tiles"] == i["m_tiles"] == 1913 and i["splits"] == 1
+    # few tiles: every tile split, down to three K blocks a split when the K loop is short (the
+    # p1 layer: 21 blocks in 7 splits), four otherwise (the deep layer: 108 blocks in 27; its
+    # bfloat16 twin: 216 in 54)
+    p1 = _describe(synth.CONFIGS[0])
+    assert (p1["splits"], p1["k_blocks_per_split"], p1["full_tiles"]) == (7, 3, 0)
+    deep = _describe(synth.CONFIGS[3])
+    assert (deep["splits"], deep["k_blocks_per_split"]) == (27, 4)
+    s3 = synth.CONFIGS[3]
+    deep2 = capi.conv3d_bf16_describe(s3.N, s3.C, s3.D, s3.H, s3.W, s3.K, s3.T, s3.R, s3.S,
+                                      s3.stride, s3.pad, 152)
+    assert (deep2["splits"], deep2["k_blocks_per_split"]) == (54, 4)
     # a split count in the options applies to every tile
     assert _describe(synth.CONFIGS[4], splits=1)["full_tiles"] == 990
     i = _describe(synth.CONFIGS[4], splits=3)
