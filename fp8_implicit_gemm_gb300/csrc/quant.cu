@@ -31,8 +31,10 @@ __global__ void __launch_bounds__(kQuantThreads) amax_kernel(const void* src, in
   const uint8_t* base = static_cast<const uint8_t*>(src);
   float m = 0.0f;
   const long long stride = (long long)gridDim.x * blockDim.x;
+  // The sweep runs from the end of the source to its start: the pass that follows (the cast, or
+  // the quantising pack) reads from the start, which is then the part still in L2.
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < nblk; i += stride) {
-    const uint8_t* p = base + i * 16 * kQuantVecs;
+    const uint8_t* p = base + (nblk - 1 - i) * 16 * kQuantVecs;
     if (type == kSrcF32) {
       float v[kQuantVecs][4];
 #pragma unroll
