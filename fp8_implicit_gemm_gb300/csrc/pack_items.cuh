@@ -14,7 +14,8 @@ namespace c3d {
 //                         aligned 4-byte loads, a byte transpose in registers, four 16-byte
 //                         stores; 16 pixels with 16-byte loads when W % 16 == 0), else 16
 //                         channels x 1 pixel; a bfloat16 x (the BF16 twin) in items of 8
-//                         channels x 2 pixels (x 1 when W is odd); a channels-last x copied in
+//                         channels x 8 pixels (W % 8 == 0; 16-byte loads), else 8 channels x 2
+//                         pixels (x 1 when W is odd); a channels-last x copied in
 //                         16-byte chunks into the padded copy (no items when the TMA routes read
 //                         that x directly). An fp32 / bfloat16 x quantised to e4m3 on the way is
 //                         always transposed by the tiled kernel; its item loop starts at x_items.
@@ -35,9 +36,11 @@ struct PackPlan {
   int w_group;
   bool hex;   // e4m3 bytes and W % 16 == 0: 16-pixel items (16-byte loads)
   bool quad;  // e4m3 and W % 4 == 0: 4-pixel items
+  bool oct;   // bfloat16 and W % 8 == 0: 8-pixel items (16-byte loads)
   bool two;   // bfloat16 and W % 2 == 0: 2-pixel items
   bool copy;  // x is channels-last already: 16-byte chunk copies
-  bool cfast; // hex items with the channel chunk fastest across threads (>= 16 chunks a pixel):
+  bool cfast; // hex or oct items with the channel chunk fastest across threads (>= 16 chunks a
+              // pixel):
               // a warp's stores of one instruction cover whole pixel rows (C = 256: large layer
               // step 262.4 -> 260.9 us); below 16 chunks the pixel-group-fastest order measured
               // faster (vae layer, C = 128: 32.3 against 33.6 us)
@@ -50,8 +53,9 @@ __host__ __device__ inline PackPlan pack_plan(const ConvParams& p) {
   q.quad = !q.copy && p.elem_bytes == 1 && (p.W % 4) == 0;
   q.hex = q.quad && (p.W % 16) == 0;
   q.two = !q.copy && p.elem_bytes == 2 && (p.W % 2) == 0;
-  q.cfast = q.hex && cq >= 16;
-  const int per_row = q.hex ? p.W / 16 : q.quad ? p.W / 4 : (q.two ? p.W / 2 : p.W);
+  q.oct = q.two && (p.W % 8) == 0;
+  q.cfast = (q.hex || q.oct) && cq >= 16;
+  const int per_row = q.hex ? p.W / 16 : q.quad ? p.W / 4 : q.oct ? p.W / 8 : (q.two ? p.W / 2 : p.W);
   q.x_items = p.xp == nullptr ? 0 : (long long)p.N * p.D * p.H * cq * per_row;
   const long long halo_rows_per_image = (long long)p.Dp * p.Hp - (long long)p.D * p.H;
   q.halo_row_items = (long long)p.N * halo_rows_per_image * p.Wp * cq;
@@ -120,13 +124,23 @@ __device__ __forceinline__ void pack_item(const ConvParams& p, const PackPlan& q
         p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) * p.Wp + w + p.pk_pw) *
                    p.C + cq * 16) = v;
   } else if (g < e1 && p.elem_bytes == 2) {
-    // interior, bfloat16: one item = 8 channels (one 16-byte chunk) x 2 pixels (or 1 when W is
-    // odd); pixels fastest, then chunk, then (n, d, h) row
-    const int per_row = q.two ? p.W / 2 : p.W;
-    const int wi = (int)(g % per_row);
-    const long long rest = g / per_row;
-    const int cq = (int)(rest % cq_n);
-    const long long row = rest / cq_n;  // n*D*H + d*H + h
+    // interior, bfloat16: one item = 8 channels (one 16-byte chunk) x 8 pixels (W % 8 == 0), 2
+    // pixels (W even) or 1; pixel group fastest, then chunk, then (n, d, h) row, or with the
+    // chunk fastest (q.cfast)
+    const int per_row = q.oct ? p.W / 8 : q.two ? p.W / 2 : p.W;
+    int wi, cq;
+    long long row;  // n*D*H + d*H + h
+    if (q.cfast) {
+      cq = (int)(g % cq_n);
+      const long long rest = g / cq_n;
+      wi = (int)(rest % per_row);
+      row = rest / per_row;
+    } else {
+      wi = (int)(g % per_row);
+      const long long rest = g / per_row;
+      cq = (int)(rest % cq_n);
+      row = rest / cq_n;
+    }
     const int h = (int)(row % p.H);
     const int d = (int)((row / p.H) % p.D);
     const int n = (int)(row / ((long long)p.H * p.D));
@@ -135,7 +149,31 @@ __device__ __forceinline__ void pack_item(const ConvParams& p, const PackPlan& q
                           ((long long)n * c_el + cq * 8) * plane + ((long long)d * p.H + h) * p.W;
     uint8_t* dst_row = p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) *
                                    p.Wp + p.pk_pw) * p.C + cq * 16;
-    if (q.two) {
+    if (q.oct) {
+      // a[c]: pixels 8wi..8wi+7 of channel c, two to a word (the even pixel in the low half);
+      // pixel 2k+j's channel pair (2m, 2m+1) is half j of word k of a[2m] and of a[2m+1]
+      uint4 a[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) a[c] = __ldg(reinterpret_cast<const uint4*>(src + c * plane) + wi);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t lo[4], hi[4];  // channel pairs of pixel 8wi + 2k and of pixel 8wi + 2k + 1
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t e = k == 0 ? a[2 * m].x : k == 1 ? a[2 * m].y : k == 2 ? a[2 * m].z : a[2 * m].w;
+          const uint32_t o = k == 0   ? a[2 * m + 1].x
+                             : k == 1 ? a[2 * m + 1].y
+                             : k == 2 ? a[2 * m + 1].z
+                                      : a[2 * m + 1].w;
+          lo[m] = __byte_perm(e, o, 0x5410);
+          hi[m] = __byte_perm(e, o, 0x7632);
+        }
+        *reinterpret_cast<uint4*>(dst_row + (long long)(8 * wi + 2 * k) * p.C) =
+            make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        *reinterpret_cast<uint4*>(dst_row + (long long)(8 * wi + 2 * k + 1) * p.C) =
+            make_uint4(hi[0], hi[1], hi[2], hi[3]);
+      }
+    } else if (q.two) {
       uint32_t v[8];  // v[c]: pixels 2wi (low half) and 2wi+1 (high half) of channel c
 #pragma unroll
       for (int j = 0; j < 8; ++j)

@@ -92,6 +92,12 @@ ODD = [
     synth.ConvShape(1, 16, 1, 1, 1, 16, pad=1),
     synth.ConvShape(2, 128, 3, 17, 19, 256),
     synth.ConvShape(1, 136, 2, 5, 6, 40),
+    # 8-pixel pack items (W % 8 == 0): pixel group fastest below 16 chunks a pixel, chunk fastest
+    # from there on
+    synth.ConvShape(2, 32, 4, 6, 8, 64),
+    synth.ConvShape(1, 64, 3, 5, 16, 48),
+    synth.ConvShape(1, 128, 2, 4, 24, 64),
+    synth.ConvShape(2, 256, 2, 3, 8, 32, stride=2),
 ]
 
 
