@@ -685,7 +685,7 @@ def run_ours(args):
                    "gflop_per_step": round(fig["flop"] / 1e9, 3),
                    "input_layout": "NDHWC" if channels_last else "NCDHW", "output_layout": "NCDHW",
                    "x_source": (f"{quant} values, quantised to e4m3 on the device every step"
-                                if quant else "e4m3 bytes"),
+                                if quant else ("bfloat16 values" if bf16 else "e4m3 bytes")),
                    "plan": {k: info[k] for k in ("route", "cta_pair", "block_m", "block_n",
                                                  "m_tiles", "n_tiles", "full_tiles", "splits",
                                                  "stages", "grid", "row_chk")},
