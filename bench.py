@@ -679,19 +679,10 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16" if bf16 else "e4m3",
         "data": DATA_BF16 if bf16 else DATA,
-        "config": {"workload": workload, "N": shape.N, "C": shape.C, "D": shape.D, "H": shape.H,
-                   "W": shape.W, "K": shape.K, "filter": [shape.T, shape.R, shape.S],
-                   "stride": list(shape.stride), "pad": list(shape.pad), "npq": fig["npq"],
-                   "gflop_per_step": round(fig["flop"] / 1e9, 3),
-                   "input_layout": "NDHWC" if channels_last else "NCDHW", "output_layout": "NCDHW",
-                   "x_source": (f"{quant} values, quantised to e4m3 on the device every step"
-                                if quant else ("bfloat16 values" if bf16 else "e4m3 bytes")),
-                   "plan": {k: info[k] for k in ("route", "cta_pair", "block_m", "block_n",
-                                                 "m_tiles", "n_tiles", "full_tiles", "splits",
-                                                 "stages", "grid", "row_chk")},
-                   "l2": f"flushed between steps ({flush.numel() >> 20} MiB write outside the "
-                         "per-step events)",
-                   "parallelism": f"replicas x{dist.world}"},
+        "config": bench_config(shape, fig, args, dist.world),
+        "plan": {k: info[k] for k in ("route", "cta_pair", "block_m", "block_n", "m_tiles",
+                                      "n_tiles", "full_tiles", "splits", "stages", "grid",
+                                      "row_chk")},
         "roofline": roof,
         "pack": pack,
         "per_config": per_config,
@@ -714,6 +705,25 @@ def run_ours(args):
 
 
 # ------------------------------------------------------------------------------------ reference
+def bench_config(shape, fig, args, world: int) -> dict:
+    """The workload of a bench line, the same for both arms: the layer, its input form, the L2
+    treatment between the GPU arm's steps and the replica count."""
+    bf16 = args.dtype == "bf16"
+    quant = args.quantize_x
+    return {"workload": shape.name + (" [bf16 inputs]" if bf16 else ""), "N": shape.N,
+            "C": shape.C, "D": shape.D, "H": shape.H, "W": shape.W, "K": shape.K,
+            "filter": [shape.T, shape.R, shape.S], "stride": list(shape.stride),
+            "pad": list(shape.pad), "npq": fig["npq"],
+            "gflop_per_step": round(fig["flop"] / 1e9, 3),
+            "input_layout": "NDHWC" if args.input_layout == "ndhwc" else "NCDHW",
+            "output_layout": "NCDHW",
+            "x_source": (f"{quant} values, quantised to e4m3 on the device every step"
+                         if quant else ("bfloat16 values" if bf16 else "e4m3 bytes")),
+            "l2": "flushed between steps (a write of at least twice the L2 size, outside the "
+                  "per-step events)",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -763,11 +773,8 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": DATA_BF16 if bf16 else DATA,
-        "config": {"workload": shape.name + (" [bf16 inputs]" if bf16 else ""), "N": shape.N, "C": shape.C, "D": shape.D,
-                   "H": shape.H, "W": shape.W, "K": shape.K,
-                   "filter": [shape.T, shape.R, shape.S], "stride": list(shape.stride),
-                   "pad": list(shape.pad), "npq": fig["npq"],
-                   "parallelism": "rank 0 only (CPU oracle)"},
+        "config": bench_config(shape, fig, args, world),
+        "oracle_run": "rank 0 only, the CPU oracle on the host cores",
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,

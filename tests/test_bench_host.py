@@ -54,3 +54,26 @@ def test_pack_bytes_per_route():
     # direct route: x read, the explicit im2col (npq x K_gemm elements) written, weights untouched
     assert bench.pack_alg_bytes(deep, True, 4) == deep["x_bytes"] + 128 * 13824
     assert bench.pack_alg_bytes(deep, True, 4, 2) == deep["x_bytes"] + 2 * 128 * 13824
+
+
+def test_both_arms_print_the_same_config():
+    # the reference arm (the CPU oracle) runs on the GPU arm's workload: one config builder serves
+    # both, and nothing in it depends on the run (plan, buffer sizes and timings live elsewhere)
+    import argparse
+    import json
+    import subprocess
+
+    args = argparse.Namespace(dtype="e4m3", quantize_x=None, input_layout="ncdhw")
+    shape = synth.CONFIGS[0]
+    cfg = bench.bench_config(shape, bench.problem_figures(shape), args, 1)
+    assert cfg["workload"] == shape.name and cfg["npq"] == 288 and "plan" not in cfg
+    assert cfg["parallelism"] == "replicas x1" and cfg["l2"].startswith("flushed between steps")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                          "--config", "0", "--steps", "2", "--warmup", "1", "--ref-seconds", "1"],
+                         capture_output=True, text=True, timeout=600, cwd=root,
+                         env={**os.environ, "WORLD_SIZE": "1", "RANK": "0", "LOCAL_RANK": "0"})
+    assert out.returncode == 0, out.stderr[-2000:]
+    line = json.loads(out.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["config"] == cfg
+    assert line["metric"] == bench.METRIC and line["unit"] == "TFLOP/s"
