@@ -80,6 +80,37 @@ def test_quantize_matches_oracle(n, kind, dtype):
     assert np.array_equal(q, ref_q)
 
 
+def test_quantize_signed_zeros_and_tiny_values():
+    # a zero or a quotient that rounds to zero keeps its sign: -0 and tiny negatives give 0x80
+    tiny = np.float32(2.0 ** -126)
+    v = np.array([3.7, -0.0, 0.0, -tiny, tiny, -1e-30, 1e-30, -2.0 ** -140, 2.0 ** -140,
+                  -1e-12, 1e-12], dtype=np.float32)
+    q, s = _gpu_quantize(torch.from_numpy(v).cuda())
+    ref_q, ref_s = Q.quantize(v)
+    assert s == ref_s and ref_q[1] == 0x80
+    assert np.array_equal(q, ref_q), [hex(a) for a in q]
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_quantize_dense_runs_of_consecutive_values(seed):
+    # runs of consecutive fp32 values at several magnitudes under a random scale: every quotient
+    # (not only those near a code boundary) must give the IEEE quotient's code
+    rng = np.random.default_rng(700 + seed)
+    amax = np.float32(rng.uniform(1.0, 2.0) * 2.0 ** rng.integers(-20, 11))
+    runs = [np.array([amax], dtype=np.float32)]
+    for frac in (1.0, 0.5, 2.0 ** -5, 2.0 ** -12, 2.0 ** -17):
+        start = np.float32(amax * frac * rng.uniform(0.5, 1.0))
+        run = np.nextafter.accumulate(np.concatenate([[start], np.full(4095, np.inf, np.float32)]
+                                                     ).astype(np.float32))
+        runs += [run, -run]
+    v = np.concatenate(runs).astype(np.float32)
+    v = v[np.abs(v) <= amax]
+    q, s = _gpu_quantize(torch.from_numpy(v).cuda())
+    ref_q, ref_s = Q.quantize(v)
+    assert s == ref_s
+    assert np.array_equal(q, ref_q), int(np.sum(q != ref_q))
+
+
 def test_quantize_ties_round_to_even():
     # amax = 448 gives scale 1, so every value is its own quotient: all e4m3 midpoints
     grid = oracle.e4m3_decode(np.arange(0x7F, dtype=np.uint8))
