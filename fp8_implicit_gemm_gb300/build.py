@@ -43,19 +43,30 @@ def _inputs() -> list[str]:
     return files
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+# The write-counting test build (C3D_COUNT_WRITES): the same sources, every store to y also counted
+COUNT_LIB_PATH = os.path.join(BUILD_DIR, "libconv3d_fp8_count.so")
+
+
+def up_to_date(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return all(os.path.getmtime(f) <= t for f in _inputs())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
+def build_counting(force: bool = False) -> str:
+    """The write-counting build, for tests; returns its path."""
+    return build(force=force, extra_flags=["-DC3D_COUNT_WRITES"], out=COUNT_LIB_PATH)
+
+
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          out: str = LIB_PATH) -> str:
     """Compile and link; returns the path of the shared library."""
-    if not force and up_to_date():
-        return LIB_PATH
+    if not force and up_to_date(out):
+        return out
     nvcc = _nvcc()
-    obj_dir = os.path.join(BUILD_DIR, "obj")
+    obj_dir = os.path.join(BUILD_DIR, "obj" if out == LIB_PATH else "obj_" +
+                           os.path.splitext(os.path.basename(out))[0])
     os.makedirs(obj_dir, exist_ok=True)
     flags = CFLAGS + (extra_flags or [])
 
@@ -71,13 +82,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
 
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

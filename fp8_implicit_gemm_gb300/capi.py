@@ -79,6 +79,8 @@ def load() -> ctypes.CDLL:
             lib.conv3d_fp8_set_timing_events.argtypes = [vp, vp, vp]
             lib.conv3d_fp8_set_pack_timing_event.restype = ci
             lib.conv3d_fp8_set_pack_timing_event.argtypes = [vp, vp]
+            lib.conv3d_fp8_set_write_counter.restype = ci
+            lib.conv3d_fp8_set_write_counter.argtypes = [vp, vp]
             lib.conv3d_fp8_run_noalloc.restype = ci
             lib.conv3d_fp8_run_noalloc.argtypes = [ci] * 9 + [i3, i3, vp, vp, vp, vp, vp, vp]
             lib.conv3d_fp8_check.restype = ci
@@ -223,6 +225,13 @@ def conv3d_fp8_set_timing_events(plan, ev_begin, ev_end) -> None:
     the main kernel of every later run of the plan."""
     _raise(load().conv3d_fp8_set_timing_events(plan, _raw_event(ev_begin), _raw_event(ev_end)),
            "conv3d_fp8_set_timing_events")
+
+
+def conv3d_fp8_set_write_counter_status(plan, counts) -> int:
+    """Count the stores to each output element into `counts` (a zeroed uint32/int32 device
+    tensor of N*K*Do*Ho*Wo elements; None stops); only a library built with C3D_COUNT_WRITES
+    counts, the product build returns CONV3D_EUNSUPPORTED."""
+    return load().conv3d_fp8_set_write_counter(plan, _ptr(counts) if counts is not None else None)
 
 
 def conv3d_fp8_set_pack_timing_event(plan, ev_pack) -> None:

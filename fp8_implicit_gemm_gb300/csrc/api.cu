@@ -762,6 +762,18 @@ conv3d_status conv3d_fp8_set_pack_timing_event(conv3d_fp8_plan_t plan, void* ev_
   return CONV3D_OK;
 }
 
+conv3d_status conv3d_fp8_set_write_counter(conv3d_fp8_plan_t plan, void* counts) {
+  if (!plan) return CONV3D_EINVAL;
+#ifdef C3D_COUNT_WRITES
+  if (counts && reinterpret_cast<uintptr_t>(counts) % 4 != 0) return CONV3D_EINVAL;
+  plan->p.write_count = static_cast<uint32_t*>(counts);
+  return CONV3D_OK;
+#else
+  (void)counts;
+  return CONV3D_EUNSUPPORTED;
+#endif
+}
+
 conv3d_status conv3d_fp8_check(conv3d_fp8_plan_t plan) {
   if (!plan) return CONV3D_EINVAL;
   DeviceGuard guard;

@@ -88,6 +88,8 @@ struct ConvParams {
   const float* scale_w;
   float* partials;       // fp32 [tile - full_tiles][split][block_n][block_m] (workspace)
   int* status;           // status word (workspace)
+  uint32_t* write_count; // a library built with C3D_COUNT_WRITES (tests): one counter per output
+                         // element, incremented by every store to it; null otherwise
   unsigned long long timeout_ns;
   int debug_flags;
 };

@@ -101,6 +101,18 @@ __device__ __forceinline__ RowDest row_dest(const ConvParams& p, int m_tile, int
   return r;
 }
 
+// Write counting, in a library built with C3D_COUNT_WRITES (a test build: every store of output
+// element i also adds one to write_count[i], so a test can check that each element is written
+// exactly once); the product build compiles it to nothing.
+__device__ __forceinline__ void count_write(const ConvParams& p, long long i) {
+#ifdef C3D_COUNT_WRITES
+  if (p.write_count) atomicAdd(p.write_count + i, 1u);
+#else
+  (void)p;
+  (void)i;
+#endif
+}
+
 // Epilogue of one thread: columns [cc0, cc1) (multiples of 32) of its accumulator row (TMEM lane)
 // of one unit, `trow` = TMEM address of the row's first column in the current buffer.
 // `row_in_tile` is the row within the unit's block_m rows. A whole tile: y = bf16(acc * scale),
@@ -127,6 +139,7 @@ __device__ __forceinline__ void epilogue_row(const ConvParams& p, const Unit& un
           if (col < p.K) {
             const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(r[j]) * scale);
             ybase[(long long)col * p.dhw] = *reinterpret_cast<const uint16_t*>(&b);
+            count_write(p, dst.y_off + (long long)col * p.dhw);
           }
         }
       }
@@ -185,7 +198,10 @@ __device__ __forceinline__ void epilogue_tile_tma(const ConvParams& p, const Uni
       const __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(r[j]) * scale);
       const uint16_t v = *reinterpret_cast<const uint16_t*>(&b);
       buf[j * kBlockM + row] = v;
-      if (spill && col0 + cc + j < p.K) p.y[y_off + (long long)(col0 + cc + j) * p.dhw] = v;
+      if (spill && col0 + cc + j < p.K) {
+        p.y[y_off + (long long)(col0 + cc + j) * p.dhw] = v;
+        count_write(p, y_off + (long long)(col0 + cc + j) * p.dhw);
+      }
     }
     fence_proxy_async_smem();  // the staged values, visible to the TMA unit
     named_barrier_sync(1, 128);
@@ -193,6 +209,12 @@ __device__ __forceinline__ void epilogue_tile_tma(const ConvParams& p, const Uni
       if (any) tma_store_3d(ymap, smem_u32(buf), pix0, col0 + cc, n0);
       bulk_commit_group();  // a group per chunk, empty for a tile whose rows are all padding
     }
+#ifdef C3D_COUNT_WRITES
+    // the box's elements the TMA unit writes: rows of image n0 (pix < dhw), columns < K
+    if (any && pix0 + row < p.dhw)
+      for (int j = 0; j < 32 && col0 + cc + j < p.K; ++j)
+        count_write(p, ((long long)n0 * p.K + col0 + cc + j) * p.dhw + pix0 + row);
+#endif
     ++chunk;
   }
 }

@@ -349,6 +349,7 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(ConvParams p) {
     for (; s < p.splits; ++s) acc += __ldcg(src + (long long)s * per_tile);
     const __nv_bfloat16 b = __float2bfloat16_rn(acc * scale);
     p.y[dst.y_off + (long long)col * p.dhw] = *reinterpret_cast<const uint16_t*>(&b);
+    count_write(p, dst.y_off + (long long)col * p.dhw);
   }
 }
 

@@ -179,6 +179,17 @@ conv3d_status conv3d_fp8_set_timing_events(conv3d_fp8_plan_t plan, void *ev_begi
 conv3d_status conv3d_fp8_set_pack_timing_event(conv3d_fp8_plan_t plan, void *ev_pack);
 
 /*
+ * Write-count hook for tests (defined by: the page's "Verification" -- every output element
+ * written exactly once -- checked directly rather than through a NaN pre-fill). Only a library
+ * built with C3D_COUNT_WRITES counts: there every store of output element i by a later run of
+ * this plan (main kernel, TMA-store box, split-K reduction) also adds one to counts[i], a device
+ * array of N*K*Do*Ho*Wo uint32 (NCDHW order, 4-byte aligned, caller-owned, zeroed by the caller);
+ * NULL stops. The product build returns EUNSUPPORTED and never counts.
+ * Errors: EINVAL (NULL plan, misaligned counts), EUNSUPPORTED (product build).
+ */
+conv3d_status conv3d_fp8_set_write_counter(conv3d_fp8_plan_t plan, void *counts);
+
+/*
  * Allocation-free run (no counterpart on the subject page; it exists for callers of this library).
  * Some callers cannot call cudaMalloc: a host framework whose caching allocator owns the device's
  * memory pool, a plugin interface that passes tensors in but offers no way to ask for memory, or a
