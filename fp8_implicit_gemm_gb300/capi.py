@@ -83,6 +83,8 @@ def load() -> ctypes.CDLL:
             lib.conv3d_fp8_set_write_counter.argtypes = [vp, vp]
             lib.conv3d_fp8_run_noalloc.restype = ci
             lib.conv3d_fp8_run_noalloc.argtypes = [ci] * 9 + [i3, i3, vp, vp, vp, vp, vp, vp]
+            lib.conv3d_fp8_noalloc_check.restype = ci
+            lib.conv3d_fp8_noalloc_check.argtypes = []
             lib.conv3d_fp8_check.restype = ci
             lib.conv3d_fp8_check.argtypes = [vp]
             lib.conv3d_fp8_get_info.restype = ci
@@ -202,6 +204,12 @@ def conv3d_fp8_run_noalloc_status(N, C, D, H, W, K, T, R, S, stride, pad, x, w, 
     return load().conv3d_fp8_run_noalloc(N, C, D, H, W, K, T, R, S, _int3(stride), _int3(pad),
                                          _ptr(x), _ptr(w), _ptr(scale_x), _ptr(scale_w), _ptr(y),
                                          _stream(stream))
+
+
+def conv3d_fp8_noalloc_check() -> int:
+    """Synchronise the current device, then report (and clear) the status word of its latest
+    allocation-free call: CONV3D_OK or CONV3D_EDEVICE."""
+    return int(load().conv3d_fp8_noalloc_check())
 
 
 def conv3d_fp8_run_noalloc(N, C, D, H, W, K, T, R, S, stride, pad, x, w, scale_x, scale_w, y,

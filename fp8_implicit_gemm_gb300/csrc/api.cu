@@ -860,6 +860,7 @@ namespace {
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void* g_noalloc_base[kNoAllocMaxDevices] = {};
+int* g_noalloc_status[kNoAllocMaxDevices] = {};  // status word of the latest call on each device
 
 // Once per device, with that device current: take the device address of the scratch array (the
 // host-side symbol is only a stand-in and must never reach a kernel) and grant the main kernel the
@@ -962,6 +963,10 @@ extern "C" conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int 
   if (st != CONV3D_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(p.status, 0, sizeof(int), s) != cudaSuccess) return CONV3D_ECUDA;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    g_noalloc_status[dev] = p.status;
+  }
   if (launch_pack(p, s) != cudaSuccess) return CONV3D_ECUDA;
   const CUtensorMap ymap{};  // explicit guarded stores here (no TMA-store epilogue)
   if (launch_conv(p, wmap, xmap, ymap, info.row_chk != 0, info.grid, s) != cudaSuccess)
@@ -969,4 +974,26 @@ extern "C" conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int 
   if (has_split_tiles(p) && launch_splitk_reduce(p, info.row_chk != 0, s) != cudaSuccess)
     return CONV3D_ECUDA;
   return CONV3D_OK;
+}
+
+extern "C" conv3d_status conv3d_fp8_noalloc_check(void) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return CONV3D_ECUDA;
+  }
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return CONV3D_EUNSUPPORTED;
+  int* status = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    status = g_noalloc_status[dev];
+  }
+  if (!status) return CONV3D_OK;  // no allocation-free call on this device yet
+  if (cudaDeviceSynchronize() != cudaSuccess) return CONV3D_ECUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return CONV3D_ECUDA;
+  if (word == 0) return CONV3D_OK;
+  if (cudaMemset(status, 0, sizeof(int)) != cudaSuccess) return CONV3D_ECUDA;
+  return CONV3D_EDEVICE;
 }

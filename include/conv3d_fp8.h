@@ -206,8 +206,8 @@ conv3d_status conv3d_fp8_set_write_counter(conv3d_fp8_plan_t plan, void *counts)
  *   Each call rewrites everything of the array it reads: the packed operands (the zero halo of
  *   the padded copy included) and the status word; partials are written before they are read.
  *   All calls share the one array and it keeps the last call's contents: calls whose work overlaps
- *   on the GPU race on it, so serialise them. Kernel-side bounded-wait errors are not reported
- *   here (use a plan and conv3d_fp8_check when you need them).
+ *   on the GPU race on it, so serialise them. Kernel-side bounded-wait errors are not returned
+ *   here: conv3d_fp8_noalloc_check reads them after the call.
  * Errors: EINVAL, EUNSUPPORTED (as for planning, and when the problem needs more scratch than the
  * array holds: packed x and w plus split-K partials), ECUDA.
  */
@@ -218,6 +218,16 @@ conv3d_status conv3d_fp8_run_noalloc(int N, int C, int D, int H, int W, int K, i
                                      const void *x_ncdhw, const void *w_kctrs,
                                      const float *scale_x, const float *scale_w, void *y_ncdhw,
                                      void *stream);
+
+/*
+ * Status of the latest conv3d_fp8_run_noalloc call on the current device (defined by: none,
+ * library plumbing: the status word of the kernels' bounded waits, in the shared scratch).
+ * Synchronises the device, then reports and clears that call's status word: OK, or EDEVICE when a
+ * bounded wait of its kernels ran out. OK when no such call has been made on the device. A later
+ * allocation-free call clears the word itself, so check before the next one.
+ * Errors: EUNSUPPORTED (device ordinal beyond the entry point's table), ECUDA.
+ */
+conv3d_status conv3d_fp8_noalloc_check(void);
 
 /* Synchronise the plan's device, then report (and clear) its status word: OK or EDEVICE.
  * Defined by: none (library plumbing: the status word of the kernels' bounded waits). */

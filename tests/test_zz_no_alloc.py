@@ -62,7 +62,10 @@ def test_noalloc_matches_planned_run_and_oracle_on_calls_in_a_row():
             cases.append((shape, inp, g))
             assert g.info["route"] == route, (shape.name, g.info["route"])
         planned = [_planned(g) for _, _, g in cases]
-        got = [_noalloc(g) for _, _, g in cases]
+        got = []
+        for _, _, g in cases:
+            got.append(_noalloc(g))
+            assert capi.conv3d_fp8_noalloc_check() == capi.CONV3D_OK
         for (shape, inp, g), ref, out in zip(cases, planned, got):
             assert np.array_equal(out, ref), (
                 f"{shape.name}: {int(np.sum(out != ref))} outputs differ from the planned run")
