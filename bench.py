@@ -578,6 +578,35 @@ def run_ours(args):
            "d2h_bytes_per_step": int(2 * y.numel()),
            "pipelining": "H2D / compute / D2H of consecutive steps on three streams, two buffer "
                          "sets"}
+    # The host link's floor under the pipelined step: the same bytes moved in both directions at
+    # once (the step's H2D copies on one stream, its D2H copy on the other) with nothing else
+    # running, timed after the e2e loop. The pipelined e2e step cannot beat it.
+    link_reps = 5
+    for i in range(link_reps + 2):
+        if i == 2:
+            torch.cuda.synchronize()
+            l_start, l_stop = ev(), ev()
+            l_start.record(stream)
+        h2d_stream.wait_stream(stream)
+        d2h_stream.wait_stream(stream)
+        with torch.cuda.stream(h2d_stream):
+            xs[0].copy_(x_h, non_blocking=True)
+            ws[0].copy_(w_h, non_blocking=True)
+            ss[0].copy_(s_h, non_blocking=True)
+        with torch.cuda.stream(d2h_stream):
+            yhs[0].copy_(ys[0], non_blocking=True)
+        stream.wait_stream(h2d_stream)
+        stream.wait_stream(d2h_stream)
+    l_stop.record(stream)
+    torch.cuda.synchronize()
+    link_ms = dist.max(l_start.elapsed_time(l_stop) / link_reps, dev)
+    e2e["link_floor"] = {
+        "ms_per_step": round(link_ms, 4),
+        "gbs": round((e2e["h2d_bytes_per_step"] + e2e["d2h_bytes_per_step"]) /
+                     (link_ms * 1e-3) / 1e9, 1),
+        "frac": round(link_ms / e2e_ms, 4),
+        "note": "the step's H2D and D2H bytes copied at once, alone, on the same streams; frac = "
+                "this floor / the e2e step"}
 
     # ---- roofline of the dominant kernel (the implicit-GEMM kernel)
     peaks, peaks_kind = load_peaks()
@@ -620,8 +649,7 @@ def run_ours(args):
     else:
         p_bytes = 2 * fig["w_bytes"] + x.numel() * x.element_size() + fig["x_bytes"]
     p_ms = statistics.mean(pack_ms)
-    pack = {"kernel": "im2col_kernel" if info["route"] == 4 else
-            ("pack_x_tiled_kernel + pack items" if quant else "pack_kernel"),
+    pack = {"kernel": pack_kernel_name(shape, info["route"], quant, bf16, channels_last),
             "alg_bytes": int(p_bytes), "ms": round(p_ms, 5),
             "achieved": round(p_bytes / (p_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
             "peak": round(hbm_peak, 1), "frac": round(p_bytes / (p_ms * 1e-3) / 1e9 / hbm_peak, 4),
@@ -705,6 +733,19 @@ def run_ours(args):
 
 
 # ------------------------------------------------------------------------------------ reference
+def pack_kernel_name(shape, route: int, quant: bool, bf16: bool, channels_last: bool) -> str:
+    """The kernel the library launches in front of the GEMM for this run (its choice, restated)."""
+    if route == 4:
+        return "im2col_kernel"
+    if quant:
+        return "pack_x_tiled_kernel + pack items"
+    dhw = shape.D * shape.H * shape.W
+    if (not bf16 and not channels_last and shape.W % 4 == 0 and dhw % 16 == 0 and
+            shape.C % 64 == 0):
+        return "pack_x_e4m3_tiled_kernel"
+    return "pack_kernel"
+
+
 def bench_config(shape, fig, args, world: int) -> dict:
     """The workload of a bench line, the same for both arms: the layer, its input form, the L2
     treatment between the GPU arm's steps and the replica count."""

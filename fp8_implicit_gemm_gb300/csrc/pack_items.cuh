@@ -104,10 +104,84 @@ __device__ __forceinline__ PackCtx pack_ctx(const ConvParams& p, const PackPlan&
   return c;
 }
 
+// Item g >= e1 of the pack: a zero chunk of the halo, or a weight chunk (g < e3 + w_items).
+__device__ __forceinline__ void pack_rest_item(const ConvParams& p, const PackPlan& q,
+                                               const PackCtx& c, long long g) {
+  const long long e1 = c.e1, e2 = c.e2, e3 = c.e3;
+  const int cq_n = c.cq_n;
+  (void)q;
+  if (g < e2) {
+    // zero chunks of a halo row: halo planes first, then the halo rows of interior planes
+    const long long gi = g - e1;
+    const long long per_row = (long long)p.Wp * cq_n;
+    const long long r = (gi / per_row);
+    const long long chunk = gi - r * per_row;
+    const long long halo_rows_per_image = (long long)p.Dp * p.Hp - (long long)p.D * p.H;
+    const int n = (int)(r / halo_rows_per_image);
+    long long rr = r - (long long)n * halo_rows_per_image;
+    const long long front = (long long)p.pk_pd * p.Hp;
+    int dp, hp;
+    if (rr < front) {
+      dp = (int)(rr / p.Hp);
+      hp = (int)(rr % p.Hp);
+    } else if (rr < 2 * front) {
+      rr -= front;
+      dp = p.pk_pd + p.D + (int)(rr / p.Hp);
+      hp = (int)(rr % p.Hp);
+    } else {
+      rr -= 2 * front;
+      const int side = 2 * p.pk_ph;
+      const int kk = (int)(rr % side);
+      dp = p.pk_pd + (int)(rr / side);
+      hp = kk < p.pk_ph ? kk : p.H + kk;
+    }
+    *reinterpret_cast<uint4*>(p.xp + (((long long)n * p.Dp + dp) * p.Hp + hp) * p.Wp * p.C +
+                              chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
+  } else if (g < e3) {
+    // zero chunks of the W-halo pixels of interior rows
+    const long long gi = g - e2;
+    const int side = p.Wp - p.W;
+    const long long per_row = (long long)side * cq_n;
+    const long long row = gi / per_row;  // n*D*H + d*H + h
+    const long long rem = gi - row * per_row;
+    const int kk = (int)(rem / cq_n);
+    const int cq = (int)(rem - (long long)kk * cq_n);
+    const int wp = kk < p.pk_pw ? kk : p.W + kk;
+    const int h = (int)(row % p.H);
+    const int d = (int)((row / p.H) % p.D);
+    const int n = (int)(row / ((long long)p.H * p.D));
+    *reinterpret_cast<uint4*>(
+        p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) * p.Wp + wp) * p.C +
+        cq * 16) = make_uint4(0u, 0u, 0u, 0u);
+  } else {
+    // weights: one item = one 16-byte chunk (16 e4m3 or 8 bfloat16 channels) of one tap
+    const long long gw = g - e3;
+    const int tap = (int)(gw % p.taps);
+    const long long rest = gw / p.taps;
+    const int cq = (int)(rest % cq_n);
+    const int k = (int)(rest / cq_n);
+    uint32_t v[4] = {0u, 0u, 0u, 0u};
+    if (p.elem_bytes == 2) {
+      const uint16_t* src = reinterpret_cast<const uint16_t*>(p.w) +
+                            ((long long)k * (p.C >> 1) + cq * 8) * p.taps + tap;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j >> 1] |= (uint32_t)__ldg(src + j * p.taps) << ((j & 1) * 16);
+    } else {
+      const uint8_t* src = p.w + ((long long)k * p.C + cq * 16) * p.taps + tap;
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        v[j >> 2] |= (uint32_t)__ldg(src + j * p.taps) << ((j & 3) * 8);
+    }
+    uint4* dst =
+        reinterpret_cast<uint4*>(p.wp + ((long long)k * p.taps + tap) * p.C + cq * 16);
+    *dst = make_uint4(v[0], v[1], v[2], v[3]);
+  }
+}
+
 // Item g of the pack (g < e3 + w_items).
 __device__ __forceinline__ void pack_item(const ConvParams& p, const PackPlan& q,
                                           const PackCtx& c, long long g) {
-  const long long e1 = c.e1, e2 = c.e2, e3 = c.e3;
+  const long long e1 = c.e1;
   const int cq_n = c.cq_n;
   const long long plane = c.plane;
   if (g < e1 && q.copy) {
@@ -270,71 +344,8 @@ __device__ __forceinline__ void pack_item(const ConvParams& p, const PackPlan& q
         v[j >> 2] |= (uint32_t)__ldg(src + j * plane + wi) << ((j & 3) * 8);
       *reinterpret_cast<uint4*>(dst_row + (long long)wi * p.C) = make_uint4(v[0], v[1], v[2], v[3]);
     }
-  } else if (g < e2) {
-    // zero chunks of a halo row: halo planes first, then the halo rows of interior planes
-    const long long gi = g - e1;
-    const long long per_row = (long long)p.Wp * cq_n;
-    const long long r = (gi / per_row);
-    const long long chunk = gi - r * per_row;
-    const long long halo_rows_per_image = (long long)p.Dp * p.Hp - (long long)p.D * p.H;
-    const int n = (int)(r / halo_rows_per_image);
-    long long rr = r - (long long)n * halo_rows_per_image;
-    const long long front = (long long)p.pk_pd * p.Hp;
-    int dp, hp;
-    if (rr < front) {
-      dp = (int)(rr / p.Hp);
-      hp = (int)(rr % p.Hp);
-    } else if (rr < 2 * front) {
-      rr -= front;
-      dp = p.pk_pd + p.D + (int)(rr / p.Hp);
-      hp = (int)(rr % p.Hp);
-    } else {
-      rr -= 2 * front;
-      const int side = 2 * p.pk_ph;
-      const int kk = (int)(rr % side);
-      dp = p.pk_pd + (int)(rr / side);
-      hp = kk < p.pk_ph ? kk : p.H + kk;
-    }
-    *reinterpret_cast<uint4*>(p.xp + (((long long)n * p.Dp + dp) * p.Hp + hp) * p.Wp * p.C +
-                              chunk * 16) = make_uint4(0u, 0u, 0u, 0u);
-  } else if (g < e3) {
-    // zero chunks of the W-halo pixels of interior rows
-    const long long gi = g - e2;
-    const int side = p.Wp - p.W;
-    const long long per_row = (long long)side * cq_n;
-    const long long row = gi / per_row;  // n*D*H + d*H + h
-    const long long rem = gi - row * per_row;
-    const int kk = (int)(rem / cq_n);
-    const int cq = (int)(rem - (long long)kk * cq_n);
-    const int wp = kk < p.pk_pw ? kk : p.W + kk;
-    const int h = (int)(row % p.H);
-    const int d = (int)((row / p.H) % p.D);
-    const int n = (int)(row / ((long long)p.H * p.D));
-    *reinterpret_cast<uint4*>(
-        p.xp + ((((long long)n * p.Dp + d + p.pk_pd) * p.Hp + h + p.pk_ph) * p.Wp + wp) * p.C +
-        cq * 16) = make_uint4(0u, 0u, 0u, 0u);
   } else {
-    // weights: one item = one 16-byte chunk (16 e4m3 or 8 bfloat16 channels) of one tap
-    const long long gw = g - e3;
-    const int tap = (int)(gw % p.taps);
-    const long long rest = gw / p.taps;
-    const int cq = (int)(rest % cq_n);
-    const int k = (int)(rest / cq_n);
-    uint32_t v[4] = {0u, 0u, 0u, 0u};
-    if (p.elem_bytes == 2) {
-      const uint16_t* src = reinterpret_cast<const uint16_t*>(p.w) +
-                            ((long long)k * (p.C >> 1) + cq * 8) * p.taps + tap;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j >> 1] |= (uint32_t)__ldg(src + j * p.taps) << ((j & 1) * 16);
-    } else {
-      const uint8_t* src = p.w + ((long long)k * p.C + cq * 16) * p.taps + tap;
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        v[j >> 2] |= (uint32_t)__ldg(src + j * p.taps) << ((j & 3) * 8);
-    }
-    uint4* dst =
-        reinterpret_cast<uint4*>(p.wp + ((long long)k * p.taps + tap) * p.C + cq * 16);
-    *dst = make_uint4(v[0], v[1], v[2], v[3]);
+    pack_rest_item(p, q, c, g);
   }
 }
 

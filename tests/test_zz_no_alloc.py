@@ -8,12 +8,15 @@ finding the previous call's packed operands and partials still in the array:
 
   1. a stride-2 layer on the TMA im2col route, whose channels-last copy of x (no halo) fills the
      first megabyte of the array with nonzero bytes;
-  2. the two-image layer on the padded-grid route: its packed copy of x carries a zero halo, and
-     that halo now lies on the bytes call 1 left behind, so the pack must rewrite it;
-  3. a 48-channel layer on the cp.async gather route, whose packed copy also has a halo;
-  4. the deep stride-2 layer on the direct route (the explicit im2col of x in the array, split-K
+  2. a two-image layer on the padded-grid route packed by the tiled transpose (W % 4 == 0, 64
+     channels): its packed copy of x carries a zero halo, and that halo now lies on the bytes
+     call 1 left behind, so the transpose's blocks must rewrite it after their tiles;
+  3. the two-image layer of the workloads (W = 15) on the padded-grid route, packed by items, whose
+     halo lies on call 2's bytes;
+  4. a 48-channel layer on the cp.async gather route, whose packed copy also has a halo;
+  5. the deep stride-2 layer on the direct route (the explicit im2col of x in the array, split-K
      partials after it);
-  5. the padded-row layer of the subject page (TMA im2col route, row guard on).
+  6. the padded-row layer of the subject page (TMA im2col route, row guard on).
 
 Each result must be bit for bit the planned run's (same kernels, same plan) and within the parity
 gates against the oracle. A problem too big for the array is refused before anything runs.
@@ -32,6 +35,7 @@ pytestmark = pytest.mark.gpu
 
 GATHER_48 = synth.ConvShape(2, 48, 4, 6, 5, 80, name="gather_2x48x4x6x5_k80_s1")
 IM2COL_S2 = synth.ConvShape(1, 64, 16, 32, 32, 64, stride=2, name="im2col_1x64x16x32x32_k64_s2")
+GRID_W16 = synth.ConvShape(2, 64, 8, 16, 16, 128, name="grid_2x64x8x16x16_k128_s1")
 
 
 def _noalloc(g: GpuConv) -> np.ndarray:
@@ -51,6 +55,7 @@ def _planned(g: GpuConv) -> np.ndarray:
 
 def test_noalloc_matches_planned_run_and_oracle_on_calls_in_a_row():
     shapes = [(IM2COL_S2, synth.make_inputs(IM2COL_S2, 6464), 2),
+              (GRID_W16, synth.make_inputs(GRID_W16, 1616), 3),
               (synth.CONFIGS[1], synth.make_config_inputs(1), 3),
               (GATHER_48, synth.make_inputs(GATHER_48, 4848), 1),
               (synth.CONFIGS[3], synth.make_config_inputs(3), 4),
