@@ -740,9 +740,9 @@ def pack_kernel_name(shape, route: int, quant: bool, bf16: bool, channels_last: 
     if quant:
         return "pack_x_tiled_kernel + pack items"
     dhw = shape.D * shape.H * shape.W
-    if (not bf16 and not channels_last and shape.W % 4 == 0 and dhw % 16 == 0 and
-            shape.C % 64 == 0):
-        return "pack_x_e4m3_tiled_kernel"
+    eb = 2 if bf16 else 1
+    if not channels_last and shape.W % 4 == 0 and (dhw * eb) % 16 == 0 and shape.C % 64 == 0:
+        return "pack_x_transpose_kernel"
     return "pack_kernel"
 
 

@@ -186,52 +186,60 @@ static cudaError_t launch_tiled_ct(const ConvParams& p, const PackPlan& q, long 
   return cudaGetLastError();
 }
 
-// Tiled transpose of the interior of an NCDHW e4m3 x (W % 4 == 0, D*H*W % 16 == 0) into the
-// channels-last copy, without rounding anything: bytes move as they are. An x tile is kCG channels
-// x kTP consecutive positions of one image's D x H x W volume, 16 KB: kCG runs of kTP bytes, one
-// per channel plane. Every block walks the tiles blockIdx.x, + gridDim.x, ... -- the x tiles, then
-// the weight tiles (pack_w_tile) -- through a ring of kE4Stages shared-memory stages:
+// Tiled transpose of the interior of an NCDHW x into the channels-last copy, for e4m3 bytes
+// (kEB = 1) and for the BF16 twin's bfloat16 elements (kEB = 2), without rounding anything: the
+// elements move as they are. Shapes: W % 4 == 0 and D*H*W*kEB % 16 == 0. An x tile is kCG channels
+// x kTP consecutive positions of one image's D x H x W volume, 16 KB: kCG runs of kTP elements,
+// one per channel plane. Every block walks the tiles blockIdx.x, + gridDim.x, ... -- the x tiles,
+// then the weight tiles (pack_w_tile) -- through a ring of kE4Stages shared-memory stages:
 //   1. the runs of the x tile two steps ahead go into the free stage with 16-byte cp.async copies
 //      (a warp's 32 copies are whole 128-byte lines of the source), in flight while
-//   2. each thread takes one (16-channel block, 4-position group) of the current tile: 16 aligned
-//      4-byte words, one per channel, through four 4x4 byte transposes into four 16-byte chunks,
-//      one per position, stored into the copy. The kCG / 16 threads of a position are adjacent in
-//      the warp, so one store instruction writes whole kCG-byte runs of pixel rows.
-// Row r of a stage keeps its 16-byte chunks rotated by (r / 16) * 512 / kCG bytes, so that the 32
-// words a warp reads in step 2 fall in 32 different banks. Then the blocks share the remaining
-// items (halo chunks, weights by items) in a grid-stride loop. The item path this replaces for
-// these shapes held 16 x 16 bytes a thread in registers (100 registers, two blocks an SM) and ran
-// its one-shot blocks in waves: 31.4 us for the large layer's x, against 18.5 us for each further
-// image of the same size. Weight tiles in blocks of their own could not share an SM with the
-// persistent blocks' stages and ran after them.
+//   2. each thread takes one (16-byte channel block, 4-position group) of the current tile: one
+//      4-position word (e4m3: 4 bytes, bfloat16: 8 bytes) from each of the block's 16 / kEB
+//      channel rows, through byte permutes into four 16-byte chunks, one per position, stored
+//      into the copy. The threads of a position are adjacent in the warp, so one store
+//      instruction writes whole kCG * kEB-byte runs of pixel rows.
+// Row r of a stage keeps its 16-byte chunks rotated by (r * kEB / 16) * 128 / kCB bytes (kCB:
+// channel blocks of a tile), so that the words a warp (bfloat16: a half-warp) reads in step 2 fall
+// in 32 different banks. Then the blocks share the remaining items (halo chunks, weights by
+// items) in a grid-stride loop. The item path this replaces for these shapes held 16 x 16 bytes a
+// thread in registers (100 registers, two blocks an SM) and ran its one-shot blocks in waves:
+// 31.4 us for the large layer's x, against 18.5 us for each further image of the same size.
+// Weight tiles in blocks of their own could not share an SM with the persistent blocks' stages
+// and ran after them.
 constexpr int kE4Stages = 3;
 constexpr int kE4StageBytes = 16384;
 constexpr int kE4BlocksPerSm = 4;  // 3 stages of 16 KB each; <= 64 registers a thread
 
-template <int kCG>
-__global__ void __launch_bounds__(256, kE4BlocksPerSm) pack_x_e4m3_tiled_kernel(
+template <int kEB, int kCG>
+__global__ void __launch_bounds__(256, kE4BlocksPerSm) pack_x_transpose_kernel(
     ConvParams p, PackPlan q, long long x_tiles) {
   pdl_launch_dependents();  // the implicit GEMM may start its prologue while the pack runs
-  constexpr int kTP = kE4StageBytes / kCG;  // positions of a tile = bytes of a stage row
-  constexpr int kCB = kCG / 16;             // 16-channel blocks of a tile
-  constexpr int kRotB = 128 / kCB;          // rotation of a row, in bytes, per 16-row block
+  constexpr int kRowB = kE4StageBytes / kCG;  // bytes of a stage row
+  constexpr int kTP = kRowB / kEB;            // positions of a tile
+  constexpr int kChB = 16 / kEB;              // channels of a 16-byte block
+  constexpr int kCB = kCG / kChB;             // channel blocks of a tile
+  constexpr int kRotB = 128 / kCB;            // rotation of a row, in bytes, per channel block
   constexpr int kChunks = kE4StageBytes / 16 / 256;  // 16-byte copies per thread per tile
-  static_assert(kCG % 16 == 0 && kTP % 128 == 0 && kChunks * 256 * 16 == kE4StageBytes, "tile");
+  static_assert(kEB == 1 || kEB == 2, "element bytes");
+  static_assert(kRowB % 128 == 0 && kRotB % 16 == 0 && kChunks * 256 * 16 == kE4StageBytes,
+                "tile");
   static_assert(kCB * (kTP / 4) == 256, "one (channel block, position group) per thread");
   static_assert(kE4StageBytes >= kWTileBytes, "a weight tile uses one stage");
-  extern __shared__ __align__(128) uint8_t raw[];  // [kE4Stages][kCG][kTP] bytes, rotated rows
+  extern __shared__ __align__(128) uint8_t raw[];  // [kE4Stages][kCG][kRowB] bytes, rotated rows
   const long long b = blockIdx.x, nb = gridDim.x;
   const long long n_tiles = x_tiles + q.w_blocks;
+  const int ch = p.C / kEB;  // channels (p.C counts bytes of a pixel)
   const long long dhw = (long long)p.D * p.H * p.W;
   const long long pt = (dhw + kTP - 1) / kTP;
-  const int cgn = p.C / kCG;
+  const int cgn = ch / kCG;
   auto tile_src = [&](long long t, int& valid, long long& q0, int& n, int& c0) {
     const long long pi = t % pt, rest = t / pt;  // positions fastest, then channel groups, images
     n = (int)(rest / cgn);
     c0 = (int)(rest % cgn) * kCG;
     q0 = pi * kTP;
-    valid = dhw - q0 < kTP ? (int)(dhw - q0) : kTP;  // a multiple of 16
-    return p.x + ((long long)n * p.C + c0) * dhw + q0;
+    valid = dhw - q0 < kTP ? (int)(dhw - q0) : kTP;  // valid * kEB is a multiple of 16
+    return p.x + (((long long)n * ch + c0) * dhw + q0) * kEB;
   };
   auto issue = [&](long long t, uint8_t* stage) {  // cp.async copies of x tile t, no wait
     int valid, n, c0;
@@ -239,11 +247,12 @@ __global__ void __launch_bounds__(256, kE4BlocksPerSm) pack_x_e4m3_tiled_kernel(
     const uint8_t* src = tile_src(t, valid, q0, n, c0);
 #pragma unroll
     for (int i = 0; i < kChunks; ++i) {
-      const int ch = threadIdx.x + 256 * i;
-      const int r = ch / (kTP / 16), s = ch - r * (kTP / 16);  // row (channel), 16-byte chunk
-      if (16 * s < valid)
-        cp_async_16_zfill(smem_u32(stage + r * kTP + ((16 * s + (r >> 4) * kRotB) & (kTP - 1))),
-                          src + (long long)r * dhw + 16 * s, 16);
+      const int c16 = threadIdx.x + 256 * i;
+      const int r = c16 / (kRowB / 16), s = c16 - r * (kRowB / 16);  // row (channel), chunk
+      if (16 * s < valid * kEB)
+        cp_async_16_zfill(
+            smem_u32(stage + r * kRowB + ((16 * s + (r / kChB) * kRotB) & (kRowB - 1))),
+            src + (long long)r * dhw * kEB + 16 * s, 16);
     }
   };
   const int cb = threadIdx.x % kCB;  // this thread's channel block and position group
@@ -267,25 +276,39 @@ __global__ void __launch_bounds__(256, kE4BlocksPerSm) pack_x_e4m3_tiled_kernel(
       long long q0;
       tile_src(t, valid, q0, n, c0);
       if (4 * qg < valid) {
-        const int col = (4 * qg + cb * kRotB) & (kTP - 1);  // rotated byte column of the group
-        uint32_t v[16];  // v[m]: positions 4qg..4qg+3 of channel 16cb + m
+        // rotated byte column of the group's word in each of its rows
+        const int col = (4 * kEB * qg + cb * kRotB) & (kRowB - 1);
+        const uint8_t* rows = stage + (kChB * cb) * kRowB + col;
+        uint32_t o[4][4];  // o[position][word of the 16-byte chunk]
+        if constexpr (kEB == 1) {
+          uint32_t v[16];  // v[m]: positions 4qg..4qg+3 of channel 16cb + m
 #pragma unroll
-        for (int m = 0; m < 16; ++m)
-          v[m] = *reinterpret_cast<const uint32_t*>(stage + (16 * cb + m) * kTP + col);
-        uint32_t o[4][4];  // o[position][word of 4 channels]
+          for (int m = 0; m < 16; ++m) v[m] = *reinterpret_cast<const uint32_t*>(rows + m * kRowB);
 #pragma unroll
-        for (int bb = 0; bb < 4; ++bb) {
-          uint32_t tt[4];
-          transpose4x4(v + 4 * bb, tt);
+          for (int bb = 0; bb < 4; ++bb) {
+            uint32_t tt[4];
+            transpose4x4(v + 4 * bb, tt);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) o[j][bb] = tt[j];
+            for (int j = 0; j < 4; ++j) o[j][bb] = tt[j];
+          }
+        } else {
+          uint2 v[8];  // v[m]: positions 4qg, 4qg+1 (.x) and 4qg+2, 4qg+3 (.y) of channel 8cb + m
+#pragma unroll
+          for (int m = 0; m < 8; ++m) v[m] = *reinterpret_cast<const uint2*>(rows + m * kRowB);
+#pragma unroll
+          for (int mm = 0; mm < 4; ++mm) {  // channel pair (2mm, 2mm + 1)
+            o[0][mm] = __byte_perm(v[2 * mm].x, v[2 * mm + 1].x, 0x5410);
+            o[1][mm] = __byte_perm(v[2 * mm].x, v[2 * mm + 1].x, 0x7632);
+            o[2][mm] = __byte_perm(v[2 * mm].y, v[2 * mm + 1].y, 0x5410);
+            o[3][mm] = __byte_perm(v[2 * mm].y, v[2 * mm + 1].y, 0x7632);
+          }
         }
         const long long qq = q0 + 4 * qg;  // first position of the group -> (d, h, w); W % 4 == 0
         const int wq = (int)(qq % p.W);    // keeps the four positions in one row
         const long long dh = qq / p.W;
         const int hq = (int)(dh % p.H), dq = (int)(dh / p.H);
         uint8_t* dst = p.xp + ((((long long)n * p.Dp + dq + p.pk_pd) * p.Hp + hq + p.pk_ph) *
-                                   p.Wp + wq + p.pk_pw) * p.C + c0 + 16 * cb;
+                                   p.Wp + wq + p.pk_pw) * p.C + (long long)c0 * kEB + 16 * cb;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
           *reinterpret_cast<uint4*>(dst + (long long)j * p.C) =
@@ -302,12 +325,12 @@ __global__ void __launch_bounds__(256, kE4BlocksPerSm) pack_x_e4m3_tiled_kernel(
     pack_rest_item(p, q, c, g);
 }
 
-template <int kCG>
-static cudaError_t launch_e4m3_tiled(const ConvParams& p, const PackPlan& q, long long x_tiles,
-                                     long long blocks, cudaStream_t stream) {
+template <int kEB, int kCG>
+static cudaError_t launch_transpose(const ConvParams& p, const PackPlan& q, long long x_tiles,
+                                    long long blocks, cudaStream_t stream) {
   // one tile per block: only the first stage is used
   const size_t smem = (size_t)kE4StageBytes * (blocks < x_tiles + q.w_blocks ? kE4Stages : 1);
-  auto k = pack_x_e4m3_tiled_kernel<kCG>;
+  auto k = pack_x_transpose_kernel<kEB, kCG>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   k<<<(unsigned)blocks, 256, smem, stream>>>(p, q, x_tiles);
@@ -433,17 +456,19 @@ cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream) {
     return launch_tiled_ct<kSrcBf16, 16>(p, q, x_tiles, tile_blocks, rest_blocks, stream);
   }
   const long long dhw = (long long)p.D * p.H * p.W;
-  if (q.x_items > 0 && !q.copy && p.elem_bytes == 1 && p.x_src_type == kSrcE4m3 &&
-      p.W % 4 == 0 && dhw % 16 == 0 && p.C % 64 == 0) {
-    // e4m3 bytes, NCDHW: the tiled transpose; the same blocks take the weight tiles and the
-    // remaining items
-    const int cg = p.C % 128 == 0 ? 128 : 64;
-    const long long tp = kE4StageBytes / cg;
-    const long long x_tiles = (long long)p.N * (p.C / cg) * ((dhw + tp - 1) / tp);
+  const int ch = p.C / p.elem_bytes;  // channels
+  if (q.x_items > 0 && !q.copy && p.x_src_type == kSrcE4m3 && p.W % 4 == 0 &&
+      (dhw * p.elem_bytes) % 16 == 0 && ch % 64 == 0) {
+    // e4m3 bytes or the twin's bfloat16, NCDHW: the tiled transpose; the same blocks take the
+    // weight tiles and the remaining items
+    const int cg = p.elem_bytes == 1 && ch % 128 == 0 ? 128 : 64;
+    const long long tp = kE4StageBytes / cg / p.elem_bytes;
+    const long long x_tiles = (long long)p.N * (ch / cg) * ((dhw + tp - 1) / tp);
     const long long blocks =
         std::min<long long>(x_tiles + q.w_blocks, (long long)sms * kE4BlocksPerSm);
-    return cg == 128 ? launch_e4m3_tiled<128>(p, q, x_tiles, blocks, stream)
-                     : launch_e4m3_tiled<64>(p, q, x_tiles, blocks, stream);
+    if (p.elem_bytes == 2) return launch_transpose<2, 64>(p, q, x_tiles, blocks, stream);
+    return cg == 128 ? launch_transpose<1, 128>(p, q, x_tiles, blocks, stream)
+                     : launch_transpose<1, 64>(p, q, x_tiles, blocks, stream);
   }
   const long long total = q.x_items + rest_items;
   long long item_blocks = (total + 255) / 256;
