@@ -186,54 +186,37 @@ static cudaError_t launch_tiled_ct(const ConvParams& p, const PackPlan& q, long 
   return cudaGetLastError();
 }
 
-// Tiled transpose of the interior of an NCDHW x into the channels-last copy, for e4m3 bytes
-// (kEB = 1) and for the BF16 twin's bfloat16 elements (kEB = 2), without rounding anything: the
-// elements move as they are. Shapes: W % 4 == 0 and D*H*W*kEB % 16 == 0. An x tile is kCG channels
-// x kTP consecutive positions of one image's D x H x W volume, 16 KB: kCG runs of kTP elements,
-// one per channel plane. Every block walks the tiles blockIdx.x, + gridDim.x, ... -- the x tiles,
-// then the weight tiles (pack_w_tile) -- through a ring of kE4Stages shared-memory stages:
-//   1. the runs of the x tile two steps ahead go into the free stage with 16-byte cp.async copies
-//      (a warp's 32 copies are whole 128-byte lines of the source), in flight while
-//   2. each thread takes one (16-byte channel block, 4-position group) of the current tile: one
-//      4-position word (e4m3: 4 bytes, bfloat16: 8 bytes) from each of the block's 16 / kEB
-//      channel rows, through byte permutes into four 16-byte chunks, one per position, stored
-//      into the copy. The threads of a position are adjacent in the warp, so one store
-//      instruction writes whole kCG * kEB-byte runs of pixel rows.
-// Row r of a stage keeps its 16-byte chunks rotated by (r * kEB / 16) * 128 / kCB bytes (kCB:
-// channel blocks of a tile), so that the words a warp (bfloat16: a half-warp) reads in step 2 fall
-// in 32 different banks. Then the blocks share the remaining items (halo chunks, weights by
-// items) in a grid-stride loop. The item path this replaces for these shapes held 16 x 16 bytes a
-// thread in registers (100 registers, two blocks an SM) and ran its one-shot blocks in waves:
-// 31.4 us for the large layer's x, against 18.5 us for each further image of the same size.
-// Weight tiles in blocks of their own could not share an SM with the persistent blocks' stages
-// and ran after them.
-constexpr int kE4Stages = 3;
-constexpr int kE4StageBytes = 16384;
-constexpr int kE4BlocksPerSm = 4;  // 3 stages of 16 KB each; <= 64 registers a thread
+// The ring of the tiled packs. An x tile is kCG channels x kTP consecutive positions of one
+// image's D x H x W volume, 16 KB: kCG runs of kTP source elements (kEB bytes each), one per
+// channel plane. Every block walks the tiles blockIdx.x, + gridDim.x, ... -- the x tiles, then the
+// weight tiles (pack_w_tile) -- through kRingStages shared-memory stages: the runs of the x tile
+// two steps ahead arrive by 16-byte cp.async copies (a warp's 32 copies are whole 128-byte lines
+// of the source) while tile_fn turns the current stage into 16-byte chunks of the channels-last
+// copy. Row r of a stage keeps its 16-byte chunks rotated by (r / kRotRows) * kRotB bytes, which
+// tile_fn's reads undo (each tile_fn picks the rotation that spreads its warp's words over the 32
+// banks). Then the blocks share the remaining items (halo chunks, weights by items) in a
+// grid-stride loop. Persistent blocks keep every SM streaming to the end; one-shot blocks ran in
+// waves, and weight tiles in blocks of their own could not share an SM with the stages and ran
+// after them. `ch` = channels of x; every block calls it with the same arguments.
+constexpr int kRingStages = 3;
+constexpr int kRingStageBytes = 16384;
+constexpr int kRingBlocksPerSm = 4;  // 3 stages of 16 KB each; <= 64 registers a thread
 
-template <int kEB, int kCG>
-__global__ void __launch_bounds__(256, kE4BlocksPerSm) pack_x_transpose_kernel(
-    ConvParams p, PackPlan q, long long x_tiles) {
-  pdl_launch_dependents();  // the implicit GEMM may start its prologue while the pack runs
-  constexpr int kRowB = kE4StageBytes / kCG;  // bytes of a stage row
-  constexpr int kTP = kRowB / kEB;            // positions of a tile
-  constexpr int kChB = 16 / kEB;              // channels of a 16-byte block
-  constexpr int kCB = kCG / kChB;             // channel blocks of a tile
-  constexpr int kRotB = 128 / kCB;            // rotation of a row, in bytes, per channel block
-  constexpr int kChunks = kE4StageBytes / 16 / 256;  // 16-byte copies per thread per tile
-  static_assert(kEB == 1 || kEB == 2, "element bytes");
-  static_assert(kRowB % 128 == 0 && kRotB % 16 == 0 && kChunks * 256 * 16 == kE4StageBytes,
+template <int kEB, int kCG, int kRotRows, int kRotB, class TileFn>
+__device__ __forceinline__ void pack_ring(const ConvParams& p, const PackPlan& q, long long x_tiles,
+                                          int ch, uint8_t* raw, TileFn&& tile_fn) {
+  constexpr int kRowB = kRingStageBytes / kCG;  // bytes of a stage row
+  constexpr int kTP = kRowB / kEB;              // positions of a tile
+  constexpr int kChunks = kRingStageBytes / 16 / 256;  // 16-byte copies per thread per tile
+  static_assert(kRowB % 128 == 0 && kRotB % 16 == 0 && kChunks * 256 * 16 == kRingStageBytes,
                 "tile");
-  static_assert(kCB * (kTP / 4) == 256, "one (channel block, position group) per thread");
-  static_assert(kE4StageBytes >= kWTileBytes, "a weight tile uses one stage");
-  extern __shared__ __align__(128) uint8_t raw[];  // [kE4Stages][kCG][kRowB] bytes, rotated rows
+  static_assert(kRingStageBytes >= kWTileBytes, "a weight tile uses one stage");
   const long long b = blockIdx.x, nb = gridDim.x;
   const long long n_tiles = x_tiles + q.w_blocks;
-  const int ch = p.C / kEB;  // channels (p.C counts bytes of a pixel)
   const long long dhw = (long long)p.D * p.H * p.W;
   const long long pt = (dhw + kTP - 1) / kTP;
   const int cgn = ch / kCG;
-  auto tile_src = [&](long long t, int& valid, long long& q0, int& n, int& c0) {
+  auto tile_at = [&](long long t, int& valid, long long& q0, int& n, int& c0) {
     const long long pi = t % pt, rest = t / pt;  // positions fastest, then channel groups, images
     n = (int)(rest / cgn);
     c0 = (int)(rest % cgn) * kCG;
@@ -244,28 +227,26 @@ __global__ void __launch_bounds__(256, kE4BlocksPerSm) pack_x_transpose_kernel(
   auto issue = [&](long long t, uint8_t* stage) {  // cp.async copies of x tile t, no wait
     int valid, n, c0;
     long long q0;
-    const uint8_t* src = tile_src(t, valid, q0, n, c0);
+    const uint8_t* src = tile_at(t, valid, q0, n, c0);
 #pragma unroll
     for (int i = 0; i < kChunks; ++i) {
       const int c16 = threadIdx.x + 256 * i;
       const int r = c16 / (kRowB / 16), s = c16 - r * (kRowB / 16);  // row (channel), chunk
       if (16 * s < valid * kEB)
         cp_async_16_zfill(
-            smem_u32(stage + r * kRowB + ((16 * s + (r / kChB) * kRotB) & (kRowB - 1))),
+            smem_u32(stage + r * kRowB + ((16 * s + (r / kRotRows) * kRotB) & (kRowB - 1))),
             src + (long long)r * dhw * kEB + 16 * s, 16);
     }
   };
-  const int cb = threadIdx.x % kCB;  // this thread's channel block and position group
-  const int qg = threadIdx.x / kCB;
   if (b < x_tiles) issue(b, raw);
   cp_async_commit();
-  if (b + nb < x_tiles) issue(b + nb, raw + kE4StageBytes);
+  if (b + nb < x_tiles) issue(b + nb, raw + kRingStageBytes);
   cp_async_commit();
   int sidx = 0;
   for (long long t = b; t < n_tiles; t += nb) {
-    uint8_t* stage = raw + sidx * kE4StageBytes;
+    uint8_t* stage = raw + sidx * kRingStageBytes;
     const long long t2 = t + 2 * nb;  // into the stage freed at the end of the last step
-    if (t2 < x_tiles) issue(t2, raw + ((sidx + 2) % kE4Stages) * kE4StageBytes);
+    if (t2 < x_tiles) issue(t2, raw + ((sidx + 2) % kRingStages) * kRingStageBytes);
     cp_async_commit();
     cp_async_wait_group<2>();  // this thread's copies of tile t have landed
     __syncthreads();           // and everyone else's
@@ -274,49 +255,11 @@ __global__ void __launch_bounds__(256, kE4BlocksPerSm) pack_x_transpose_kernel(
     } else {
       int valid, n, c0;
       long long q0;
-      tile_src(t, valid, q0, n, c0);
-      if (4 * qg < valid) {
-        // rotated byte column of the group's word in each of its rows
-        const int col = (4 * kEB * qg + cb * kRotB) & (kRowB - 1);
-        const uint8_t* rows = stage + (kChB * cb) * kRowB + col;
-        uint32_t o[4][4];  // o[position][word of the 16-byte chunk]
-        if constexpr (kEB == 1) {
-          uint32_t v[16];  // v[m]: positions 4qg..4qg+3 of channel 16cb + m
-#pragma unroll
-          for (int m = 0; m < 16; ++m) v[m] = *reinterpret_cast<const uint32_t*>(rows + m * kRowB);
-#pragma unroll
-          for (int bb = 0; bb < 4; ++bb) {
-            uint32_t tt[4];
-            transpose4x4(v + 4 * bb, tt);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) o[j][bb] = tt[j];
-          }
-        } else {
-          uint2 v[8];  // v[m]: positions 4qg, 4qg+1 (.x) and 4qg+2, 4qg+3 (.y) of channel 8cb + m
-#pragma unroll
-          for (int m = 0; m < 8; ++m) v[m] = *reinterpret_cast<const uint2*>(rows + m * kRowB);
-#pragma unroll
-          for (int mm = 0; mm < 4; ++mm) {  // channel pair (2mm, 2mm + 1)
-            o[0][mm] = __byte_perm(v[2 * mm].x, v[2 * mm + 1].x, 0x5410);
-            o[1][mm] = __byte_perm(v[2 * mm].x, v[2 * mm + 1].x, 0x7632);
-            o[2][mm] = __byte_perm(v[2 * mm].y, v[2 * mm + 1].y, 0x5410);
-            o[3][mm] = __byte_perm(v[2 * mm].y, v[2 * mm + 1].y, 0x7632);
-          }
-        }
-        const long long qq = q0 + 4 * qg;  // first position of the group -> (d, h, w); W % 4 == 0
-        const int wq = (int)(qq % p.W);    // keeps the four positions in one row
-        const long long dh = qq / p.W;
-        const int hq = (int)(dh % p.H), dq = (int)(dh / p.H);
-        uint8_t* dst = p.xp + ((((long long)n * p.Dp + dq + p.pk_pd) * p.Hp + hq + p.pk_ph) *
-                                   p.Wp + wq + p.pk_pw) * p.C + (long long)c0 * kEB + 16 * cb;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(dst + (long long)j * p.C) =
-              make_uint4(o[j][0], o[j][1], o[j][2], o[j][3]);
-      }
+      tile_at(t, valid, q0, n, c0);
+      tile_fn(static_cast<const uint8_t*>(stage), valid, q0, n, c0);
     }
     __syncthreads();  // the stage is free for the copies three tiles on
-    sidx = (sidx + 1) % kE4Stages;
+    sidx = (sidx + 1) % kRingStages;
   }
   cp_async_wait_all();
   const PackCtx c = pack_ctx(p, q);
@@ -325,15 +268,88 @@ __global__ void __launch_bounds__(256, kE4BlocksPerSm) pack_x_transpose_kernel(
     pack_rest_item(p, q, c, g);
 }
 
+// Byte offset in the channels-last copy of position qq of image n's volume, channel byte cb0. The
+// ring kernels run only for D*H*W < 2^31, so the position splits into (d, h, w) with 32-bit
+// unsigned divisions (a 64-bit division is a long subroutine, and there is one per item).
+__device__ __forceinline__ long long xp_offset(const ConvParams& p, int n, long long qq, int cb0) {
+  const unsigned u = (unsigned)qq, W = (unsigned)p.W, H = (unsigned)p.H;
+  const unsigned dh = u / W, wq = u - dh * W;
+  const unsigned dq = dh / H, hq = dh - dq * H;
+  return ((((long long)n * p.Dp + dq + p.pk_pd) * p.Hp + hq + p.pk_ph) * p.Wp + wq + p.pk_pw) *
+             p.C + cb0;
+}
+
+// Tiled transpose of an NCDHW x into the channels-last copy, for e4m3 bytes (kEB = 1) and for the
+// BF16 twin's bfloat16 elements (kEB = 2), without rounding anything: the elements move as they
+// are. Shapes: W % 4 == 0, D*H*W*kEB % 16 == 0, C % kCG == 0. A tile is 128 (e4m3, C % 128 == 0)
+// or 64 channels. Each thread takes one (16-byte channel block, 4-position group) of a tile: one
+// 4-position word (e4m3: 4 bytes, bfloat16: 8 bytes) from each of the block's 16 / kEB channel
+// rows, through byte permutes into four 16-byte chunks, one per position. The threads of a
+// position are adjacent in the warp, so one store instruction writes whole kCG * kEB-byte runs of
+// pixel rows. Rows rotate by 128 / (channel blocks of a tile) bytes per channel block, so that
+// the words a warp (bfloat16: a half-warp) reads fall in 32 different banks. The item path this
+// replaced for these shapes held 16 x 16 bytes a thread in registers (100 registers, two blocks an
+// SM): 31.4 us for the large layer's x, against 18.5 us for each further image of the same size.
 template <int kEB, int kCG>
-static cudaError_t launch_transpose(const ConvParams& p, const PackPlan& q, long long x_tiles,
-                                    long long blocks, cudaStream_t stream) {
+__global__ void __launch_bounds__(256, kRingBlocksPerSm) pack_x_transpose_kernel(
+    ConvParams p, PackPlan q, long long x_tiles) {
+  pdl_launch_dependents();  // the implicit GEMM may start its prologue while the pack runs
+  constexpr int kRowB = kRingStageBytes / kCG;
+  constexpr int kChB = 16 / kEB;   // channels of a 16-byte block
+  constexpr int kCB = kCG / kChB;  // channel blocks of a tile
+  constexpr int kRotB = 128 / kCB;
+  static_assert(kEB == 1 || kEB == 2, "element bytes");
+  static_assert(kCB * (kRowB / kEB / 4) == 256, "one (channel block, position group) per thread");
+  extern __shared__ __align__(16) uint8_t raw[];  // [kRingStages][kCG][kRowB] bytes
+  const int cb = threadIdx.x % kCB;  // this thread's channel block and position group
+  const int qg = threadIdx.x / kCB;
+  pack_ring<kEB, kCG, kChB, kRotB>(p, q, x_tiles, p.C / kEB, raw,
+      [&](const uint8_t* stage, int valid, long long q0, int n, int c0) {
+    if (4 * qg >= valid) return;
+    // the group's word in each of its rows, at the rotated byte column
+    const uint8_t* rows = stage + (kChB * cb) * kRowB + ((4 * kEB * qg + cb * kRotB) & (kRowB - 1));
+    uint32_t o[4][4];  // o[position][word of the 16-byte chunk]
+    if constexpr (kEB == 1) {
+      uint32_t v[16];  // v[m]: positions 4qg..4qg+3 of channel 16cb + m
+#pragma unroll
+      for (int m = 0; m < 16; ++m) v[m] = *reinterpret_cast<const uint32_t*>(rows + m * kRowB);
+#pragma unroll
+      for (int bb = 0; bb < 4; ++bb) {
+        uint32_t tt[4];
+        transpose4x4(v + 4 * bb, tt);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j][bb] = tt[j];
+      }
+    } else {
+      uint2 v[8];  // v[m]: positions 4qg, 4qg+1 (.x) and 4qg+2, 4qg+3 (.y) of channel 8cb + m
+#pragma unroll
+      for (int m = 0; m < 8; ++m) v[m] = *reinterpret_cast<const uint2*>(rows + m * kRowB);
+#pragma unroll
+      for (int mm = 0; mm < 4; ++mm) {  // channel pair (2mm, 2mm + 1)
+        o[0][mm] = __byte_perm(v[2 * mm].x, v[2 * mm + 1].x, 0x5410);
+        o[1][mm] = __byte_perm(v[2 * mm].x, v[2 * mm + 1].x, 0x7632);
+        o[2][mm] = __byte_perm(v[2 * mm].y, v[2 * mm + 1].y, 0x5410);
+        o[3][mm] = __byte_perm(v[2 * mm].y, v[2 * mm + 1].y, 0x7632);
+      }
+    }
+    // W % 4 == 0 keeps the group's four positions in one row
+    uint8_t* dst = p.xp + xp_offset(p, n, q0 + 4 * qg, c0 * kEB + 16 * cb);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      *reinterpret_cast<uint4*>(dst + (long long)j * p.C) =
+          make_uint4(o[j][0], o[j][1], o[j][2], o[j][3]);
+  });
+}
+
+template <class K>
+static cudaError_t launch_ring(K kernel, const ConvParams& p, const PackPlan& q, long long x_tiles,
+                               long long blocks, cudaStream_t stream) {
   // one tile per block: only the first stage is used
-  const size_t smem = (size_t)kE4StageBytes * (blocks < x_tiles + q.w_blocks ? kE4Stages : 1);
-  auto k = pack_x_transpose_kernel<kEB, kCG>;
-  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const size_t smem = (size_t)kRingStageBytes * (blocks < x_tiles + q.w_blocks ? kRingStages : 1);
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
   if (e != cudaSuccess) return e;
-  k<<<(unsigned)blocks, 256, smem, stream>>>(p, q, x_tiles);
+  kernel<<<(unsigned)blocks, 256, smem, stream>>>(p, q, x_tiles);
   return cudaGetLastError();
 }
 
@@ -433,16 +449,19 @@ cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long cap = (long long)sms * 16;
   const long long rest_items = q.halo_row_items + q.halo_side_items + q.w_items;
+  const long long dhw = (long long)p.D * p.H * p.W;
   if (q.x_items > 0 && !q.copy && p.elem_bytes == 1 && p.x_src_type != kSrcE4m3) {
     // an NCDHW x quantised on the way: the tiled transpose, plus blocks for the remaining items
-    // and the weight tiles (for e4m3 bytes the item path measured faster: 26 us against 55 us on
-    // the large layer). bfloat16 x: persistent blocks over 32-channel tiles in two 32 KB stages
-    // (large layer step 332 -> 323 us against one tile per block); fp32 x: one 32-channel tile
-    // (64 KB) per block (the two-stage forms measured 364 us with 16 channels, 399 us with 32 on
-    // one block per SM, against 362 us).
+    // and the weight tiles. bfloat16 x: persistent blocks over 32-channel tiles in two 32 KB
+    // stages (large layer step 332 -> 323 us against one tile per block); fp32 x: one 32-channel
+    // tile (64 KB) per block (the two-stage forms measured 364 us with 16 channels, 399 us with
+    // 32 on one block per SM, against 362 us). The ring of the plain transposes (16 KB tiles of
+    // 32 channels x 128 / 256 positions, 4 blocks an SM, one 16-channel column of a position a
+    // thread, a position's 32 bytes written by one instruction) measured slower here, bit-exact
+    // all the same: the large layer's pack 74.5 -> 82.3 us from fp32, 61.7 -> 67.7 us from
+    // bfloat16.
     const bool f32 = p.x_src_type == kSrcF32;
     const int ct = p.C % 32 == 0 ? 32 : 16;
-    const long long dhw = (long long)p.D * p.H * p.W;
     const long long x_tiles = (long long)p.N * (p.C / ct) * ((dhw + kTileP - 1) / kTileP);
     const long long tile_blocks =
         f32 ? x_tiles : std::min<long long>(x_tiles, (long long)sms * kTiledBlocksPerSm);
@@ -455,20 +474,20 @@ cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream) {
       return launch_tiled_ct<kSrcBf16, 32>(p, q, x_tiles, tile_blocks, rest_blocks, stream);
     return launch_tiled_ct<kSrcBf16, 16>(p, q, x_tiles, tile_blocks, rest_blocks, stream);
   }
-  const long long dhw = (long long)p.D * p.H * p.W;
   const int ch = p.C / p.elem_bytes;  // channels
   if (q.x_items > 0 && !q.copy && p.x_src_type == kSrcE4m3 && p.W % 4 == 0 &&
-      (dhw * p.elem_bytes) % 16 == 0 && ch % 64 == 0) {
+      (dhw * p.elem_bytes) % 16 == 0 && ch % 64 == 0 && dhw < (1LL << 31)) {
     // e4m3 bytes or the twin's bfloat16, NCDHW: the tiled transpose; the same blocks take the
     // weight tiles and the remaining items
     const int cg = p.elem_bytes == 1 && ch % 128 == 0 ? 128 : 64;
-    const long long tp = kE4StageBytes / cg / p.elem_bytes;
+    const long long tp = kRingStageBytes / cg / p.elem_bytes;
     const long long x_tiles = (long long)p.N * (ch / cg) * ((dhw + tp - 1) / tp);
     const long long blocks =
-        std::min<long long>(x_tiles + q.w_blocks, (long long)sms * kE4BlocksPerSm);
-    if (p.elem_bytes == 2) return launch_transpose<2, 64>(p, q, x_tiles, blocks, stream);
-    return cg == 128 ? launch_transpose<1, 128>(p, q, x_tiles, blocks, stream)
-                     : launch_transpose<1, 64>(p, q, x_tiles, blocks, stream);
+        std::min<long long>(x_tiles + q.w_blocks, (long long)sms * kRingBlocksPerSm);
+    if (p.elem_bytes == 2)
+      return launch_ring(pack_x_transpose_kernel<2, 64>, p, q, x_tiles, blocks, stream);
+    return cg == 128 ? launch_ring(pack_x_transpose_kernel<1, 128>, p, q, x_tiles, blocks, stream)
+                     : launch_ring(pack_x_transpose_kernel<1, 64>, p, q, x_tiles, blocks, stream);
   }
   const long long total = q.x_items + rest_items;
   long long item_blocks = (total + 255) / 256;
