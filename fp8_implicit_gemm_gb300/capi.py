@@ -99,6 +99,10 @@ def load() -> ctypes.CDLL:
                                                 + [ctypes.POINTER(Options)])
             lib.conv3d_bf16_run.restype = ci
             lib.conv3d_bf16_run.argtypes = [vp, vp, vp, vp, i3, i3, vp]
+            lib.conv3d_fp8_run_host.restype = ci
+            lib.conv3d_fp8_run_host.argtypes = [vp, vp, vp, vp, vp, i3, i3, vp]
+            lib.conv3d_bf16_run_host.restype = ci
+            lib.conv3d_bf16_run_host.argtypes = [vp, vp, vp, vp, i3, i3, vp]
             lib.conv3d_bf16_describe.restype = ci
             lib.conv3d_bf16_describe.argtypes = ([ci] * 9 + [i3, i3, ci, ctypes.POINTER(Options),
                                                              ctypes.POINTER(PlanInfo)])
@@ -150,6 +154,19 @@ def _ptr(t) -> int:
     return t.data_ptr()
 
 
+def _host_ptr(t) -> int:
+    """Host address of a CPU torch tensor (or an int address, passed through)."""
+    if t is None:
+        return 0
+    if isinstance(t, int):
+        return t
+    if t.is_cuda:
+        raise ValueError("expected a CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
 def _stream(stream) -> int:
     if stream is None:
         import torch
@@ -195,6 +212,21 @@ def conv3d_fp8_run_status(plan, x, w, scale_x, scale_w, y, stride, pad, stream=N
     """As conv3d_fp8_run, but returns the status code instead of raising."""
     return load().conv3d_fp8_run(plan, _ptr(x), _ptr(w), _ptr(scale_x), _ptr(scale_w), _ptr(y),
                                  _int3(stride), _int3(pad), _stream(stream))
+
+
+def conv3d_fp8_run_host_status(plan, x_host, w_host, scales_host, y_host, stride, pad,
+                               stream=None) -> int:
+    """conv3d_fp8_run_host: CPU tensors (page-locked for asynchronous copies); scales_host holds
+    (scale_x, scale_w) as fp32. Returns the status code."""
+    return load().conv3d_fp8_run_host(plan, _host_ptr(x_host), _host_ptr(w_host),
+                                      _host_ptr(scales_host), _host_ptr(y_host), _int3(stride),
+                                      _int3(pad), _stream(stream))
+
+
+def conv3d_fp8_run_host(plan, x_host, w_host, scales_host, y_host, stride, pad,
+                        stream=None) -> None:
+    _raise(conv3d_fp8_run_host_status(plan, x_host, w_host, scales_host, y_host, stride, pad,
+                                      stream), "conv3d_fp8_run_host")
 
 
 def conv3d_fp8_run_noalloc_status(N, C, D, H, W, K, T, R, S, stride, pad, x, w, scale_x,
@@ -318,6 +350,17 @@ def conv3d_bf16_run_status(plan, x, w, y, stride, pad, stream=None) -> int:
 
 def conv3d_bf16_run(plan, x, w, y, stride, pad, stream=None) -> None:
     _raise(conv3d_bf16_run_status(plan, x, w, y, stride, pad, stream), "conv3d_bf16_run")
+
+
+def conv3d_bf16_run_host_status(plan, x_host, w_host, y_host, stride, pad, stream=None) -> int:
+    return load().conv3d_bf16_run_host(plan, _host_ptr(x_host), _host_ptr(w_host),
+                                       _host_ptr(y_host), _int3(stride), _int3(pad),
+                                       _stream(stream))
+
+
+def conv3d_bf16_run_host(plan, x_host, w_host, y_host, stride, pad, stream=None) -> None:
+    _raise(conv3d_bf16_run_host_status(plan, x_host, w_host, y_host, stride, pad, stream),
+           "conv3d_bf16_run_host")
 
 
 def conv3d_bf16_describe_status(N, C, D, H, W, K, T, R, S, stride, pad, sm_count,

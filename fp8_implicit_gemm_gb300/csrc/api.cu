@@ -31,6 +31,7 @@ struct conv3d_fp8_plan_s {
   cudaEvent_t ev_begin = nullptr;  // measurement hook, caller-owned
   cudaEvent_t ev_end = nullptr;
   cudaEvent_t ev_pack = nullptr;   // measurement hook before the pack, caller-owned
+  void* host_stage = nullptr;      // device copies of the host-buffer runs' x, w, scales and y
 };
 
 namespace {
@@ -658,9 +659,70 @@ conv3d_status run_impl(conv3d_fp8_plan_t plan, const void* x, const void* w,
   return CONV3D_OK;
 }
 
+// Runs with host buffers: x, w and (e4m3 plans) the two scales are copied into device buffers the
+// plan owns, the run reads them there, and y is copied back; one cudaMemcpyAsync per copy, all on
+// the caller's stream, in that order.
+conv3d_status run_host_impl(conv3d_fp8_plan_t plan, const void* x_host, const void* w_host,
+                            const float* scales_host, void* y_host, const int stride[3],
+                            const int pad[3], void* stream) {
+  if (!plan || !x_host || !w_host || !y_host || !stride || !pad) return CONV3D_EINVAL;
+  if (plan->elem_bytes == 1 && !scales_host) return CONV3D_EINVAL;
+  for (int i = 0; i < 3; ++i)
+    if (stride[i] != plan->stride[i] || pad[i] != plan->pad[i]) return CONV3D_EINVAL;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return CONV3D_ECUDA;
+  if (cur != plan->device) return CONV3D_EINVAL;
+  const ConvParams& q = plan->p;  // C counts bytes of a pixel
+  const size_t x_bytes = (size_t)q.N * q.C * q.D * q.H * q.W;
+  const size_t w_bytes = (size_t)q.K * q.C * q.taps;
+  const size_t y_bytes = (size_t)q.npq * q.K * 2;
+  const size_t off_w = (size_t)round_up((long long)x_bytes, 256);
+  const size_t off_s = off_w + (size_t)round_up((long long)w_bytes, 256);
+  const size_t off_y = off_s + 256;
+  const size_t total = off_y + (size_t)round_up((long long)y_bytes, 256);
+  if (!plan->host_stage && cudaMalloc(&plan->host_stage, total) != cudaSuccess) {
+    cudaGetLastError();
+    plan->host_stage = nullptr;
+    return CONV3D_ENOMEM;
+  }
+  uint8_t* st = static_cast<uint8_t*>(plan->host_stage);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(st, x_host, x_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(st + off_w, w_host, w_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return CONV3D_ECUDA;
+  const float* sx = plan->ones;
+  const float* sw = plan->ones + 1;
+  if (plan->elem_bytes == 1) {
+    if (cudaMemcpyAsync(st + off_s, scales_host, 2 * sizeof(float), cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+      return CONV3D_ECUDA;
+    sx = reinterpret_cast<const float*>(st + off_s);
+    sw = sx + 1;
+  }
+  const conv3d_status rs = run_impl(plan, st, st + off_w, sx, sw, st + off_y, stride, pad, stream);
+  if (rs != CONV3D_OK) return rs;
+  if (cudaMemcpyAsync(y_host, st + off_y, y_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return CONV3D_ECUDA;
+  return CONV3D_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+conv3d_status conv3d_fp8_run_host(conv3d_fp8_plan_t plan, const void* x_host, const void* w_host,
+                                  const float* scales, void* y_host, const int stride[3],
+                                  const int pad[3], void* stream) {
+  if (plan && plan->elem_bytes != 1) return CONV3D_EINVAL;
+  return run_host_impl(plan, x_host, w_host, scales, y_host, stride, pad, stream);
+}
+
+conv3d_status conv3d_bf16_run_host(conv3d_fp8_plan_t plan, const void* x_host, const void* w_host,
+                                   void* y_host, const int stride[3], const int pad[3],
+                                   void* stream) {
+  if (!plan || plan->elem_bytes != 2) return CONV3D_EINVAL;
+  return run_host_impl(plan, x_host, w_host, nullptr, y_host, stride, pad, stream);
+}
 
 conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t* out, int N, int C, int D, int H, int W, int K,
                                  int T, int R, int S, const int stride[3], const int pad[3],
@@ -815,6 +877,7 @@ void conv3d_fp8_destroy(conv3d_fp8_plan_t plan) {
     if (guard.set(plan->device) == cudaSuccess) {
       cudaDeviceSynchronize();
       cudaFree(plan->workspace);
+      cudaFree(plan->host_stage);
     }
   }
   delete plan;

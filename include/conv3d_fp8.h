@@ -20,8 +20,10 @@
  * Conventions for every entry point:
  *   - Returns a conv3d_status. Argument errors are reported before anything is launched.
  *   - Device pointers are plain CUDA device addresses on the plan's device; the caller owns them.
+ *     Only the *_run_host calls take host pointers (x_host, w_host, scales, y_host).
  *   - "stream" is a cudaStream_t passed as void*; NULL means the legacy default stream.
- *   - Nothing here synchronises the device except conv3d_fp8_check and conv3d_fp8_destroy.
+ *   - Nothing here synchronises the device except conv3d_fp8_check and conv3d_fp8_destroy (and
+ *     the allocation of a plan's device buffers by its first *_run_host call).
  */
 #ifndef CONV3D_FP8_H
 #define CONV3D_FP8_H
@@ -158,6 +160,27 @@ conv3d_status conv3d_fp8_plan_ex(conv3d_fp8_plan_t *plan, int N, int C, int D, i
 conv3d_status conv3d_fp8_run(conv3d_fp8_plan_t plan, const void *x_ncdhw, const void *w_kctrs,
                              const float *scale_x, const float *scale_w, void *y_ncdhw,
                              const int stride[3], const int pad[3], void *stream);
+
+/*
+ * conv3d_fp8_run with the tensors in host memory (defined by: none -- library plumbing around
+ * conv3d_fp8_run, for callers whose data lives on the host). Enqueued on `stream`, in this order:
+ * copies of x_host (N*C*D*H*W e4m3 bytes, in the plan's input layout), w_host (K*C*T*R*S bytes)
+ * and scales[0] = scale_x, scales[1] = scale_w (two fp32) into device buffers the plan owns; the
+ * run of conv3d_fp8_run on those buffers; a copy of y (N*K*Do*Ho*Wo bfloat16, NCDHW) into y_host.
+ * One cudaMemcpyAsync per copy. The call returns once all of it is enqueued: y_host holds the
+ * result after the stream has passed that point (e.g. cudaStreamSynchronize). The device buffers
+ * (x, w, y, each rounded up to 256 bytes, plus 256) are allocated by the plan's first such call
+ * and freed by conv3d_fp8_destroy; conv3d_fp8_workspace_size does not count them. The host
+ * buffers stay caller-owned; page-locked ones (cudaHostAlloc / cudaHostRegister) let the copies
+ * run asynchronously and overlap work on other streams, pageable ones work too (the copies are
+ * then staged by the driver). As for conv3d_fp8_run, at most one run of a plan is in flight at a
+ * time: to overlap one step's copies with another's compute, use one plan per stream.
+ * Errors: EINVAL (NULL pointer, a bfloat16 plan, stride / pad / device mismatch), ENOMEM (the
+ * device buffers), ECUDA; then as conv3d_fp8_run.
+ */
+conv3d_status conv3d_fp8_run_host(conv3d_fp8_plan_t plan, const void *x_host, const void *w_host,
+                                  const float scales[2], void *y_host, const int stride[3],
+                                  const int pad[3], void *stream);
 
 /*
  * Measurement hook: while ev_begin / ev_end (cudaEvent_t values passed as void*; either may be
@@ -316,6 +339,10 @@ conv3d_status conv3d_bf16_plan_ex(conv3d_fp8_plan_t *plan, int N, int C, int D, 
                                   const int pad[3], int device, const conv3d_fp8_options *opts);
 conv3d_status conv3d_bf16_run(conv3d_fp8_plan_t plan, const void *x_ncdhw, const void *w_kctrs,
                               void *y_ncdhw, const int stride[3], const int pad[3], void *stream);
+/* The twin of conv3d_fp8_run_host: bfloat16 x_host and w_host (2 bytes an element), no scales. */
+conv3d_status conv3d_bf16_run_host(conv3d_fp8_plan_t plan, const void *x_host, const void *w_host,
+                                   void *y_host, const int stride[3], const int pad[3],
+                                   void *stream);
 /* Host-only planning of the BF16 twin, as conv3d_fp8_describe. */
 conv3d_status conv3d_bf16_describe(int N, int C, int D, int H, int W, int K, int T, int R, int S,
                                    const int stride[3], const int pad[3], int sm_count,

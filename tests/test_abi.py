@@ -1,5 +1,6 @@
 """C-ABI checks that need no GPU: the library loads, exports every declared entry point, and its
 host-only planning and validation behave as documented in include/conv3d_fp8.h."""
+import ctypes
 import os
 import re
 
@@ -20,13 +21,14 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(conv3d_fp8_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(conv3d_(?:fp8|bf16)_[a-z_0-9]+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
     names = declared_functions()
     for n in ("conv3d_fp8_plan", "conv3d_fp8_run", "conv3d_fp8_destroy",
-              "conv3d_fp8_workspace_size", "conv3d_fp8_strerror"):
+              "conv3d_fp8_workspace_size", "conv3d_fp8_strerror", "conv3d_fp8_run_host",
+              "conv3d_bf16_plan", "conv3d_bf16_run", "conv3d_bf16_run_host"):
         assert n in names
 
 
@@ -283,3 +285,8 @@ def test_null_plan_entry_points(lib):
     capi.conv3d_fp8_destroy(None)
     assert lib.conv3d_fp8_set_timing_events(None, None, None) == capi.CONV3D_EINVAL
     assert lib.conv3d_fp8_set_pack_timing_event(None, None) == capi.CONV3D_EINVAL
+    # the host-buffer runs reject a missing plan before any copy or allocation
+    st3 = (ctypes.c_int * 3)(1, 1, 1)
+    assert lib.conv3d_fp8_run_host(None, None, None, None, None, st3, st3,
+                                   None) == capi.CONV3D_EINVAL
+    assert lib.conv3d_bf16_run_host(None, None, None, None, st3, st3, None) == capi.CONV3D_EINVAL
