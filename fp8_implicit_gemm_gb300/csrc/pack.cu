@@ -193,9 +193,9 @@ static cudaError_t launch_tiled_ct(const ConvParams& p, const PackPlan& q, long 
 // two steps ahead arrive by 16-byte cp.async copies (a warp's 32 copies are whole 128-byte lines
 // of the source) while tile_fn turns the current stage into 16-byte chunks of the channels-last
 // copy. Row r of a stage keeps its 16-byte chunks rotated by (r / kRotRows) * kRotB bytes, which
-// tile_fn's reads undo (each tile_fn picks the rotation that spreads its warp's words over the 32
-// banks). Then the blocks share the remaining items (halo chunks, weights by items) in a
-// grid-stride loop. Persistent blocks keep every SM streaming to the end; one-shot blocks ran in
+// tile_fn's reads undo (each kernel picks kRotRows and kRotB so that the words its warps read
+// fall in distinct banks). Then the blocks share the remaining items (halo chunks, weights by
+// items) in a grid-stride loop. Persistent blocks keep every SM streaming to the end; one-shot blocks ran in
 // waves, and weight tiles in blocks of their own could not share an SM with the stages and ran
 // after them. `ch` = channels of x; every block calls it with the same arguments.
 constexpr int kRingStages = 3;
