@@ -195,9 +195,9 @@ static cudaError_t launch_tiled_ct(const ConvParams& p, const PackPlan& q, long 
 // copy. Row r of a stage keeps its 16-byte chunks rotated by (r / kRotRows) * kRotB bytes, which
 // tile_fn's reads undo (each kernel picks kRotRows and kRotB so that the words its warps read
 // fall in distinct banks). Then the blocks share the remaining items (halo chunks, weights by
-// items) in a grid-stride loop. Persistent blocks keep every SM streaming to the end; one-shot blocks ran in
-// waves, and weight tiles in blocks of their own could not share an SM with the stages and ran
-// after them. `ch` = channels of x; every block calls it with the same arguments.
+// items) in a grid-stride loop. Persistent blocks keep every SM streaming to the end; one-shot
+// blocks ran in waves, and weight tiles in blocks of their own could not share an SM with the
+// stages and ran after them. `ch` = channels of x; every block calls it with the same arguments.
 constexpr int kRingStages = 3;
 constexpr int kRingStageBytes = 16384;
 constexpr int kRingBlocksPerSm = 4;  // 3 stages of 16 KB each; <= 64 registers a thread
