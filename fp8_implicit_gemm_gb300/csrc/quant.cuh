@@ -37,15 +37,14 @@ __device__ __forceinline__ float scale_from_amax(unsigned amax_bits) {
   return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
 }
 
-// Four values -> four e4m3 codes (the first in the lowest byte).
+// Four values -> four e4m3 codes (the first in the lowest byte). The clamp to +-448 is the
+// conversion's own saturation: a quotient above 448 in magnitude rounds to 448 or to the first
+// magnitude past it, which saturates to 448 -- the code of the clamped value either way.
 __device__ __forceinline__ uint32_t quant4(float a, float b, float c, float d, float s) {
-  const float lim = 448.0f;
-  a = fminf(fmaxf(__fdiv_rn(a, s), -lim), lim);
-  b = fminf(fmaxf(__fdiv_rn(b, s), -lim), lim);
-  c = fminf(fmaxf(__fdiv_rn(c, s), -lim), lim);
-  d = fminf(fmaxf(__fdiv_rn(d, s), -lim), lim);
-  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
-  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(a, s), __fdiv_rn(b, s)),
+                                               __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(c, s), __fdiv_rn(d, s)),
+                                               __NV_SATFINITE, __NV_E4M3);
   return (lo & 0xFFFFu) | (hi << 16);
 }
 
