@@ -43,23 +43,34 @@ __global__ void __launch_bounds__(256) pack_kernel(ConvParams p, PackPlan q, int
 //      values of its column (consecutive threads read consecutive positions: no bank conflicts),
 //      quantises them and stores the 16 codes with one 16-byte store into the padded
 //      channels-last copy.
-// The source is read in runs of kTileP elements per channel plane (2 KB from fp32). The item path
+// The source is read in runs of kTileP elements per channel plane (1.5 KB from fp32). The item path
 // it replaced (one thread = 16 channels x 4 pixels, 16 planes per thread) made the quantised step
 // of the large layer 450 us (fp32 x) and 409 us (bf16 x).
 // Blocks past the persistent ones run the remaining items (halo, weights by items) of the item
 // path, then one weight tile each (pack_w_tile).
-constexpr int kTileP = 512;
-constexpr int kTiledBlocksPerSm = 3;  // 2 stages of <= 32 KB each, <= 80 registers a thread
-
 template <int kType>
 __host__ __device__ constexpr int src_bytes() {
   return kType == kSrcF32 ? 4 : 2;  // fp32 or bfloat16
 }
+// Positions of a tile and blocks an SM: an fp32 x takes tiles of 384 positions, one per block, 4
+// blocks an SM (48 KB each, <= 64 registers a thread: the large layer's pack 73.9 -> 69.8 us
+// against 512 positions and 3 blocks); a bfloat16 x keeps 512 positions and 3 persistent blocks
+// with two 32 KB stages (<= 80 registers), which measured faster for it (60.2-63.3 against
+// 64.6 us with 384 positions and 4 blocks).
+template <int kType>
+__host__ __device__ constexpr int tile_positions() {
+  return kType == kSrcF32 ? 384 : 512;
+}
+template <int kType>
+__host__ __device__ constexpr int tiled_blocks_per_sm() {
+  return kType == kSrcF32 ? 4 : 3;
+}
 
 template <int kType, int kCT>
-__global__ void __launch_bounds__(256, kTiledBlocksPerSm) pack_x_tiled_kernel(
+__global__ void __launch_bounds__(256, tiled_blocks_per_sm<kType>()) pack_x_tiled_kernel(
     ConvParams p, PackPlan q, long long x_tiles, int tile_blocks, long long rest_blocks) {
   pdl_launch_dependents();  // the implicit GEMM may start its prologue while the pack runs
+  constexpr int kTileP = tile_positions<kType>();
   constexpr int kEB = src_bytes<kType>();
   constexpr int kRowBytes = kTileP * kEB;
   constexpr int kStageBytes = kCT * kRowBytes;
@@ -175,7 +186,7 @@ template <int kType, int kCT>
 static cudaError_t launch_tiled_ct(const ConvParams& p, const PackPlan& q, long long x_tiles,
                                    long long tile_blocks, long long rest_blocks,
                                    cudaStream_t stream) {
-  constexpr size_t stage = (size_t)kCT * kTileP * src_bytes<kType>();
+  constexpr size_t stage = (size_t)kCT * tile_positions<kType>() * src_bytes<kType>();
   static_assert(stage >= (size_t)kWTileBytes, "the weight tiles use the stages");
   const size_t smem = tile_blocks < x_tiles ? 2 * stage : stage;
   const unsigned blocks = (unsigned)(tile_blocks + rest_blocks + q.w_blocks);
@@ -454,17 +465,21 @@ cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream) {
     // an NCDHW x quantised on the way: the tiled transpose, plus blocks for the remaining items
     // and the weight tiles. bfloat16 x: persistent blocks over 32-channel tiles in two 32 KB
     // stages (large layer step 332 -> 323 us against one tile per block); fp32 x: one 32-channel
-    // tile (64 KB) per block (the two-stage forms measured 364 us with 16 channels, 399 us with
-    // 32 on one block per SM, against 362 us). The ring of the plain transposes (16 KB tiles of
+    // tile (48 KB) per block (two-stage forms of 512-position tiles measured 364 us with 16
+    // channels, 399 us with 32 on one block per SM, against 362 us for one 64 KB tile per block;
+    // 384-position tiles, 4 blocks an SM, then took the pack from 73.9 to 69.8 us). The ring of
+    // the plain transposes (16 KB tiles of
     // 32 channels x 128 / 256 positions, 4 blocks an SM, one 16-channel column of a position a
     // thread, a position's 32 bytes written by one instruction) measured slower here, bit-exact
     // all the same: the large layer's pack 74.5 -> 82.3 us from fp32, 61.7 -> 67.7 us from
     // bfloat16.
     const bool f32 = p.x_src_type == kSrcF32;
     const int ct = p.C % 32 == 0 ? 32 : 16;
-    const long long x_tiles = (long long)p.N * (p.C / ct) * ((dhw + kTileP - 1) / kTileP);
+    const long long tp = f32 ? tile_positions<kSrcF32>() : tile_positions<kSrcBf16>();
+    const long long x_tiles = (long long)p.N * (p.C / ct) * ((dhw + tp - 1) / tp);
     const long long tile_blocks =
-        f32 ? x_tiles : std::min<long long>(x_tiles, (long long)sms * kTiledBlocksPerSm);
+        f32 ? x_tiles
+            : std::min<long long>(x_tiles, (long long)sms * tiled_blocks_per_sm<kSrcBf16>());
     long long rest_blocks = (rest_items + 255) / 256;
     if (rest_blocks > cap) rest_blocks = cap;
     if (f32 && ct == 32)
