@@ -376,7 +376,8 @@ def measure_config(index: int, inp, dev, stream, flush, fp8_peak: float, hbm_pea
         "kernel_gbs": round(fig["alg_bytes"] / (k_ms * 1e-3) / 1e9, 1),
         "step_gbs": round(fig["alg_bytes"] / (s_ms * 1e-3) / 1e9, 1),
         "roofline": roof, "step_roofline_frac": step_roof["frac"],
-        "pack": {"alg_bytes": pbytes, "ms": round(p_ms, 5),
+        "pack": {"kernel": pack_kernel_name(shape, info["route"], False, False, False),
+                 "alg_bytes": pbytes, "ms": round(p_ms, 5),
                  "achieved_gbs": round(pbytes / (p_ms * 1e-3) / 1e9, 1),
                  "frac_of_hbm": round(pbytes / (p_ms * 1e-3) / 1e9 / hbm_peak, 4)},
         "steps": steps, "timing": "medians (means beside them: the event clock ticks in ~1 us "

@@ -56,6 +56,18 @@ def test_pack_bytes_per_route():
     assert bench.pack_alg_bytes(deep, True, 4, 2) == deep["x_bytes"] + 2 * 128 * 13824
 
 
+def test_pack_kernel_names_follow_the_library_rule():
+    # the tiled transpose takes an NCDHW x with W % 4 == 0, D*H*W*bytes % 16 == 0, C % 64 == 0
+    names = [bench.pack_kernel_name(s, 3, False, False, False) for s in synth.CONFIGS]
+    assert names == ["pack_kernel", "pack_kernel", "pack_x_transpose_kernel",
+                     "pack_x_transpose_kernel", "pack_x_transpose_kernel"]
+    large = synth.CONFIGS[4]
+    assert bench.pack_kernel_name(large, 3, False, True, False) == "pack_x_transpose_kernel"
+    assert bench.pack_kernel_name(large, 3, False, False, True) == "pack_kernel"  # weights only
+    assert bench.pack_kernel_name(large, 4, False, False, False) == "im2col_kernel"
+    assert bench.pack_kernel_name(large, 3, True, False, False).startswith("pack_x_tiled_kernel")
+
+
 def test_both_arms_print_the_same_config():
     # the reference arm (the CPU oracle) runs on the GPU arm's workload: one config builder serves
     # both, and nothing in it depends on the run (plan, buffer sizes and timings live elsewhere)
