@@ -279,6 +279,32 @@ def pack_alg_bytes(fig, packs_x: bool, route: int = 0, elem_bytes: int = 1) -> i
     return 2 * fig["w_bytes"] + (2 * fig["x_bytes"] if packs_x else 0)
 
 
+PACK_TILE_POSITIONS = 256  # the library rounds the first pack's positions up to this
+
+
+def overlap_pack_bytes(fig, shape, info, elem_bytes: int = 1):
+    """With the pack beside the GEMM (plan info overlap_planes > 0): the compulsory bytes of the
+    pack before the GEMM (the weights, and x's first planes read and written) and of the light
+    pack beside it (the rest of x read and written). None without the overlap."""
+    planes = info.get("overlap_planes", 0)
+    if not planes:
+        return None
+    hw, dhw_in = shape.H * shape.W, shape.D * shape.H * shape.W
+    q_a = min(dhw_in, -(-planes * hw // PACK_TILE_POSITIONS) * PACK_TILE_POSITIONS)
+    x_first = fig["x_bytes"] * q_a // dhw_in
+    return 2 * fig["w_bytes"] + 2 * x_first, 2 * (fig["x_bytes"] - x_first)
+
+
+def gemm_label(info) -> str:
+    k = "conv3d_fp8_tc_pair_kernel" if info["cta_pair"] == 2 else "conv3d_fp8_tc_kernel"
+    if info.get("overlap_planes", 0):
+        k += " (two launches) + pack_x_transpose_kernel beside the first"
+    if info["full_tiles"] < info["m_tiles"] * info["n_tiles"]:
+        # the timed window then also holds the reduction of the tiles split along K
+        k += " + splitk_reduce_kernel"
+    return k
+
+
 def roofline_of(fig, kernel_ms: float, fp8_peak: float, hbm_peak: float) -> dict:
     """Roofline of one launch: the slower of the dense tensor rate and HBM bandwidth for the
     algorithmic FLOP and bytes (x + w + y once), against the measured kernel time."""
@@ -358,14 +384,16 @@ def measure_config(index: int, inp, dev, stream, flush, fp8_peak: float, hbm_pea
     roof = roofline_of(fig, k_ms, fp8_peak, hbm_peak)
     step_roof = roofline_of(fig, s_ms, fp8_peak, hbm_peak)
     pbytes = pack_alg_bytes(fig, True, info["route"])
-    split = info["full_tiles"] < info["m_tiles"] * info["n_tiles"]
+    ov = overlap_pack_bytes(fig, shape, info)
+    if ov:
+        pbytes = ov[0]
     return {
         "workload": shape.name, "config_index": index,
         "plan": {k: info[k] for k in ("route", "cta_pair", "block_m", "block_n", "m_tiles",
-                                      "n_tiles", "full_tiles", "splits", "stages", "grid")},
+                                      "n_tiles", "full_tiles", "splits", "stages", "grid",
+                                      "overlap_planes", "overlap_units")},
         "gflop": round(fig["flop"] / 1e9, 4), "alg_bytes": fig["alg_bytes"],
-        "kernel": ("conv3d_fp8_tc_pair_kernel" if info["cta_pair"] == 2 else
-                   "conv3d_fp8_tc_kernel") + (" + splitk_reduce_kernel" if split else ""),
+        "kernel": gemm_label(info),
         "kernel_ms": round(k_ms, 5), "kernel_ms_min": round(min(kern), 5),
         "kernel_ms_mean": round(statistics.mean(kern), 5),
         "step_ms": round(s_ms, 5), "step_ms_min": round(min(step), 5),
@@ -379,7 +407,8 @@ def measure_config(index: int, inp, dev, stream, flush, fp8_peak: float, hbm_pea
         "pack": {"kernel": pack_kernel_name(shape, info["route"], False, False, False),
                  "alg_bytes": pbytes, "ms": round(p_ms, 5),
                  "achieved_gbs": round(pbytes / (p_ms * 1e-3) / 1e9, 1),
-                 "frac_of_hbm": round(pbytes / (p_ms * 1e-3) / 1e9 / hbm_peak, 4)},
+                 "frac_of_hbm": round(pbytes / (p_ms * 1e-3) / 1e9 / hbm_peak, 4),
+                 "beside_gemm_bytes": ov[1] if ov else 0},
         "steps": steps, "timing": "medians (means beside them: the event clock ticks in ~1 us "
                                   "steps); CUDA events on the launching stream; L2 flushed before "
                                   "every step",
@@ -414,7 +443,7 @@ def run_ours(args):
     make_plan = capi.conv3d_bf16_plan if bf16 else capi.conv3d_fp8_plan
     plan = make_plan(shape.N, shape.C, shape.D, shape.H, shape.W, shape.K, shape.T, shape.R,
                      shape.S, shape.stride, shape.pad, dev, input_layout=1 if channels_last else 0,
-                     route=ROUTES[args.route])
+                     route=ROUTES[args.route], overlap=args.overlap)
     info = capi.conv3d_fp8_get_info(plan)
     stream = torch.cuda.current_stream()
     x = x_lib.to(dev)
@@ -429,6 +458,8 @@ def run_ours(args):
     # reduction and the scale finalisation when x is quantised on the device)
     launches_per_step = 2 + (1 if info["full_tiles"] < info["m_tiles"] * info["n_tiles"] else 0)
     launches_per_step += 2 if quant else 0
+    # the pack beside the GEMM: a second GEMM launch and the light pack
+    launches_per_step += 2 if (info.get("overlap_planes", 0) and not quant) else 0
 
     def run(scale_x, scale_w):
         if quant:
@@ -572,7 +603,8 @@ def run_ours(args):
         plans = [plan] + [make_plan(shape.N, shape.C, shape.D, shape.H, shape.W, shape.K, shape.T,
                                     shape.R, shape.S, shape.stride, shape.pad, dev,
                                     input_layout=1 if channels_last else 0,
-                                    route=ROUTES[args.route]) for _ in range(nhost - 1)]
+                                    route=ROUTES[args.route], overlap=args.overlap)
+                          for _ in range(nhost - 1)]
         host_streams = [stream] + [torch.cuda.Stream() for _ in range(nhost - 1)]
         yhs = [torch.empty(y.shape, dtype=torch.bfloat16).pin_memory() for _ in range(nhost)]
 
@@ -667,11 +699,8 @@ def run_ours(args):
                 "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
                 "peak_source": f"{peaks_kind} copy bandwidth"}
     roof["traffic"] = traffic
-    roof["kernel"] = ("conv3d_fp8_tc_pair_kernel" if info["cta_pair"] == 2
-                      else "conv3d_fp8_tc_kernel")
-    if info["full_tiles"] < info["m_tiles"] * info["n_tiles"]:
-        # the timed window then also holds the reduction of the tiles split along K
-        roof["kernel"] += " + splitk_reduce_kernel"
+    ov_active = bool(info.get("overlap_planes", 0)) and not quant
+    roof["kernel"] = gemm_label(info if ov_active else dict(info, overlap_planes=0))
     roof["kernel_ms"] = round(mean_kern_ms, 5)
     roof["kernel_timing"] = (f"library events around the GEMM (+ reduce) on the launching stream, "
                              f"{K2} steps after the {K} timed ones")
@@ -686,6 +715,9 @@ def run_ours(args):
         p_bytes = x.numel() * x.element_size() + fig["npq"] * fig["k_gemm"]
     else:
         p_bytes = 2 * fig["w_bytes"] + x.numel() * x.element_size() + fig["x_bytes"]
+    ov = overlap_pack_bytes(fig, shape, info, 2 if bf16 else 1) if ov_active else None
+    if ov:
+        p_bytes = ov[0]
     p_ms = statistics.mean(pack_ms)
     pack = {"kernel": pack_kernel_name(shape, info["route"], quant, bf16, channels_last),
             "alg_bytes": int(p_bytes), "ms": round(p_ms, 5),
@@ -693,6 +725,11 @@ def run_ours(args):
             "peak": round(hbm_peak, 1), "frac": round(p_bytes / (p_ms * 1e-3) / 1e9 / hbm_peak, 4),
             "timing": "library events before the pack and before the main kernel, same steps as "
                       "kernel_ms"}
+    if ov:
+        pack["beside_gemm"] = {
+            "alg_bytes": int(ov[1]),
+            "note": "the other input planes, packed by the light pack_x_transpose_kernel beside "
+                    "the first GEMM launch: inside kernel_ms, not in this record's ms or bytes"}
 
     # ---- every workload's default e4m3 plan (NCDHW x), one record each
     per_config = None
@@ -748,7 +785,7 @@ def run_ours(args):
         "config": bench_config(shape, fig, args, dist.world),
         "plan": {k: info[k] for k in ("route", "cta_pair", "block_m", "block_n", "m_tiles",
                                       "n_tiles", "full_tiles", "splits", "stages", "grid",
-                                      "row_chk")},
+                                      "row_chk", "overlap_planes", "overlap_units")},
         "roofline": roof,
         "pack": pack,
         "per_config": per_config,
@@ -880,6 +917,9 @@ def main():
                     help="hand x over as fp32 / bf16 values: each step quantises it on the device")
     ap.add_argument("--route", choices=list(ROUTES), default="auto",
                     help="how A reaches the tensor cores: the library's choice, or one route forced")
+    ap.add_argument("--overlap", type=int, default=0,
+                    help="conv3d_fp8_options.overlap: 0 the library's choice, -1 never, P > 0 "
+                         "pack P input planes before the GEMM starts")
     ap.add_argument("--input-layout", choices=["ncdhw", "ndhwc"], default="ncdhw",
                     help="layout of x handed to the library (y is NCDHW either way)")
     args = ap.parse_args()

@@ -33,7 +33,8 @@ class Options(ctypes.Structure):
     _fields_ = [("splits", ctypes.c_int), ("block_n", ctypes.c_int), ("max_ctas", ctypes.c_int),
                 ("wait_timeout_ms", ctypes.c_int), ("debug_flags", ctypes.c_int),
                 ("route", ctypes.c_int), ("cta_pair", ctypes.c_int),
-                ("input_layout", ctypes.c_int), ("epilogue", ctypes.c_int)]
+                ("input_layout", ctypes.c_int), ("epilogue", ctypes.c_int),
+                ("overlap", ctypes.c_int)]
 
 
 class PlanInfo(ctypes.Structure):
@@ -45,7 +46,8 @@ class PlanInfo(ctypes.Structure):
                 ("row_chk", ctypes.c_int), ("grid", ctypes.c_int), ("sm_count", ctypes.c_int),
                 ("workspace_bytes", ctypes.c_size_t), ("route", ctypes.c_int),
                 ("cta_pair", ctypes.c_int), ("full_tiles", ctypes.c_int),
-                ("epilogue", ctypes.c_int)]
+                ("epilogue", ctypes.c_int), ("overlap_planes", ctypes.c_int),
+                ("overlap_units", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}

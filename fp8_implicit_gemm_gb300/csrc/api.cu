@@ -244,7 +244,52 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
   if (stages < (route == kRouteGrid ? 2 : 3)) return CONV3D_EUNSUPPORTED;
   long long grid = std::min<long long>(units, slots);
   if (pair) grid *= 2;  // two CTAs per unit
-  if (o.max_ctas < 0 || o.wait_timeout_ms < 0) return CONV3D_EINVAL;
+  if (o.max_ctas < 0 || o.wait_timeout_ms < 0 || o.overlap < -1) return CONV3D_EINVAL;
+
+  // Pack beside the GEMM (padded-grid route, one image, an NCDHW x taken by the tiled transpose):
+  // the first P input planes are packed before the GEMM starts on the tiles that read only those
+  // (whole waves), while a light pack (one block an SM, one 16 KB stage) copies the rest beside
+  // it; the remaining units run as a second launch. The pack block must fit beside a GEMM CTA:
+  // its shared memory in the SM's 228 KB (1 KB reserved a block), its 256 x 64 registers beside
+  // the GEMM's 320 x 128. Measured: a 64 MB copy that takes 45.7 us alone added 7.3 us to the
+  // large layer's run when it ran beside the GEMM on one block an SM.
+  long long ov_planes = 0, ov_units = 0;
+  {
+    const long long dhw_in = (long long)D * H * W;
+    const long long gemm_smem =
+        1024 + stages * stage_bytes + (2LL * stages + 5) * 8 + 16;  // the pair kernel's
+    const bool ov_ok = route == kRouteGrid && !x_cl && N == 1 && W % 4 == 0 &&
+                       (dhw_in * elem_bytes) % 16 == 0 && C_el % 64 == 0 &&
+                       dhw_in < (1LL << 31) && D >= 2 &&
+                       gemm_smem + 1024 + kPackLightSmem + 1024 <= kSmemPerSm;
+    const long long waves = full_tiles / slots;  // whole waves of whole tiles (a unit each)
+    if (o.overlap > 0 && !ov_ok) return CONV3D_EUNSUPPORTED;
+    if (ov_ok && (o.overlap > 0 || (o.overlap == 0 && waves >= 4))) {
+      // m tiles that read only the padded planes [0, pd + P): the last grid row of tile m plus
+      // the farthest tap lies below (pd + P) planes of the padded grid
+      const long long reach = (T - 1LL) * Hg * Wg + (R - 1LL) * Wg + (S - 1LL);
+      auto units_for = [&](long long P) {
+        const long long room = (pad[0] + P) * Hg * Wg - reach;
+        const long long m_ok = room > 0 ? room / block_m : 0;
+        const long long u = std::min(m_ok * n_tiles, full_tiles);
+        return (u / slots) * slots;  // whole waves
+      };
+      // by default about 2/9 of the waves go first: enough GEMM to hide the light pack of the
+      // rest, which runs at about a third of the copy bandwidth
+      const long long want = std::max<long long>(1, (2 * waves + 5) / 9) * slots;
+      long long P = o.overlap > 0 ? o.overlap : 0;
+      if (P == 0)
+        for (long long c = 1; c < D && P == 0; ++c)
+          if (units_for(c) >= want) P = c;
+      if (P > 0 && P < D && units_for(P) >= slots &&
+          round_up(P * H * W, kPackTilePositions) < dhw_in) {
+        ov_planes = P;
+        ov_units = units_for(P);
+      } else if (o.overlap > 0) {
+        return CONV3D_EUNSUPPORTED;
+      }
+    }
+  }
 
   Layout L{};
   L.xp_off = 0;
@@ -271,6 +316,8 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
   info->k_blocks_per_split = (int)kbps;
   info->full_tiles = (int)full_tiles;
   info->epilogue = epi_tma ? 2 : 1;
+  info->overlap_planes = (int)ov_planes;
+  info->overlap_units = (int)ov_units;
   info->stages = stages;
   info->row_chk = route == kRouteGrid ? 1 : (npq % block_m) != 0;
   info->grid = (int)grid;
@@ -604,6 +651,12 @@ conv3d_status plan_impl(int elem_bytes, conv3d_fp8_plan_t* out, int N, int C, in
     delete plan;
     return st;
   }
+  if (plan->info.overlap_planes > 0 &&
+      smem + 1024 + (size_t)kPackLightSmem + 1024 > (size_t)prop.sharedMemPerMultiprocessor) {
+    // this device's SM cannot hold a pack block beside a GEMM CTA: the pack runs whole first
+    plan->info.overlap_planes = 0;
+    plan->info.overlap_units = 0;
+  }
   *out = plan;
   return CONV3D_OK;
 }
@@ -648,13 +701,42 @@ conv3d_status run_impl(conv3d_fp8_plan_t plan, const void* x, const void* w,
     plan->wmap_src = w;
   }
   if (plan->ev_pack && cudaEventRecord(plan->ev_pack, s) != cudaSuccess) return CONV3D_ECUDA;
-  if (launch_pack(p, s) != cudaSuccess) return CONV3D_ECUDA;
-  if (plan->ev_begin && cudaEventRecord(plan->ev_begin, s) != cudaSuccess) return CONV3D_ECUDA;
-  if (launch_conv(p, plan->wmap, plan->xmap, plan->ymap, plan->info.row_chk != 0,
-                  plan->info.grid, s) != cudaSuccess)
-    return CONV3D_ECUDA;
-  if (has_split_tiles(p) && launch_splitk_reduce(p, plan->info.row_chk != 0, s) != cudaSuccess)
-    return CONV3D_ECUDA;
+  const bool row_chk = plan->info.row_chk != 0;
+  if (plan->info.overlap_planes > 0 && x_src_type == kSrcE4m3 && pack_transposes_x(p)) {
+    // The pack beside the GEMM, as one chain of programmatic dependent launches on the caller's
+    // stream: the first planes of x and the weights; the GEMM on the units that read only those
+    // (whole waves); the light pack of the other planes (one block an SM), launched once every
+    // CTA of that GEMM has passed its wait on the first pack and triggered its dependents, so
+    // that it only takes the room left beside them, and never waiting on that GEMM; the second
+    // GEMM launch on the remaining units, whose CTAs take the SMs the first launch frees and
+    // whose wait covers the light pack (the first pack completed before it began); the
+    // reduction of the split tiles.
+    const long long dhw_in = (long long)p.D * p.H * p.W;
+    const long long q_a = std::min<long long>(
+        dhw_in, round_up((long long)plan->info.overlap_planes * p.H * p.W, kPackTilePositions));
+    ConvParams pa = p, pb = p;
+    pa.num_units = plan->info.overlap_units;
+    pb.unit_base = pa.num_units;
+    pb.num_units = p.num_units - pa.num_units;
+    const int grid_a = std::min(plan->info.grid, 2 * pa.num_units);
+    const int grid_b = std::min(plan->info.grid, 2 * pb.num_units);
+    if (launch_pack_range(p, 0, q_a, true, false, s) != cudaSuccess) return CONV3D_ECUDA;
+    if (plan->ev_begin && cudaEventRecord(plan->ev_begin, s) != cudaSuccess) return CONV3D_ECUDA;
+    if (launch_conv(pa, plan->wmap, plan->xmap, plan->ymap, row_chk, grid_a, s) != cudaSuccess ||
+        launch_pack_range(p, q_a, dhw_in, false, true, s) != cudaSuccess ||
+        launch_conv(pb, plan->wmap, plan->xmap, plan->ymap, row_chk, grid_b, s) != cudaSuccess)
+      return CONV3D_ECUDA;
+    if (has_split_tiles(p) && launch_splitk_reduce(p, row_chk, s) != cudaSuccess)
+      return CONV3D_ECUDA;
+  } else {
+    if (launch_pack(p, s) != cudaSuccess) return CONV3D_ECUDA;
+    if (plan->ev_begin && cudaEventRecord(plan->ev_begin, s) != cudaSuccess) return CONV3D_ECUDA;
+    if (launch_conv(p, plan->wmap, plan->xmap, plan->ymap, row_chk, plan->info.grid, s) !=
+        cudaSuccess)
+      return CONV3D_ECUDA;
+    if (has_split_tiles(p) && launch_splitk_reduce(p, row_chk, s) != cudaSuccess)
+      return CONV3D_ECUDA;
+  }
   if (plan->ev_end && cudaEventRecord(plan->ev_end, s) != cudaSuccess) return CONV3D_ECUDA;
   return CONV3D_OK;
 }

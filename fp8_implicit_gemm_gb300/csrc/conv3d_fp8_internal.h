@@ -13,6 +13,8 @@ constexpr int kMmaK = 32;           // K of one tcgen05.mma kind::f8f6f4
 constexpr int kATileBytes = kBlockM * kBlockK;  // 16 KB
 constexpr int kNumThreads = 320;    // 4 epilogue warps, 4 A-loader warps, 1 TMA warp, 1 MMA warp
 constexpr int kSmemBudget = 200 * 1024;
+constexpr long long kSmemPerSm = 228 * 1024;    // shared memory of one SM
+constexpr long long kPackLightSmem = 16384;     // one stage of the light pack's ring
 constexpr int kMaxStages = 8;
 constexpr int kEpiStageBytes = 2 * 32 * kBlockM * 2;  // two bf16 boxes [32 columns][128 rows]
 
@@ -71,6 +73,8 @@ struct ConvParams {
   int block_m;           // M tile: 128 (one CTA) or 256 (CTA pair)
   int block_n;           // N tile (multiple of 32, <= 256)
   int m_tiles, n_tiles, k_blocks, splits, kb_per_split, num_units;
+  int unit_base;         // this launch runs units unit_base .. unit_base + num_units - 1 (a plan
+                         // that overlaps its pack with the GEMM runs the units in two launches)
   int full_tiles;        // tiles 0..full_tiles-1 are computed whole (one unit each, bf16 out);
                          // the others are split `splits` ways along K into fp32 partials
   int stages;
@@ -96,6 +100,14 @@ struct ConvParams {
 
 // Launchers (defined in the .cu files). Each returns the CUDA error of its launch.
 cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream);
+// The tiled transpose of x (e4m3 or bfloat16 NCDHW, W % 4 == 0, D*H*W*bytes % 16 == 0,
+// C % 64 == 0: pack_transposes_x) over the positions [q_lo, q_hi) of every image's volume (q_lo a
+// multiple of kPackTilePositions), with the weights and the remaining items when `whole` is set.
+// `light`: one block an SM with a single 16 KB stage, small enough to run beside a GEMM CTA.
+bool pack_transposes_x(const ConvParams& p);
+constexpr int kPackTilePositions = 256;  // every tile length of the transposes divides it
+cudaError_t launch_pack_range(const ConvParams& p, long long q_lo, long long q_hi, bool whole,
+                              bool light, cudaStream_t stream);
 cudaError_t launch_conv(const ConvParams& p, const CUtensorMap& wmap, const CUtensorMap& xmap,
                         const CUtensorMap& ymap, bool row_chk, int grid, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ConvParams& p, bool row_chk, cudaStream_t stream);

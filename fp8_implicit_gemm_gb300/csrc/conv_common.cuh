@@ -9,7 +9,8 @@
 namespace c3d {
 
 // One work unit: an M tile of block_m rows, an N tile of block_n channels and a slice [kb0, kb1)
-// of the K blocks. The first full_tiles units are whole tiles (part = -1); after them come the
+// of the K blocks. A launch's unit u is the plan's unit unit_base + u. The first full_tiles units
+// are whole tiles (part = -1); after them come the
 // remaining tiles, each split `splits` ways along K, split-fastest (part = index of the unit's
 // fp32 partial slice). Tiles are numbered n-tile fastest.
 struct Unit {
@@ -18,6 +19,7 @@ struct Unit {
 
 __device__ __forceinline__ Unit decode_unit(const ConvParams& p, int u) {
   Unit r;
+  u += p.unit_base;  // the launch's units are a contiguous range of the plan's
   if (u < p.full_tiles) {
     r.tile = u;
     r.split = 0;

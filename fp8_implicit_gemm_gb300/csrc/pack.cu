@@ -213,26 +213,32 @@ constexpr int kRingStages = 3;
 constexpr int kRingStageBytes = 16384;
 constexpr int kRingBlocksPerSm = 4;  // 3 stages of 16 KB each; <= 64 registers a thread
 
-template <int kEB, int kCG, int kRotRows, int kRotB, class TileFn>
+// The tiles cover the positions [q_lo, q_hi) of every image's volume (q_lo a multiple of the tile
+// length); the weight tiles and the remaining items are taken only when `whole` is set. kStages:
+// the ring's depth (3; or 1, no copies ahead: the light form that runs beside a GEMM CTA).
+template <int kEB, int kCG, int kRotRows, int kRotB, int kStages, class TileFn>
 __device__ __forceinline__ void pack_ring(const ConvParams& p, const PackPlan& q, long long x_tiles,
-                                          int ch, uint8_t* raw, TileFn&& tile_fn) {
+                                          long long q_lo, long long q_hi, bool whole, int ch,
+                                          uint8_t* raw, TileFn&& tile_fn) {
   constexpr int kRowB = kRingStageBytes / kCG;  // bytes of a stage row
   constexpr int kTP = kRowB / kEB;              // positions of a tile
   constexpr int kChunks = kRingStageBytes / 16 / 256;  // 16-byte copies per thread per tile
   static_assert(kRowB % 128 == 0 && kRotB % 16 == 0 && kChunks * 256 * 16 == kRingStageBytes,
                 "tile");
   static_assert(kRingStageBytes >= kWTileBytes, "a weight tile uses one stage");
+  static_assert(kStages == 1 || kStages == 3, "ring depth");
+  static_assert(kPackTilePositions % kTP == 0, "range starts fall on tile boundaries");
   const long long b = blockIdx.x, nb = gridDim.x;
-  const long long n_tiles = x_tiles + q.w_blocks;
+  const long long n_tiles = x_tiles + (whole ? q.w_blocks : 0);
   const long long dhw = (long long)p.D * p.H * p.W;
-  const long long pt = (dhw + kTP - 1) / kTP;
+  const long long pt = (q_hi - q_lo + kTP - 1) / kTP;
   const int cgn = ch / kCG;
   auto tile_at = [&](long long t, int& valid, long long& q0, int& n, int& c0) {
     const long long pi = t % pt, rest = t / pt;  // positions fastest, then channel groups, images
     n = (int)(rest / cgn);
     c0 = (int)(rest % cgn) * kCG;
-    q0 = pi * kTP;
-    valid = dhw - q0 < kTP ? (int)(dhw - q0) : kTP;  // valid * kEB is a multiple of 16
+    q0 = q_lo + pi * kTP;
+    valid = q_hi - q0 < kTP ? (int)(q_hi - q0) : kTP;  // valid * kEB is a multiple of 16
     return p.x + (((long long)n * ch + c0) * dhw + q0) * kEB;
   };
   auto issue = [&](long long t, uint8_t* stage) {  // cp.async copies of x tile t, no wait
@@ -249,18 +255,26 @@ __device__ __forceinline__ void pack_ring(const ConvParams& p, const PackPlan& q
             src + (long long)r * dhw * kEB + 16 * s, 16);
     }
   };
-  if (b < x_tiles) issue(b, raw);
-  cp_async_commit();
-  if (b + nb < x_tiles) issue(b + nb, raw + kRingStageBytes);
-  cp_async_commit();
+  if constexpr (kStages == 3) {
+    if (b < x_tiles) issue(b, raw);
+    cp_async_commit();
+    if (b + nb < x_tiles) issue(b + nb, raw + kRingStageBytes);
+    cp_async_commit();
+  }
   int sidx = 0;
   for (long long t = b; t < n_tiles; t += nb) {
     uint8_t* stage = raw + sidx * kRingStageBytes;
-    const long long t2 = t + 2 * nb;  // into the stage freed at the end of the last step
-    if (t2 < x_tiles) issue(t2, raw + ((sidx + 2) % kRingStages) * kRingStageBytes);
-    cp_async_commit();
-    cp_async_wait_group<2>();  // this thread's copies of tile t have landed
-    __syncthreads();           // and everyone else's
+    if constexpr (kStages == 3) {
+      const long long t2 = t + 2 * nb;  // into the stage freed at the end of the last step
+      if (t2 < x_tiles) issue(t2, raw + ((sidx + 2) % kRingStages) * kRingStageBytes);
+      cp_async_commit();
+      cp_async_wait_group<2>();  // this thread's copies of tile t have landed
+    } else {
+      if (t < x_tiles) issue(t, stage);
+      cp_async_commit();
+      cp_async_wait_group<0>();
+    }
+    __syncthreads();  // and everyone else's
     if (t >= x_tiles) {
       pack_w_tile(p, q, t - x_tiles, stage);  // nothing is in flight into this stage
     } else {
@@ -269,10 +283,11 @@ __device__ __forceinline__ void pack_ring(const ConvParams& p, const PackPlan& q
       tile_at(t, valid, q0, n, c0);
       tile_fn(static_cast<const uint8_t*>(stage), valid, q0, n, c0);
     }
-    __syncthreads();  // the stage is free for the copies three tiles on
-    sidx = (sidx + 1) % kRingStages;
+    __syncthreads();  // the stage is free for the copies kStages tiles on
+    sidx = (sidx + 1) % kStages;
   }
   cp_async_wait_all();
+  if (!whole) return;
   const PackCtx c = pack_ctx(p, q);
   const long long total = c.e3 + q.w_items;
   for (long long g = c.e1 + b * blockDim.x + threadIdx.x; g < total; g += nb * blockDim.x)
@@ -301,9 +316,9 @@ __device__ __forceinline__ long long xp_offset(const ConvParams& p, int n, long 
 // the words a warp (bfloat16: a half-warp) reads fall in 32 different banks. The item path this
 // replaced for these shapes held 16 x 16 bytes a thread in registers (100 registers, two blocks an
 // SM): 31.4 us for the large layer's x, against 18.5 us for each further image of the same size.
-template <int kEB, int kCG>
+template <int kEB, int kCG, int kStages>
 __global__ void __launch_bounds__(256, kRingBlocksPerSm) pack_x_transpose_kernel(
-    ConvParams p, PackPlan q, long long x_tiles) {
+    ConvParams p, PackPlan q, long long x_tiles, long long q_lo, long long q_hi, int whole) {
   pdl_launch_dependents();  // the implicit GEMM may start its prologue while the pack runs
   constexpr int kRowB = kRingStageBytes / kCG;
   constexpr int kChB = 16 / kEB;   // channels of a 16-byte block
@@ -314,7 +329,8 @@ __global__ void __launch_bounds__(256, kRingBlocksPerSm) pack_x_transpose_kernel
   extern __shared__ __align__(16) uint8_t raw[];  // [kRingStages][kCG][kRowB] bytes
   const int cb = threadIdx.x % kCB;  // this thread's channel block and position group
   const int qg = threadIdx.x / kCB;
-  pack_ring<kEB, kCG, kChB, kRotB>(p, q, x_tiles, p.C / kEB, raw,
+  pack_ring<kEB, kCG, kChB, kRotB, kStages>(p, q, x_tiles, q_lo, q_hi, whole != 0, p.C / kEB,
+                                             raw,
       [&](const uint8_t* stage, int valid, long long q0, int n, int c0) {
     if (4 * qg >= valid) return;
     // the group's word in each of its rows, at the rotated byte column
@@ -352,16 +368,63 @@ __global__ void __launch_bounds__(256, kRingBlocksPerSm) pack_x_transpose_kernel
   });
 }
 
-template <class K>
-static cudaError_t launch_ring(K kernel, const ConvParams& p, const PackPlan& q, long long x_tiles,
-                               long long blocks, cudaStream_t stream) {
+bool pack_transposes_x(const ConvParams& p) {
+  const long long dhw = (long long)p.D * p.H * p.W;
+  return p.xp != nullptr && !p.x_cl && p.x_src_type == kSrcE4m3 && p.W % 4 == 0 &&
+         (dhw * p.elem_bytes) % 16 == 0 && (p.C / p.elem_bytes) % 64 == 0 && dhw < (1LL << 31);
+}
+
+// The light form (kStages == 1) is launched as a programmatic dependent of the GEMM before it: it
+// starts once every CTA of that GEMM has triggered its dependents, and never waits for it.
+template <int kEB, int kCG, int kStages>
+static cudaError_t launch_transpose(const ConvParams& p, const PackPlan& q, long long x_tiles,
+                                    long long blocks, long long q_lo, long long q_hi, bool whole,
+                                    cudaStream_t stream) {
+  auto kernel = pack_x_transpose_kernel<kEB, kCG, kStages>;
   // one tile per block: only the first stage is used
-  const size_t smem = (size_t)kRingStageBytes * (blocks < x_tiles + q.w_blocks ? kRingStages : 1);
+  const long long n_tiles = x_tiles + (whole ? q.w_blocks : 0);
+  const size_t smem = (size_t)kRingStageBytes * (blocks < n_tiles ? kStages : 1);
   cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
-  kernel<<<(unsigned)blocks, 256, smem, stream>>>(p, q, x_tiles);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr{};
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = kStages == 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, p, q, x_tiles, q_lo, q_hi, whole ? 1 : 0);
+}
+
+cudaError_t launch_pack_range(const ConvParams& p, long long q_lo, long long q_hi, bool whole,
+                              bool light, cudaStream_t stream) {
+  const PackPlan q = pack_plan(p);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int ch = p.C / p.elem_bytes;  // channels
+  const int cg = p.elem_bytes == 1 && ch % 128 == 0 ? 128 : 64;
+  const long long tp = kRingStageBytes / cg / p.elem_bytes;
+  const long long x_tiles = q_hi > q_lo ? (long long)p.N * (ch / cg) * ((q_hi - q_lo + tp - 1) / tp)
+                                        : 0;
+  const long long n_tiles = x_tiles + (whole ? q.w_blocks : 0);
+  if (n_tiles == 0 && !whole) return cudaSuccess;
+  long long blocks = std::min<long long>(n_tiles, (long long)sms * (light ? 1 : kRingBlocksPerSm));
+  if (blocks < 1) blocks = 1;
+  if (light) {
+    if (p.elem_bytes == 2)
+      return launch_transpose<2, 64, 1>(p, q, x_tiles, blocks, q_lo, q_hi, whole, stream);
+    return cg == 128 ? launch_transpose<1, 128, 1>(p, q, x_tiles, blocks, q_lo, q_hi, whole, stream)
+                     : launch_transpose<1, 64, 1>(p, q, x_tiles, blocks, q_lo, q_hi, whole, stream);
+  }
+  if (p.elem_bytes == 2)
+    return launch_transpose<2, 64, 3>(p, q, x_tiles, blocks, q_lo, q_hi, whole, stream);
+  return cg == 128 ? launch_transpose<1, 128, 3>(p, q, x_tiles, blocks, q_lo, q_hi, whole, stream)
+                   : launch_transpose<1, 64, 3>(p, q, x_tiles, blocks, q_lo, q_hi, whole, stream);
 }
 
 // Direct route: the explicit A = im2col(x), [npq][kg] bytes with K_gemm in the caller's KCTRS
@@ -489,20 +552,10 @@ cudaError_t launch_pack(const ConvParams& p, cudaStream_t stream) {
       return launch_tiled_ct<kSrcBf16, 32>(p, q, x_tiles, tile_blocks, rest_blocks, stream);
     return launch_tiled_ct<kSrcBf16, 16>(p, q, x_tiles, tile_blocks, rest_blocks, stream);
   }
-  const int ch = p.C / p.elem_bytes;  // channels
-  if (q.x_items > 0 && !q.copy && p.x_src_type == kSrcE4m3 && p.W % 4 == 0 &&
-      (dhw * p.elem_bytes) % 16 == 0 && ch % 64 == 0 && dhw < (1LL << 31)) {
+  if (q.x_items > 0 && pack_transposes_x(p)) {
     // e4m3 bytes or the twin's bfloat16, NCDHW: the tiled transpose; the same blocks take the
     // weight tiles and the remaining items
-    const int cg = p.elem_bytes == 1 && ch % 128 == 0 ? 128 : 64;
-    const long long tp = kRingStageBytes / cg / p.elem_bytes;
-    const long long x_tiles = (long long)p.N * (ch / cg) * ((dhw + tp - 1) / tp);
-    const long long blocks =
-        std::min<long long>(x_tiles + q.w_blocks, (long long)sms * kRingBlocksPerSm);
-    if (p.elem_bytes == 2)
-      return launch_ring(pack_x_transpose_kernel<2, 64>, p, q, x_tiles, blocks, stream);
-    return cg == 128 ? launch_ring(pack_x_transpose_kernel<1, 128>, p, q, x_tiles, blocks, stream)
-                     : launch_ring(pack_x_transpose_kernel<1, 64>, p, q, x_tiles, blocks, stream);
+    return launch_pack_range(p, 0, dhw, true, false, stream);
   }
   const long long total = q.x_items + rest_items;
   long long item_blocks = (total + 255) / 256;

@@ -88,6 +88,16 @@ typedef struct {
                             guarded stores). 2 needs an output-position route (not the padded
                             grid) and dhw % 8 == 0 (EUNSUPPORTED otherwise); the map of y is
                             re-encoded on the host whenever y differs from the previous run's */
+    int overlap;         /* 0: the library chooses; -1: never; P > 0: pack the first P input
+                            planes, run the GEMM on the whole waves of tiles that read only
+                            those, and meanwhile pack the other planes beside it (one block an
+                            SM, next to the GEMM's CTAs), then run the remaining tiles as a second
+                            GEMM launch; all on the run's stream, chained by programmatic
+                            dependent launches (padded-grid route, one image, an NCDHW x that the
+                            tiled transpose takes, a GEMM tile that leaves room for a pack block;
+                            EUNSUPPORTED otherwise, or when P leaves no whole wave or no plane to
+                            pack beside the GEMM). By default it is taken for layers of at least
+                            four waves that meet those conditions */
 } conv3d_fp8_options;
 
 /* What a plan (or a would-be plan) decided. */
@@ -115,6 +125,9 @@ typedef struct {
                                  a split count in the options splits every tile; by default
                                  only the tiles of a mostly idle last wave are split */
     int epilogue;             /* 1: explicit guarded stores, 2: TMA stores (as in options) */
+    int overlap_planes;       /* input planes packed before the GEMM starts; 0: the pack runs
+                                 whole before a single GEMM launch (no overlap) */
+    int overlap_units;        /* units of the first GEMM launch (whole waves), with overlap */
 } conv3d_fp8_plan_info;
 
 /*

@@ -32,7 +32,9 @@ CASES = [
     ("channels-last x, grid", synth.CONFIGS[1], dict(input_layout=1), "e4m3"),
     ("fp32 x quantised in the pack", synth.CONFIGS[1], dict(), "fp32"),
     ("vae layer", synth.CONFIGS[2], dict(), "e4m3"),
-    ("large layer (tail split over 18 units)", synth.CONFIGS[4], dict(), "e4m3"),
+    ("large layer (tail split over 18 units, pack beside the GEMM)", synth.CONFIGS[4], dict(),
+     "e4m3"),
+    ("vae layer, pack beside the GEMM from plane 6", synth.CONFIGS[2], dict(overlap=6), "e4m3"),
 ]
 
 
@@ -73,7 +75,8 @@ def main() -> int:
             print(f"{'ok ' if good else 'BAD'} {name}: {n} elements, counts in [{lo}, {hi}], "
                   f"{n - ones} not written exactly once, NaN left {nan_left}, plan route "
                   f"{info['route']} pair {info['cta_pair']} epilogue {info['epilogue']} "
-                  f"splits {info['splits']} whole tiles {info['full_tiles']}", flush=True)
+                  f"splits {info['splits']} whole tiles {info['full_tiles']} overlap "
+                  f"{info['overlap_planes']}/{info['overlap_units']}", flush=True)
         finally:
             capi.conv3d_fp8_destroy(plan)
     return 1 if bad else 0

@@ -181,6 +181,38 @@ def test_describe_tail_split(lib):
     assert _describe(short, max_ctas=150)["splits"] == 1
 
 
+def test_describe_pack_beside_gemm(lib):
+    # the large layer (13 whole waves): the first 5 planes packed first, 3 waves of tiles read only
+    # those; the rest of x is packed beside them, the other units run as a second launch
+    i = _describe(synth.CONFIGS[4])
+    assert (i["overlap_planes"], i["overlap_units"]) == (5, 3 * 76)
+    s4 = synth.CONFIGS[4]
+    b = capi.conv3d_bf16_describe(s4.N, s4.C, s4.D, s4.H, s4.W, s4.K, s4.T, s4.R, s4.S,
+                                  s4.stride, s4.pad, 152)
+    assert (b["overlap_planes"], b["overlap_units"]) == (5, 3 * 76)
+    # off on request; a chosen plane count runs the whole waves of tiles those planes feed
+    assert _describe(s4, overlap=-1)["overlap_planes"] == 0
+    assert (_describe(s4, overlap=3)["overlap_units"], _describe(s4, overlap=16)["overlap_units"]) \
+        == (76, 11 * 76)
+    # none by default under four whole waves (the vae layer: 273 tiles on 76 pairs), where a plane
+    # count can still ask for it; never on the other routes, with a channels-last x or 2 images
+    assert _describe(synth.CONFIGS[2])["overlap_planes"] == 0
+    assert (_describe(synth.CONFIGS[2], overlap=6)["overlap_units"]) == 76
+    for cfg in (0, 1, 3):
+        assert _describe(synth.CONFIGS[cfg])["overlap_planes"] == 0
+    assert _describe(s4, input_layout=1)["overlap_planes"] == 0
+    two = synth.ConvShape(2, 256, 17, 90, 160, 256)
+    assert _describe(two)["overlap_planes"] == 0
+    # a plane count that feeds no whole wave, or leaves nothing to pack beside the GEMM, or a
+    # shape the overlap cannot take, is refused
+    for bad, opts in ((s4, dict(overlap=2)), (s4, dict(overlap=17)), (two, dict(overlap=5)),
+                      (s4, dict(overlap=5, input_layout=1)), (s4, dict(overlap=-2))):
+        st = capi.conv3d_fp8_describe_status(bad.N, bad.C, bad.D, bad.H, bad.W, bad.K, bad.T,
+                                             bad.R, bad.S, bad.stride, bad.pad, 152, **opts)
+        assert st == (capi.CONV3D_EINVAL if opts.get("overlap") == -2
+                      else capi.CONV3D_EUNSUPPORTED), (bad, opts, st)
+
+
 def test_describe_channels_last_input(lib):
     # the TMA routes read the caller's NDHWC x: no copy of x in the workspace; the gather route
     # still keeps its zero-padded copy

@@ -7,7 +7,7 @@ import pytest
 
 sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 import bench  # noqa: E402
-from fp8_implicit_gemm_gb300 import synth  # noqa: E402
+from fp8_implicit_gemm_gb300 import build, capi, synth  # noqa: E402
 
 
 def test_problem_figures_match_the_workloads():
@@ -54,6 +54,22 @@ def test_pack_bytes_per_route():
     # direct route: x read, the explicit im2col (npq x K_gemm elements) written, weights untouched
     assert bench.pack_alg_bytes(deep, True, 4) == deep["x_bytes"] + 128 * 13824
     assert bench.pack_alg_bytes(deep, True, 4, 2) == deep["x_bytes"] + 2 * 128 * 13824
+
+
+def test_overlap_splits_the_pack_bytes():
+    # the large layer packs 5 of 17 planes (rounded up to whole 256-position tiles) before the
+    # GEMM and the rest beside it: the two parts add up to the whole pack
+    build.build()  # host-only planning through the library (no GPU needed)
+    s = synth.CONFIGS[4]
+    fig = bench.problem_figures(s)
+    info = capi.conv3d_fp8_describe(s.N, s.C, s.D, s.H, s.W, s.K, s.T, s.R, s.S, s.stride,
+                                    s.pad, 152)
+    first, beside = bench.overlap_pack_bytes(fig, s, info)
+    assert first + beside == bench.pack_alg_bytes(fig, True, 3)
+    q_a = 72192  # 5 * 90 * 160 = 72000 positions, rounded up to a multiple of 256
+    assert first == 2 * fig["w_bytes"] + 2 * 256 * q_a
+    assert bench.overlap_pack_bytes(fig, s, dict(info, overlap_planes=0)) is None
+    assert "two launches" in bench.gemm_label(info)
 
 
 def test_pack_kernel_names_follow_the_library_rule():

@@ -27,7 +27,7 @@ def test_every_element_written_exactly_once():
                        capture_output=True, text=True, timeout=1200)
     print(r.stdout)
     assert r.returncode == 0, r.stdout[-4000:] + r.stderr[-4000:]
-    assert r.stdout.count("ok ") >= 12
+    assert r.stdout.count("ok ") >= 13
 
 
 def test_product_build_does_not_count():
