@@ -274,13 +274,29 @@ conv3d_status decide(int elem_bytes, int N, int C, int D, int H, int W, int K, i
         const long long u = std::min(m_ok * n_tiles, full_tiles);
         return (u / slots) * slots;  // whole waves
       };
-      // by default about 2/9 of the waves go first: enough GEMM to hide the light pack of the
-      // rest, which runs at about a third of the copy bandwidth
-      const long long want = std::max<long long>(1, (2 * waves + 5) / 9) * slots;
+      // By default, a cost model of measured rates: a wave of units takes about 1.13 x a tile's
+      // tensor-core cycles at 1.9 GHz (the large layer's kernel); the light pack moves about
+      // 2.5 TB/s of x beside the GEMM, the whole pack about 6 TB/s alone; the overlap costs
+      // about 8 us (the second launch's start, the light pack's pull on the GEMM). P is the
+      // fewest planes whose first launch outlasts the light pack of the rest by 10%, taken only
+      // when the pack time it saves exceeds that cost (the large layer: P = 5, 3 of 13 waves
+      // first; measured best of 4, 5 and 6; the vae layer, 3 waves, measured slower with it).
+      const double x_tr_bytes = 2.0 * (double)N * C * dhw_in;  // x read and its copy written
+      auto rest_frac = [&](long long P) {
+        return (double)(dhw_in - std::min(dhw_in, round_up(P * H * W, kPackTilePositions))) /
+               (double)dhw_in;
+      };
       long long P = o.overlap > 0 ? o.overlap : 0;
-      if (P == 0)
-        for (long long c = 1; c < D && P == 0; ++c)
-          if (units_for(c) >= want) P = c;
+      if (P == 0) {
+        for (long long c = 1; c < D && P == 0; ++c) {
+          const long long ua = units_for(c);
+          if (ua < slots) continue;
+          const double t_first_us = (double)(ua / slots) * (double)tile_cycles * 1.13 / 1900.0;
+          const double t_light_us = x_tr_bytes * rest_frac(c) / 2.5e6;
+          if (t_first_us >= 1.1 * t_light_us) P = c;
+        }
+        if (P > 0 && x_tr_bytes * rest_frac(P) / 6.0e6 < 8.0) P = 0;  // not worth its cost
+      }
       if (P > 0 && P < D && units_for(P) >= slots &&
           round_up(P * H * W, kPackTilePositions) < dhw_in) {
         ov_planes = P;

@@ -97,7 +97,9 @@ typedef struct {
                             tiled transpose takes, a GEMM tile that leaves room for a pack block;
                             EUNSUPPORTED otherwise, or when P leaves no whole wave or no plane to
                             pack beside the GEMM). By default it is taken for layers of at least
-                            four waves that meet those conditions */
+                            four waves that meet those conditions when a model of the measured
+                            rates finds a plane count whose first GEMM launch hides the rest of
+                            the pack and saves more than the overlap costs */
 } conv3d_fp8_options;
 
 /* What a plan (or a would-be plan) decided. */
