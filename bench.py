@@ -87,10 +87,12 @@ def main_kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def committed_traffic(workload: str, input_layout: str = "NCDHW"):
-    """DRAM bytes per launch of the main kernel from a committed ncu summary, if that summary was
-    taken on the current kernel source for this workload and input layout (line:
-    ``bench-traffic: {json}``; a line without "input_layout" is an NCDHW capture)."""
+def committed_traffic(workload: str, input_layout: str = "NCDHW", overlap_planes: int = 0):
+    """DRAM bytes of the main kernel in one step from a committed ncu summary, if that summary was
+    taken on the current kernel source for this workload, input layout and plane count of the
+    pack beside the GEMM (line: ``bench-traffic: {json}``; a line without "input_layout" is an
+    NCDHW capture, one without "overlap_planes" a single GEMM launch). With the overlap the two
+    GEMM launches of a step are summed ("dram_bytes_per_step")."""
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
@@ -106,8 +108,9 @@ def committed_traffic(workload: str, input_layout: str = "NCDHW"):
                     except ValueError:
                         continue
                     if (d.get("workload") == workload and d.get("source_sha256") == want and
-                            d.get("input_layout", "NCDHW") == input_layout):
-                        return d.get("dram_bytes_per_launch")
+                            d.get("input_layout", "NCDHW") == input_layout and
+                            d.get("overlap_planes", 0) == overlap_planes):
+                        return d.get("dram_bytes_per_step", d.get("dram_bytes_per_launch"))
     return None
 
 
@@ -686,7 +689,8 @@ def run_ours(args):
     t_flop = fig["flop"] / (fp8_peak * 1e12)
     t_hbm = fig["alg_bytes"] / (hbm_peak * 1e9)
     workload = shape.name + (" [bf16 inputs]" if bf16 else "")
-    traffic = committed_traffic(workload, "NDHWC" if channels_last else "NCDHW")
+    traffic = committed_traffic(workload, "NDHWC" if channels_last else "NCDHW",
+                                0 if quant else info.get("overlap_planes", 0))
     if t_flop >= t_hbm:
         achieved = fig["flop"] / (mean_kern_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp8_peak, 1),

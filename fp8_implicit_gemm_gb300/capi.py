@@ -190,7 +190,8 @@ def conv3d_fp8_strerror(status: int) -> str:
 def conv3d_fp8_plan(N, C, D, H, W, K, T, R, S, stride, pad, device=0, **options) -> int:
     """Create a plan; returns its handle. Keyword options (0 = the library's choice): splits,
     block_n, max_ctas, wait_timeout_ms, debug_flags, route, cta_pair, input_layout (1 = x is
-    NDHWC), epilogue (2 = TMA-store epilogue); see conv3d_fp8_options in include/conv3d_fp8.h."""
+    NDHWC), epilogue (2 = TMA-store epilogue), overlap (-1 = never pack beside the GEMM, P > 0 =
+    pack P input planes before it); see conv3d_fp8_options in include/conv3d_fp8.h."""
     lib = load()
     h = ctypes.c_void_p()
     o = _options(**options)
