@@ -213,6 +213,45 @@ def test_describe_pack_beside_gemm(lib):
                       else capi.CONV3D_EUNSUPPORTED), (bad, opts, st)
 
 
+def _overlap_reads_and_writes(shape, info):
+    """Padded planes the first GEMM launch reads (the last tile's last row plus the farthest tap)
+    and the first padded plane the light pack writes, from the plan's figures alone."""
+    pd, ph, pw = shape.pad
+    Hg, Wg = shape.H + 2 * ph, shape.W + 2 * pw
+    reach = (shape.T - 1) * Hg * Wg + (shape.R - 1) * Wg + (shape.S - 1)
+    last_m = (info["overlap_units"] - 1) // info["n_tiles"]
+    last_row = info["block_m"] * (last_m + 1) - 1 + reach
+    hw = shape.H * shape.W
+    q_a = min(shape.D * hw, -(-info["overlap_planes"] * hw // 256) * 256)
+    return last_row // (Hg * Wg), pd + q_a // hw, q_a
+
+
+@pytest.mark.parametrize("shape", [synth.CONFIGS[4], synth.CONFIGS[2],
+                                   synth.ConvShape(1, 128, 33, 128, 128, 128),
+                                   synth.ConvShape(1, 64, 20, 40, 256, 192)])
+def test_overlap_first_launch_reads_only_packed_planes(lib, shape):
+    # for every plane count the planner accepts: the first launch's tiles read only padded planes
+    # that the first pack completed, the light pack writes only planes past them, and the first
+    # launch holds whole waves of whole tiles
+    accepted = 0
+    for planes in range(1, shape.D):
+        st = capi.conv3d_fp8_describe_status(shape.N, shape.C, shape.D, shape.H, shape.W, shape.K,
+                                             shape.T, shape.R, shape.S, shape.stride, shape.pad,
+                                             152, overlap=planes)
+        if st != capi.CONV3D_OK:
+            assert st == capi.CONV3D_EUNSUPPORTED
+            continue
+        i = _describe(shape, overlap=planes)
+        read_upto, first_written, q_a = _overlap_reads_and_writes(shape, i)
+        # the padded planes below first_written are whole after the first pack (positions
+        # [0, q_a)); the light pack writes from position q_a on, in plane first_written or later
+        assert read_upto < first_written, (planes, read_upto, first_written)
+        assert i["overlap_units"] % (i["grid"] // 2) == 0 and i["overlap_units"] <= i["full_tiles"]
+        assert q_a % 256 == 0 and q_a < shape.D * shape.H * shape.W
+        accepted += 1
+    assert accepted > 0
+
+
 def test_describe_channels_last_input(lib):
     # the TMA routes read the caller's NDHWC x: no copy of x in the workspace; the gather route
     # still keeps its zero-padded copy
